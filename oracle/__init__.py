@@ -1,0 +1,212 @@
+"""fp64 CPU oracle for the paged MXFP4 index-K scorer (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: tests/, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package; the product path (``sparse_attention_mxfp4_gb300``) never does, and
+this package imports nothing from it.
+
+The arithmetic lives in ``mx4_oracle.c`` (plain C, fp64); this file only
+compiles it with gcc and marshals numpy arrays.  Every function states the
+passage it follows in the C source.
+
+Parity unpinned: only the cosine-against-bf16 context figure
+(``score(..., unquantized=True)``), which the pages report as quantisation
+context, not as a pass criterion.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mx4_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libmx4oracle.so")
+
+HEADS = 64
+DIM = 128
+PAGE = 128
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, OpenMP) into oracle/_build/."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-add, so every product and sum is
+    # rounded as written in the source.
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        c_i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.orc_e2m1_value.restype = ctypes.c_double
+        lib.orc_e2m1_value.argtypes = [ctypes.c_int]
+        lib.orc_e8m0_value.restype = ctypes.c_double
+        lib.orc_e8m0_value.argtypes = [ctypes.c_int]
+        lib.orc_e4m3_value.restype = ctypes.c_double
+        lib.orc_e4m3_value.argtypes = [ctypes.c_int]
+        lib.orc_bf16_value.restype = ctypes.c_double
+        lib.orc_bf16_value.argtypes = [ctypes.c_uint16]
+        lib.orc_e4m3_from_double.restype = ctypes.c_int
+        lib.orc_e4m3_from_double.argtypes = [ctypes.c_double]
+        lib.orc_bf16_to_e4m3.restype = ctypes.c_int
+        lib.orc_bf16_to_e4m3.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_to_e4m3_n.restype = None
+        lib.orc_bf16_to_e4m3_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+        lib.orc_e4m3_values_n.restype = None
+        lib.orc_e4m3_values_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
+        lib.orc_score.restype = ctypes.c_int
+        lib.orc_score.argtypes = [
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int64,
+            c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.orc_live_pairs.restype = ctypes.c_int64
+        lib.orc_live_pairs.argtypes = [
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, c_i64p, ctypes.c_int64]
+        _lib = lib
+        return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u8(a):
+    a = np.asarray(a)
+    assert a.dtype == np.uint8, a.dtype
+    return np.ascontiguousarray(a)
+
+
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+# ------------------------------------------------------------------ codecs --
+def e2m1_value(code: int) -> float:
+    """Value of a 4-bit e2m1 code (MXFP4 element; aiter #7061, "Format")."""
+    return _load().orc_e2m1_value(int(code))
+
+
+def e8m0_value(byte: int) -> float:
+    """2^(byte-127) (aiter #7061, "Format": value = e2m1 x 2^(byte-127))."""
+    return _load().orc_e8m0_value(int(byte))
+
+
+def e4m3_value(byte: int) -> float:
+    """Value of an e4m3 (fn) byte."""
+    return _load().orc_e4m3_value(int(byte))
+
+
+def bf16_value(bits: int) -> float:
+    return _load().orc_bf16_value(int(bits))
+
+
+def e4m3_from_double(x: float) -> int:
+    """RNE, satfinite rounding of a real to an e4m3 byte."""
+    return _load().orc_e4m3_from_double(float(x))
+
+
+def bf16_to_e4m3(bits) -> np.ndarray:
+    """Round bf16 bit patterns (uint16 array) to e4m3 bytes, RNE-satfinite
+    (aiter #7061, "Kernels": a bf16 query is rounded to e4m3)."""
+    a = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    out = np.empty(a.shape, dtype=np.uint8)
+    _load().orc_bf16_to_e4m3_n(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def e4m3_values(codes) -> np.ndarray:
+    a = _u8(codes)
+    out = np.empty(a.shape, dtype=np.float64)
+    _load().orc_e4m3_values_n(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+# ------------------------------------------------------------------ scorer --
+def score(*, decode: bool, q: np.ndarray, q_is_e4m3: bool, k_data: np.ndarray,
+          k_scale: np.ndarray, k_data_page_stride: int, k_scale_page_stride: int,
+          block_table: np.ndarray, block_table_stride: int, seq_lens,
+          max_seq_len: int, sm_scale: float, cu_seqlens_q=None, prefix_lens=None,
+          rows=None, want_scores: bool = True, want_logits: bool = False,
+          unquantized: bool = False, num_pool_pages: int = 0,
+          num_threads: int = 0):
+    """Block scores and/or per-token logits for the listed query rows, fp64.
+
+    ``q``: [rows_total, 64, 128] uint16 (bf16 bits) or uint8 (e4m3).
+    ``k_data`` / ``k_scale``: flat uint8 buffers; page p's data starts at byte
+    ``p * k_data_page_stride`` and its scales at ``p * k_scale_page_stride``.
+    ``block_table``: int32, request b's page j at ``b * block_table_stride + j``.
+    Returns ``(scores, logits)``, each ``None`` unless requested;
+    scores [n_rows, 64, ceil(max_seq_len/128)], logits [n_rows, 64, max_seq_len].
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q)
+    if q_is_e4m3:
+        assert q.dtype == np.uint8
+    else:
+        assert q.dtype == np.uint16
+    k_data = _u8(k_data).reshape(-1)
+    k_scale = _u8(k_scale).reshape(-1)
+    bt = _i32(block_table).reshape(-1)
+    sl = _i32(seq_lens)
+    cu = _i32(cu_seqlens_q)
+    pl = _i32(prefix_lens)
+    num_seqs = int(sl.shape[0])
+    if rows is None:
+        n_total = num_seqs if decode else int(cu[-1])
+        rows = np.arange(n_total, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    P = (max_seq_len + PAGE - 1) // PAGE
+    sc = np.empty((n, HEADS, P), dtype=np.float64) if want_scores else None
+    lg = np.empty((n, HEADS, max_seq_len), dtype=np.float64) if want_logits else None
+    st = lib.orc_score(
+        1 if decode else 0, _ptr(q), 1 if q_is_e4m3 else 0, 1 if unquantized else 0,
+        _ptr(k_data), _ptr(k_scale), int(k_data_page_stride), int(k_scale_page_stride),
+        _ptr(bt), int(block_table_stride), _ptr(cu), _ptr(sl), _ptr(pl),
+        num_seqs, int(max_seq_len), float(sm_scale), int(num_pool_pages),
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+        _ptr(sc), _ptr(lg), int(num_threads))
+    if st != 0:
+        raise ValueError(f"oracle rejected the inputs (status {st})")
+    return sc, lg
+
+
+def live_pairs(*, decode: bool, seq_lens, max_seq_len: int, cu_seqlens_q=None,
+               prefix_lens=None, rows=None) -> int:
+    """Number of live (row, token) pairs under the causal limit."""
+    lib = _load()
+    sl = _i32(seq_lens)
+    cu = _i32(cu_seqlens_q)
+    pl = _i32(prefix_lens)
+    if rows is None:
+        n_total = sl.shape[0] if decode else int(cu[-1])
+        rows = np.arange(n_total, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    return int(lib.orc_live_pairs(1 if decode else 0, _ptr(cu), _ptr(sl), _ptr(pl),
+                                  int(sl.shape[0]), int(max_seq_len),
+                                  rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+                                  rows.shape[0]))

@@ -1,0 +1,326 @@
+/*
+ * mx4_oracle.c -- plain, slow fp64 CPU oracle for the paged MXFP4 index-K scorer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file: it is used by tests/, by __graft_entry__.smoke() and by the
+ * cpu_baseline / --impl reference legs of bench.py.  It shares no code, header,
+ * table or constant with the CUDA library.
+ *
+ * What it computes, and where the sources say so:
+ *
+ *   aiter #7061 "MiniMax-M3 index score: MXFP4 index-cache prefill scorer",
+ *   section "Format": MXFP4 is e2m1 data with one e8m0 scale per 32 elements;
+ *   a page of 128 tokens is [128 x 64 B data][128 x 4 B scale] = 8704 B, read
+ *   through two views k_data [pages,128,64] and k_scale [pages,128,4] that
+ *   each carry their own byte page stride.  The same section fixes the value
+ *   of a cached element as  e2m1 x 2^(byte-127)  and the block score as the
+ *   max over live tokens of the dot with Q.
+ *
+ *   Same page, section "Kernels": a bf16 query is rounded to e4m3 before the
+ *   product; an e4m3 query is used as stored; the causal mask is shared with
+ *   the fp8 scorer.
+ *
+ *   aiter #5518 "[FlyDSL][gfx950] explicit page strides and 64-bit rebase for
+ *   FP4 MQA logits", section "Summary": the block table stride is in int32
+ *   elements and physical page offsets are 64-bit; the per-token ("MQA
+ *   logits") output keeps -inf for masked tokens (section "Correctness").
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *   - nibble order: element 2i is the low nibble of byte i, 2i+1 the high one;
+ *   - scale byte g of a token covers elements 32g .. 32g+31;
+ *   - token i of a page sits at byte i*64 of the data view, i*4 of the scale view;
+ *   - bf16 -> e4m3 is round-to-nearest-even with saturation to +-448
+ *     ("satfinite"), signed zero kept, subnormals kept;
+ *   - live limit of a prefill row: L = min(seq_len, prefix_len + row_pos + 1);
+ *     a decode row: L = seq_len;
+ *   - pages j with 128*j >= L score -inf (also pages past the request's own
+ *     length but below ceil(max_seq_len/128));
+ *   - sm_scale multiplies every token's dot before the max.
+ *
+ * Arithmetic is fp64 throughout.  With e4m3 Q (multiples of 2^-9, |q|<=448),
+ * e2m1 K (multiples of 1/2, |k|<=6) and scale bytes >= 122, every product is a
+ * multiple of 2^-15 below 2^12 in magnitude and a 128-term sum is exact in fp64,
+ * so for such inputs the pre-scale dot is the exact real number.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_HEADS 64
+#define ORC_DIM 128
+#define ORC_PAGE 128
+#define ORC_TOKEN_DATA_BYTES 64
+#define ORC_TOKEN_SCALE_BYTES 4
+
+/* ---------------------------------------------------------------- codecs -- */
+
+/* e2m1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no inf/NaN.
+ * Magnitudes of codes 0..7, from the format definition. */
+static const double ORC_E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1_value(int code)
+{
+    double m = ORC_E2M1_MAG[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* e8m0: the byte is a biased power-of-two exponent, value 2^(byte-127).
+ * Bytes 0 and 255 are outside the contract (aiter #7061, "Format"). */
+double orc_e8m0_value(int byte)
+{
+    return ldexp(1.0, byte - 127);
+}
+
+/* e4m3 (fn variant): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
+ * subnormal step 2^-9, largest finite 448, S.1111.111 is NaN, no infinity. */
+double orc_e4m3_value(int byte)
+{
+    int s = (byte >> 7) & 1, e = (byte >> 3) & 15, m = byte & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);
+    else
+        v = ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+double orc_bf16_value(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a real value to e4m3: nearest representable value, ties to the
+ * even mantissa, magnitudes at or above 448 saturate to 448, sign of zero
+ * kept.  NaN maps to 0x7F (never produced by the generators). */
+int orc_e4m3_from_double(double x)
+{
+    int sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x), q, n, fl, frac, r, v;
+    int e, E, mant;
+
+    if (isnan(x))
+        return 0x7F;
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a == 0.0)
+        return sign;
+    frexp(a, &e);          /* a = f * 2^e with f in [0.5, 1) */
+    E = e - 1;             /* floor(log2(a)) */
+    if (E < -6)
+        E = -6;            /* below the normal range the quantum stays 2^-9 */
+    q = ldexp(1.0, E - 3); /* spacing of e4m3 values in this binade */
+    n = a / q;             /* exact: q is a power of two */
+    fl = floor(n);
+    frac = n - fl;
+    if (frac > 0.5)
+        r = fl + 1.0;
+    else if (frac < 0.5)
+        r = fl;
+    else
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    v = r * q;
+    if (v == 0.0)
+        return sign;
+    /* encode v */
+    frexp(v, &e);
+    E = e - 1;
+    if (E < -6) {
+        mant = (int)ldexp(v, 9); /* subnormal: v = m * 2^-9 */
+        return sign | mant;
+    }
+    mant = (int)(ldexp(v, 3 - E)) - 8;
+    return sign | ((E + 7) << 3) | mant;
+}
+
+int orc_bf16_to_e4m3(uint16_t bits)
+{
+    return orc_e4m3_from_double(orc_bf16_value(bits));
+}
+
+/* Vector helpers for the Python side. */
+void orc_bf16_to_e4m3_n(const uint16_t *in, uint8_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (uint8_t)orc_bf16_to_e4m3(in[i]);
+}
+
+void orc_e4m3_values_n(const uint8_t *in, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_value(in[i]);
+}
+
+/* ----------------------------------------------------------- the scorer -- */
+
+/* Value of element d of token i in physical page p: e2m1 code times its
+ * group's e8m0 scale (aiter #7061, "Format"). */
+static double orc_k_value(const uint8_t *k_data, const uint8_t *k_scale,
+                          int64_t sd, int64_t ss, int64_t p, int i, int d)
+{
+    uint8_t byte = k_data[p * sd + (int64_t)i * ORC_TOKEN_DATA_BYTES + d / 2];
+    int code = (d & 1) ? (byte >> 4) : (byte & 15);
+    uint8_t sbyte = k_scale[p * ss + (int64_t)i * ORC_TOKEN_SCALE_BYTES + d / 32];
+    return orc_e2m1_value(code) * orc_e8m0_value(sbyte);
+}
+
+/* Query value of (row, head, d).  mode 0: the e4m3 value the scorer uses
+ * (bf16 rounded to e4m3, or the stored e4m3 byte).  mode 1: the unrounded
+ * bf16 value, used only for the cosine context figure. */
+static double orc_q_value(const void *q, int q_is_e4m3, int unquantized,
+                          int64_t row, int h, int d)
+{
+    int64_t idx = (row * ORC_HEADS + h) * ORC_DIM + d;
+    if (q_is_e4m3)
+        return orc_e4m3_value(((const uint8_t *)q)[idx]);
+    if (unquantized)
+        return orc_bf16_value(((const uint16_t *)q)[idx]);
+    return orc_e4m3_value(orc_bf16_to_e4m3(((const uint16_t *)q)[idx]));
+}
+
+/* Request that owns global query row r (prefill), or -1. */
+static int orc_request_of_row(const int32_t *cu, int num_seqs, int64_t r)
+{
+    for (int b = 0; b < num_seqs; ++b)
+        if (cu[b] <= r && r < cu[b + 1])
+            return b;
+    return -1;
+}
+
+/* Live limit of a row: tokens t < L are visible to it. */
+int64_t orc_live_limit(int decode, const int32_t *cu, const int32_t *seq_lens,
+                       const int32_t *prefix_lens, int b, int64_t r)
+{
+    int64_t seq = seq_lens[b];
+    int64_t lim;
+    if (decode)
+        return seq;
+    lim = (int64_t)prefix_lens[b] + (r - cu[b]) + 1;
+    return lim < seq ? lim : seq;
+}
+
+/*
+ * Score the query rows listed in rows[0..n_rows).
+ *
+ * decode = 0: prefill.  Rows are global rows of q; cu_seqlens_q[num_seqs+1]
+ *             assigns them to requests; prefix_lens gives each request's
+ *             cached prefix.
+ * decode = 1: decode.   Row r is request r (one query row each); cu_seqlens_q
+ *             and prefix_lens are ignored and L = seq_len.
+ *
+ * scores (optional): [n_rows, 64, P] with P = ceil(max_seq_len/128):
+ *     max over live t in page j of sm_scale * sum_d Q[r,h,d] * K[t,d], else -inf.
+ * logits (optional): [n_rows, 64, max_seq_len]:
+ *     sm_scale * sum_d Q[r,h,d] * K[t,d] for t < L, else -inf.
+ *
+ * Returns 0, or -1 if a row is not in any request, -2 if a live token maps
+ * to a page id outside [0, num_pool_pages), -3 on a bad argument.
+ */
+int orc_score(int decode, const void *q, int q_is_e4m3, int unquantized,
+              const uint8_t *k_data, const uint8_t *k_scale,
+              int64_t k_data_page_stride, int64_t k_scale_page_stride,
+              const int32_t *block_table, int64_t block_table_stride,
+              const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+              const int32_t *prefix_lens, int num_seqs, int max_seq_len,
+              double sm_scale, int64_t num_pool_pages,
+              const int64_t *rows, int64_t n_rows,
+              double *scores, double *logits, int num_threads)
+{
+    const int64_t P = ((int64_t)max_seq_len + ORC_PAGE - 1) / ORC_PAGE;
+    int status = 0;
+
+    if (max_seq_len < 0 || num_seqs < 0 || n_rows < 0 || !q || !k_data || !k_scale
+        || !block_table || !seq_lens || (!decode && (!cu_seqlens_q || !prefix_lens)))
+        return -3;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t ri = 0; ri < n_rows; ++ri) {
+        int64_t r = rows[ri];
+        int b = decode ? (int)r : orc_request_of_row(cu_seqlens_q, num_seqs, r);
+        int64_t L, t;
+        double qv[ORC_HEADS][ORC_DIM], kv[ORC_DIM];
+
+        for (int h = 0; h < ORC_HEADS; ++h) {
+            if (scores)
+                for (int64_t j = 0; j < P; ++j)
+                    scores[(ri * ORC_HEADS + h) * P + j] = -INFINITY;
+            if (logits)
+                for (t = 0; t < max_seq_len; ++t)
+                    logits[(ri * ORC_HEADS + h) * (int64_t)max_seq_len + t] = -INFINITY;
+        }
+        if (b < 0 || b >= num_seqs) {
+#pragma omp atomic write
+            status = -1;
+            continue;
+        }
+        L = orc_live_limit(decode, cu_seqlens_q, seq_lens, prefix_lens, b, r);
+        if (L > max_seq_len)
+            L = max_seq_len;
+        for (int h = 0; h < ORC_HEADS; ++h)
+            for (int d = 0; d < ORC_DIM; ++d)
+                qv[h][d] = orc_q_value(q, q_is_e4m3, unquantized, r, h, d);
+
+        for (t = 0; t < L; ++t) {
+            int64_t j = t / ORC_PAGE;
+            int i = (int)(t % ORC_PAGE);
+            int64_t p = block_table[(int64_t)b * block_table_stride + j];
+            if (p < 0 || (num_pool_pages > 0 && p >= num_pool_pages)) {
+#pragma omp atomic write
+                status = -2;
+                break;
+            }
+            for (int d = 0; d < ORC_DIM; ++d)
+                kv[d] = orc_k_value(k_data, k_scale, k_data_page_stride,
+                                    k_scale_page_stride, p, i, d);
+            for (int h = 0; h < ORC_HEADS; ++h) {
+                double dot = 0.0, val;
+                for (int d = 0; d < ORC_DIM; ++d)
+                    dot += qv[h][d] * kv[d];
+                val = sm_scale * dot;
+                if (logits)
+                    logits[(ri * ORC_HEADS + h) * (int64_t)max_seq_len + t] = val;
+                if (scores) {
+                    double *s = &scores[(ri * ORC_HEADS + h) * P + j];
+                    if (val > *s)
+                        *s = val;
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/* Number of live (row, token) pairs over the listed rows: the causal mask
+ * alone, for closed-form checks of the live limit. */
+int64_t orc_live_pairs(int decode, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                       const int32_t *prefix_lens, int num_seqs, int max_seq_len,
+                       const int64_t *rows, int64_t n_rows)
+{
+    int64_t total = 0;
+    for (int64_t ri = 0; ri < n_rows; ++ri) {
+        int64_t r = rows[ri];
+        int b = decode ? (int)r : orc_request_of_row(cu_seqlens_q, num_seqs, r);
+        int64_t L;
+        if (b < 0 || b >= num_seqs)
+            continue;
+        L = orc_live_limit(decode, cu_seqlens_q, seq_lens, prefix_lens, b, r);
+        if (L > max_seq_len)
+            L = max_seq_len;
+        if (L > 0)
+            total += L;
+    }
+    return total;
+}

@@ -1,0 +1,340 @@
+"""Seeded synthetic inputs for the paged MXFP4 index-K scorer.
+
+This module only draws random inputs and lays them out in memory; it holds
+none of the scorer's arithmetic and imports neither the CUDA binding nor the
+oracle.  Tests, ``bench.py`` and ``__graft_entry__`` use it to feed both sides
+the same bytes.
+
+Distributions follow the workloads the pages measure on (aiter #7061,
+"Performance": random K data, e8m0 bytes in [122, 127]; the wide-scale check
+of the same page, "Format", uses bytes 100..150):
+
+* Q bf16: N(0, 1) per element, rounded to bf16 by torch.
+* Q e4m3 (MTP workload only): N(0, 1) cast to float8_e4m3fn by torch (round to
+  nearest even; |x| < 448 always holds for these draws).  This is input
+  synthesis, not the scorer's query rounding.
+* K data: uniform random bytes, i.e. all 16 e2m1 codes in both nibbles.
+* K scales: uniform integers in [lo, hi] per (token, 32-element group).
+* Bytes of tokens past a request's ``seq_len`` inside its last page are random
+  garbage, scale bytes 0 and 255 included.
+* Block-table entries past a request's last page are filled with -1.
+* sm_scale = fp32(1/sqrt(128)).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+HEADS = 64
+DIM = 128
+PAGE = 128
+DATA_BYTES = PAGE * DIM // 2      # 8192: 128 tokens x 64 B of e2m1 codes
+SCALE_BYTES = PAGE * DIM // 32    # 512: 128 tokens x 4 e8m0 bytes
+PAGE_BYTES = DATA_BYTES + SCALE_BYTES  # 8704
+
+SM_SCALE = float(np.float32(1.0 / math.sqrt(DIM)))
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    decode: bool
+    q: torch.Tensor                 # [rows, 64, 128] bfloat16, or uint8 e4m3 bytes
+    q_is_e4m3: bool
+    pages_data: torch.Tensor        # [U, 128, 64] uint8: contents of the used pages
+    pages_scale: torch.Tensor       # [U, 128, 4] uint8
+    page_ids: torch.Tensor          # [U] int64: physical id of each used page
+    num_pool_pages: int
+    layout: str                     # "single" (8704 B pages) or "split"
+    k_data_page_stride: int         # bytes
+    k_scale_page_stride: int        # bytes
+    block_table: torch.Tensor       # [B, width] int32 physical ids (-1 padded)
+    seq_lens: torch.Tensor          # [B] int32
+    cu_seqlens_q: Optional[torch.Tensor]   # [B+1] int32 (prefill)
+    prefix_lens: Optional[torch.Tensor]    # [B] int32 (prefill)
+    max_query_len: int
+    max_seq_len: int
+    sm_scale: float = SM_SCALE
+    description: str = ""
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def total_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_out_pages(self) -> int:
+        return (self.max_seq_len + PAGE - 1) // PAGE
+
+    @property
+    def block_table_stride(self) -> int:
+        return int(self.block_table.shape[1])
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return g
+
+
+def _q_bf16(g, rows):
+    return torch.randn((rows, HEADS, DIM), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _q_e4m3(g, rows):
+    x = torch.randn((rows, HEADS, DIM), generator=g, dtype=torch.float32).clamp_(-448.0, 448.0)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _page_contents(g, n_pages, scale_lo, scale_hi):
+    data = torch.randint(0, 256, (n_pages, PAGE, DIM // 2), generator=g, dtype=torch.uint8)
+    scale = torch.randint(scale_lo, scale_hi + 1, (n_pages, PAGE, DIM // 32),
+                          generator=g, dtype=torch.uint8)
+    return data, scale
+
+
+def _garbage_tails(g, bt, seq_lens, page_index, pages_data, pages_scale):
+    """Fill bytes of tokens past each request's end (inside its last page)
+    with random garbage, including e8m0 bytes 0 and 255."""
+    for b in range(bt.shape[0]):
+        s = int(seq_lens[b])
+        if s % PAGE == 0 or s == 0:
+            continue
+        pid = int(bt[b, s // PAGE])
+        u = page_index[pid]
+        tail = PAGE - s % PAGE
+        pages_data[u, PAGE - tail:] = torch.randint(0, 256, (tail, DIM // 2), generator=g,
+                                                    dtype=torch.uint8)
+        sc = torch.randint(0, 256, (tail, DIM // 32), generator=g, dtype=torch.uint8)
+        sc[0, 0] = 0
+        sc[-1, -1] = 255
+        pages_scale[u, PAGE - tail:] = sc
+
+
+def make_workload(name, *, seed, q_lens, seq_lens, prefix_lens=None, decode=False,
+                  pool_pages, q_e4m3=False, scale_lo=122, scale_hi=127,
+                  layout="single", k_data_page_stride=None, k_scale_page_stride=None,
+                  page_id_range=None, forced_page_ids=(), bt_width=None,
+                  description="") -> Workload:
+    """Generic seeded workload.
+
+    ``q_lens`` (prefill) / one row per request (decode), ``seq_lens`` and
+    ``prefix_lens`` per request.  Physical pages are distinct and drawn from
+    ``page_id_range`` (default the whole pool) by a seeded permutation.
+    """
+    g = _gen(seed)
+    B = len(seq_lens)
+    seq_lens_t = torch.tensor(seq_lens, dtype=torch.int32)
+    if decode:
+        q_lens = [1] * B
+    rows = int(sum(q_lens))
+    q = _q_e4m3(g, rows) if q_e4m3 else _q_bf16(g, rows)
+    max_seq_len = int(max(seq_lens)) if B else 0
+    pages_per_req = [(s + PAGE - 1) // PAGE for s in seq_lens]
+    width = bt_width if bt_width is not None else max(1, (max_seq_len + PAGE - 1) // PAGE)
+    n_used = int(sum(pages_per_req))
+    lo, hi = page_id_range if page_id_range is not None else (0, pool_pages)
+    assert hi - lo >= n_used and hi <= pool_pages
+    forced = [int(p) for p in forced_page_ids]
+    perm = (torch.randperm(hi - lo, generator=g) + lo).tolist()
+    ids = forced + [p for p in perm if p not in set(forced)]
+    ids = ids[:n_used]
+    # shuffle so forced ids do not always land on request 0's first page
+    order = torch.randperm(n_used, generator=g).tolist()
+    ids = [ids[i] for i in order]
+    bt = torch.full((B, width), -1, dtype=torch.int32)
+    k = 0
+    for b in range(B):
+        for j in range(pages_per_req[b]):
+            bt[b, j] = ids[k]
+            k += 1
+    page_ids = torch.tensor(ids, dtype=torch.int64)
+    pages_data, pages_scale = _page_contents(g, n_used, scale_lo, scale_hi)
+    page_index = {int(p): u for u, p in enumerate(ids)}
+    _garbage_tails(g, bt, seq_lens, page_index, pages_data, pages_scale)
+    if layout == "single":
+        sd = ss = k_data_page_stride or PAGE_BYTES
+    else:
+        sd = k_data_page_stride or DATA_BYTES
+        ss = k_scale_page_stride or SCALE_BYTES
+    if decode:
+        cu = None
+        pl = None
+        max_q = 1
+    else:
+        cu = torch.zeros(B + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
+        if prefix_lens is None:
+            prefix_lens = [s - ql for s, ql in zip(seq_lens, q_lens)]
+        pl = torch.tensor(prefix_lens, dtype=torch.int32)
+        max_q = int(max(q_lens)) if B else 0
+    return Workload(name=name, decode=decode, q=q, q_is_e4m3=q_e4m3,
+                    pages_data=pages_data, pages_scale=pages_scale, page_ids=page_ids,
+                    num_pool_pages=pool_pages, layout=layout, k_data_page_stride=sd,
+                    k_scale_page_stride=ss, block_table=bt, seq_lens=seq_lens_t,
+                    cu_seqlens_q=cu, prefix_lens=pl, max_query_len=max_q,
+                    max_seq_len=max_seq_len, description=description)
+
+
+# ---------------------------------------------------------------- configs --
+CONFIG_NAMES = ("prefill-tiny", "decode", "prefill-long", "mtp", "chunked")
+
+# 2^32 lies inside page 493447 of an 8704 B-page pool (it starts at byte
+# 4,294,962,688), so forcing that page in exercises the 64-bit page rebase.
+STRADDLE_2_32_PAGE = 493447
+
+
+def make_config(name: str, seed: Optional[int] = None) -> Workload:
+    """The five measured configurations (H=64, D=128, 128-token pages)."""
+    idx = CONFIG_NAMES.index(name)
+    seed = idx if seed is None else seed
+    if name == "prefill-tiny":
+        return make_workload(name, seed=seed, q_lens=[32], seq_lens=[1024], prefix_lens=[992],
+                             pool_pages=16, layout="single",
+                             description="B=1, 32 rows, prefix 992, seq 1024, 16-page pool")
+    if name == "decode":
+        return make_workload(name, seed=seed, q_lens=None, seq_lens=[131072] * 64, decode=True,
+                             pool_pages=70000, layout="split", k_data_page_stride=8320,
+                             k_scale_page_stride=576,
+                             description="B=64 x 1 row, seq 131072, split views in a 70000-page pool")
+    if name == "prefill-long":
+        return make_workload(name, seed=seed, q_lens=[4096], seq_lens=[131072],
+                             prefix_lens=[126976], pool_pages=2048, layout="single",
+                             description="B=1, 4096 rows, prefix 126976, seq 131072, 2048-page pool")
+    if name == "mtp":
+        return make_workload(name, seed=seed, q_lens=[8] * 32, seq_lens=[32768] * 32,
+                             prefix_lens=[32760] * 32, pool_pages=600000, q_e4m3=True,
+                             scale_lo=100, scale_hi=150, layout="single",
+                             page_id_range=(480000, 600000),
+                             forced_page_ids=(STRADDLE_2_32_PAGE,),
+                             description="B=32 x 8 rows, seq 32768, e4m3 Q, e8m0 100..150, "
+                                         "600000-page pool (5.2 GB, pages past 2^32 B)")
+    if name == "chunked":
+        return make_workload(name, seed=seed, q_lens=[32768], seq_lens=[132768],
+                             prefix_lens=[100000], pool_pages=1200, layout="single",
+                             description="B=1, 32768 rows, prefix 100000, seq 132768, 1200-page pool")
+    raise KeyError(name)
+
+
+# ---------------------------------------------------------------- layouts --
+def relayout(w: Workload, layout: str, k_data_page_stride=None, k_scale_page_stride=None,
+             num_pool_pages=None) -> Workload:
+    """Same logical cache, other memory layout (single-region or split views)."""
+    if layout == "single":
+        sd = ss = k_data_page_stride or PAGE_BYTES
+    else:
+        sd = k_data_page_stride or DATA_BYTES
+        ss = k_scale_page_stride or SCALE_BYTES
+    return dataclasses.replace(w, layout=layout, k_data_page_stride=sd, k_scale_page_stride=ss,
+                               num_pool_pages=num_pool_pages or w.num_pool_pages)
+
+
+def permute_pages(w: Workload, seed: int) -> Workload:
+    """Move every used page to another physical id and rewrite the block table."""
+    g = _gen(seed)
+    new_ids = torch.randperm(w.num_pool_pages, generator=g)[: w.page_ids.shape[0]].to(torch.int64)
+    mapping = {int(o): int(n) for o, n in zip(w.page_ids.tolist(), new_ids.tolist())}
+    bt = w.block_table.clone()
+    flat = bt.view(-1)
+    for i in range(flat.shape[0]):
+        v = int(flat[i])
+        if v >= 0:
+            flat[i] = mapping[v]
+    return dataclasses.replace(w, page_ids=new_ids, block_table=bt)
+
+
+def _fill_pool(data_buf, scale_buf, w, ids, pages_data, pages_scale):
+    sd, ss = w.k_data_page_stride, w.k_scale_page_stride
+    n = ids.shape[0]
+    if n == 0:
+        return
+    d_idx = (ids.view(-1, 1) * sd + torch.arange(DATA_BYTES, device=ids.device)).view(-1)
+    s_idx = (ids.view(-1, 1) * ss + torch.arange(SCALE_BYTES, device=ids.device)).view(-1)
+    data_buf.index_copy_(0, d_idx, pages_data.reshape(-1))
+    scale_buf.index_copy_(0, s_idx, pages_scale.reshape(-1))
+
+
+def pool_nbytes(w: Workload):
+    """Bytes of the pool buffers: (data_buffer, scale_buffer or 0 when single)."""
+    if w.layout == "single":
+        return (w.num_pool_pages - 1) * w.k_data_page_stride + PAGE_BYTES, 0
+    return ((w.num_pool_pages - 1) * w.k_data_page_stride + DATA_BYTES,
+            (w.num_pool_pages - 1) * w.k_scale_page_stride + SCALE_BYTES)
+
+
+def build_pool(w: Workload, device="cpu", fill_seed: Optional[int] = 1234,
+               pin_memory: bool = False):
+    """Materialise the pool.  Returns (buffers, k_data_view, k_scale_view) where
+    the views are (tensor, byte offset) pairs into the buffers; unused pages
+    hold seeded random bytes (or zeros when ``fill_seed`` is None)."""
+    nd, ns = pool_nbytes(w)
+    # 256-byte slack so the views can be placed on any alignment on request
+    def alloc(n):
+        if fill_seed is None or device != "cpu":
+            t = torch.zeros(n, dtype=torch.uint8, device=device)
+        else:
+            t = torch.randint(0, 256, (n,), generator=_gen(fill_seed), dtype=torch.uint8)
+        if pin_memory:
+            t = t.pin_memory()
+        return t
+    ids = w.page_ids.to(device)
+    pd = w.pages_data.to(device)
+    ps = w.pages_scale.to(device)
+    if w.layout == "single":
+        buf = alloc(nd)
+        # data of page p at p*stride, scales at p*stride + 8192
+        d_idx = (ids.view(-1, 1) * w.k_data_page_stride
+                 + torch.arange(DATA_BYTES, device=device)).view(-1)
+        s_idx = (ids.view(-1, 1) * w.k_data_page_stride + DATA_BYTES
+                 + torch.arange(SCALE_BYTES, device=device)).view(-1)
+        buf.index_copy_(0, d_idx, pd.reshape(-1))
+        buf.index_copy_(0, s_idx, ps.reshape(-1))
+        return [buf], (buf, 0), (buf, DATA_BYTES)
+    dbuf = alloc(nd)
+    sbuf = alloc(ns)
+    _fill_pool(dbuf, sbuf, w, ids, pd, ps)
+    return [dbuf, sbuf], (dbuf, 0), (sbuf, 0)
+
+
+def compact_host(w: Workload):
+    """Host arrays for the oracle holding only the used pages: returns
+    (k_data, k_scale, sd, ss, block_table, num_pool_pages) with the block
+    table rewritten to compact page indices.  Physical placement does not
+    enter the arithmetic; the layout and 64-bit placement invariances are
+    checked separately on the real pools."""
+    ids = w.page_ids.tolist()
+    index = {p: u for u, p in enumerate(ids)}
+    bt = w.block_table.clone()
+    flat = bt.view(-1)
+    for i in range(flat.shape[0]):
+        v = int(flat[i])
+        flat[i] = index[v] if v >= 0 else -1
+    kd = w.pages_data.numpy().reshape(-1)
+    ks = w.pages_scale.numpy().reshape(-1)
+    return kd, ks, DATA_BYTES, SCALE_BYTES, bt.numpy(), len(ids)
+
+
+def q_numpy(w: Workload) -> np.ndarray:
+    """Q as raw bits for the oracle: uint16 (bf16) or uint8 (e4m3)."""
+    if w.q_is_e4m3:
+        return w.q.numpy()
+    return w.q.view(torch.int16).numpy().view(np.uint16)
+
+
+def sample_rows(w: Workload, n: int, seed: int = 0) -> np.ndarray:
+    """Seeded sample of query rows (sorted), always including the first and
+    last row."""
+    total = w.total_rows
+    if n >= total:
+        return np.arange(total, dtype=np.int64)
+    g = _gen(seed + 77)
+    pick = torch.randperm(total, generator=g)[: max(0, n - 2)].tolist()
+    s = sorted(set(pick) | {0, total - 1})
+    return np.array(s[:n] if len(s) > n else s, dtype=np.int64)

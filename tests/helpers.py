@@ -1,0 +1,149 @@
+"""Shared test helpers: run the oracle on a workload, compare results."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from sparse_attention_mxfp4_gb300 import workloads as W
+
+# Tolerance for finite fp32 scores against the fp64 oracle: relative 1e-5,
+# absolute 1e-6 (the accuracy the scorer is specified to).  -inf placement is
+# compared exactly.
+RTOL = 1e-5
+ATOL = 1e-6
+
+
+def oracle_run(w: W.Workload, rows=None, logits=False, scores=True, real_pool=False,
+               unquantized=False, num_threads=0):
+    """Oracle block scores / logits of workload ``w`` for ``rows`` (default all).
+
+    ``real_pool``: read the pages from a host pool in the workload's own
+    layout (single-region or split, real page ids); otherwise from a compact
+    copy of the used pages."""
+    if real_pool:
+        bufs, (dbuf, doff), (sbuf, soff) = W.build_pool(w, "cpu")
+        kd = dbuf.numpy()[doff:]
+        ks = sbuf.numpy()[soff:]
+        sd, ss = w.k_data_page_stride, w.k_scale_page_stride
+        bt = w.block_table.numpy()
+        npool = w.num_pool_pages
+    else:
+        kd, ks, sd, ss, bt, npool = W.compact_host(w)
+    return oracle.score(
+        decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, k_data=kd, k_scale=ks,
+        k_data_page_stride=sd, k_scale_page_stride=ss, block_table=bt,
+        block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
+        cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
+        prefix_lens=None if w.decode else w.prefix_lens.numpy(),
+        max_seq_len=w.max_seq_len, sm_scale=w.sm_scale, rows=rows,
+        want_scores=scores, want_logits=logits, unquantized=unquantized,
+        num_pool_pages=npool, num_threads=num_threads)
+
+
+def compare(got, ref, rtol=RTOL, atol=ATOL, what="scores"):
+    """Assert fp32 ``got`` matches fp64 ``ref``: -inf placement exactly,
+    finite values within |got-ref| <= atol + rtol*|ref|.  Returns stats."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    ninf_ref = np.isneginf(ref)
+    ninf_got = np.isneginf(got)
+    bad_mask = ninf_ref != ninf_got
+    if bad_mask.any():
+        idx = np.argwhere(bad_mask)[:5]
+        raise AssertionError(f"{what}: -inf placement differs at {idx.tolist()} "
+                             f"(got {got[tuple(idx[0])]}, ref {ref[tuple(idx[0])]}); "
+                             f"{int(bad_mask.sum())} cells")
+    fin = ~ninf_ref
+    assert np.isfinite(got[fin]).all(), f"{what}: non-finite value where a finite one is expected"
+    err = np.abs(got[fin] - ref[fin])
+    lim = atol + rtol * np.abs(ref[fin])
+    bad = err > lim
+    if bad.any():
+        i = int(np.argmax(err - lim))
+        raise AssertionError(f"{what}: {int(bad.sum())} of {fin.sum()} cells out of tolerance; "
+                             f"worst got {got[fin][i]!r} ref {ref[fin][i]!r}")
+    exact = float((got[fin] == ref[fin].astype(np.float32).astype(np.float64)).mean()) if fin.any() else 1.0
+    rel = float((err / np.maximum(np.abs(ref[fin]), 1e-30)).max()) if fin.any() else 0.0
+    return {"cells": int(got.size), "finite": int(fin.sum()), "max_abs_err": float(err.max()) if fin.any() else 0.0,
+            "max_rel_err": rel, "fp32_exact_fraction": exact}
+
+
+def dequant_numpy(w: W.Workload):
+    """Independent dequantisation in numpy from the bit fields of each code
+    (used to pin the oracle; shares nothing with the oracle's C code)."""
+    data = w.pages_data.numpy()
+    scale = w.pages_scale.numpy().astype(np.float64)
+    lo = data & 15
+    hi = data >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(data.shape[0], W.PAGE, W.DIM)
+    s = (codes >> 3) & 1
+    e = (codes >> 1) & 3
+    m = codes & 1
+    mag = np.where(e > 0, np.exp2(e.astype(np.float64) - 1) * (1 + m / 2.0), m / 2.0)
+    val = np.where(s == 1, -mag, mag)
+    sc = np.exp2(np.repeat(scale, 32, axis=-1) - 127.0)
+    return val * sc          # [U, 128, 128]
+
+
+def q_values_numpy(w: W.Workload):
+    """Independent e4m3 value of every Q element (bf16 inputs rounded by
+    exhaustive nearest-even search)."""
+    if w.q_is_e4m3:
+        codes = w.q.numpy().astype(np.int64)
+    else:
+        bits = w.q.view(torch.int16).numpy().view(np.uint16).astype(np.uint32)
+        x = (bits << 16).view(np.float32).astype(np.float64)
+        grid_codes = np.array([c for c in range(127)], dtype=np.int64)
+        e = (grid_codes >> 3) & 15
+        m = grid_codes & 7
+        grid = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
+        ax = np.minimum(np.abs(x), 448.0).reshape(-1)
+        idx = np.searchsorted(grid, ax)          # grid[idx-1] < ax <= grid[idx]
+        idx = np.clip(idx, 1, len(grid) - 1)
+        lo_v, hi_v = grid[idx - 1], grid[idx]
+        pick_hi = (hi_v - ax < ax - lo_v) | ((hi_v - ax == ax - lo_v) & (grid_codes[idx] % 2 == 0))
+        mag_code = np.where(ax == 0, 0, np.where(pick_hi, idx, idx - 1))
+        codes = (mag_code | (np.signbit(x.reshape(-1)).astype(np.int64) << 7)).reshape(x.shape)
+    s = (codes >> 7) & 1
+    e = (codes >> 3) & 15
+    m = codes & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
+    return np.where(s == 1, -mag, mag)       # [rows, 64, 128]
+
+
+def scores_numpy(w: W.Workload, rows=None, logits=False):
+    """Block scores by a different formulation: dense dequantised K gathered
+    per request, one float64 matmul per request, a broadcast causal mask and a
+    reshape-max per page."""
+    kv = dequant_numpy(w)
+    qv = q_values_numpy(w)
+    ids = {int(p): u for u, p in enumerate(w.page_ids.tolist())}
+    P = w.num_out_pages
+    B = w.num_seqs
+    total = w.total_rows
+    rows = np.arange(total) if rows is None else np.asarray(rows)
+    out = np.full((len(rows), W.HEADS, P), -np.inf)
+    lg = np.full((len(rows), W.HEADS, w.max_seq_len), -np.inf) if logits else None
+    for ri, r in enumerate(rows):
+        if w.decode:
+            b, pos = int(r), 0
+            L = int(w.seq_lens[b])
+        else:
+            cu = w.cu_seqlens_q.numpy()
+            b = int(np.searchsorted(cu, r, side="right") - 1)
+            pos = int(r - cu[b])
+            L = min(int(w.seq_lens[b]), int(w.prefix_lens[b]) + pos + 1)
+        L = min(L, w.max_seq_len)
+        if L <= 0:
+            continue
+        npg = (L + W.PAGE - 1) // W.PAGE
+        k = np.concatenate([kv[ids[int(w.block_table[b, j])]] for j in range(npg)], axis=0)[:L]
+        v = w.sm_scale * (qv[r] @ k.T)                       # [64, L]
+        pad = np.full((W.HEADS, npg * W.PAGE), -np.inf)
+        pad[:, :L] = v
+        out[ri, :, :npg] = pad.reshape(W.HEADS, npg, W.PAGE).max(axis=2)
+        if logits:
+            lg[ri, :, :L] = v
+    return out, lg
