@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged MXFP4 index-K scorer on GB300.
+
+Metric: microseconds per scorer call (lower is better), with the achieved HBM
+bandwidth (decode) or block-scaled MMA rate (prefill) against the GB300 peak.
+
+Headline workload: decode, B=64 requests x 1 query row, 131,072-token contexts
+(1024 pages each) scattered by a seeded block table over a 70,000-page pool
+with split data/scale views.  One step = one call over the whole batch.
+The pool (623 MB, 570 MB read per call) is larger than L2, so no flush is
+needed between calls.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config decode|prefill-tiny|prefill-long|mtp|chunked]
+                  [--no-secondary]
+
+For N > 1 run under torchrun: every rank scores its own replica of the
+workload (the calls are independent; there is no exchange step).
+``--impl reference`` times the fp64 CPU oracle on the machine's host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import signal
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# nominal dense ratios on GB300: fp8 = 2 x bf16, fp4 = 6 x bf16
+FP8_OVER_BF16 = 2.0
+FP4_OVER_BF16 = 6.0
+
+
+# ------------------------------------------------------------------ helpers --
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs")
+            bf16 = d.get("bf16_tflops")
+            bf16s = d.get("bf16_tflops_sustained", bf16)
+            if hbm and bf16:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf16),
+                        "bf16_tflops_sustained": float(bf16s), "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def library_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_mxfp4_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when the summary is missing or was taken on other
+    kernel source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    src = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    if not m or not src or src.group(1) != library_source_hash():
+        return None
+    return int(m.group(1))
+
+
+def workload_work(w):
+    """Algorithmic bytes and flops of one call (each live page read once)."""
+    import numpy as np
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    seq = w.seq_lens.numpy().astype(np.int64)
+    if w.decode:
+        L_last = np.minimum(seq, w.max_seq_len)
+        live_pairs = int(L_last.sum())
+        rows_L = L_last
+    else:
+        cu = w.cu_seqlens_q.numpy().astype(np.int64)
+        pl = w.prefix_lens.numpy().astype(np.int64)
+        rows_L = []
+        L_last = np.zeros_like(seq)
+        for b in range(w.num_seqs):
+            ql = cu[b + 1] - cu[b]
+            if ql <= 0:
+                continue
+            Ls = np.minimum(seq[b], pl[b] + np.arange(ql) + 1).clip(0, w.max_seq_len)
+            rows_L.append(Ls)
+            L_last[b] = Ls.max()
+        rows_L = np.concatenate(rows_L) if rows_L else np.zeros(0, np.int64)
+        live_pairs = int(rows_L.sum())
+    pages_read = int(((L_last + W.PAGE - 1) // W.PAGE).sum())
+    q_bytes = w.q.numel() * w.q.element_size()
+    out_bytes = w.total_rows * W.HEADS * w.num_out_pages * 4
+    k_bytes = pages_read * W.PAGE_BYTES
+    bt_bytes = pages_read * 4
+    flops = live_pairs * W.HEADS * W.DIM * 2
+    return {"k_bytes": k_bytes, "q_bytes": q_bytes, "out_bytes": out_bytes, "bt_bytes": bt_bytes,
+            "bytes": k_bytes + q_bytes + out_bytes + bt_bytes, "flops": flops, "live_pairs": live_pairs,
+            "pages_read": pages_read}
+
+
+# ------------------------------------------------------------------ our arm --
+def time_calls(case, out, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        case.run(out=out, stream=stream)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        case.run(out=out, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def measure_e2e(case, steps, stream):
+    """Same call through the public API with host-resident inputs: every step
+    copies the inputs from pinned host memory, scores, and reads the scores
+    back into pinned host memory."""
+    import torch
+    from sparse_attention_mxfp4_gb300.harness import DeviceCase
+    dev_bufs = [case.q, case.block_table, case.seq_lens] + list(case.buffers)
+    if case.cu_seqlens_q is not None:
+        dev_bufs += [case.cu_seqlens_q, case.prefix_lens]
+    host_bufs = [b.cpu().pin_memory() for b in dev_bufs]
+    out = torch.empty(case.out_shape_scores, dtype=torch.float32, device=case.q.device)
+    host_out = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(b.numel() * b.element_size() for b in host_bufs)
+    d2h = out.numel() * 4
+
+    def step():
+        for d, h in zip(dev_bufs, host_bufs):
+            d.copy_(h, non_blocking=True)
+        case.run(out=out, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def cpu_baseline_decode(w):
+    """The oracle, as it stands, on all 64 requests of the decode workload
+    (one full call), on every host core."""
+    import numpy as np
+    import oracle
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    kd, ks, sd, ss, bt, n = W.compact_host(w)
+    cores = os.cpu_count() or 1
+    rows = np.arange(w.total_rows)
+    t0 = time.perf_counter()
+    oracle.score(decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, k_data=kd, k_scale=ks,
+                 k_data_page_stride=sd, k_scale_page_stride=ss, block_table=bt,
+                 block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
+                 cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
+                 prefix_lens=None if w.decode else w.prefix_lens.numpy(), max_seq_len=w.max_seq_len,
+                 sm_scale=w.sm_scale, rows=rows, num_pool_pages=n, num_threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": dt * 1e6, "unit": "us/call", "cores": cores, "kind": "oracle",
+            "sample": f"full call: all {len(rows)} query rows of the {w.name} workload, fp64, "
+                      f"OpenMP over rows, 1 repetition (not extrapolated)"}
+
+
+def secondary_configs(names, peaks, stream):
+    import torch
+    from sparse_attention_mxfp4_gb300 import harness
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    res = {}
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    for name in names:
+        w = W.make_config(name)
+        case = harness.to_device(w)
+        out = torch.empty(case.out_shape_scores, dtype=torch.float32, device="cuda")
+        work = workload_work(w)
+        steps = 200 if name == "prefill-tiny" else (5 if name == "chunked" else 20)
+        ms = time_calls(case, out, steps, 3, stream)
+        tf = work["flops"] / (ms * 1e-3) / 1e12
+        res[name] = {"us_per_call": round(ms * 1e3, 3), "steps": steps,
+                     "mma_tflops": round(tf, 1),
+                     "frac_of_fp8_dense_peak": round(tf / fp8_peak, 4),
+                     "frac_of_fp4_dense_peak": round(tf / fp4_peak, 4),
+                     "hbm_gbs_algorithmic": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
+                     "flops_per_call": work["flops"], "bytes_per_call": work["bytes"]}
+        del case, out
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import sparse_attention_mxfp4_gb300 as mx4
+    from sparse_attention_mxfp4_gb300 import harness
+    from sparse_attention_mxfp4_gb300 import workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    mx4.build()
+    mx4.load_library()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+
+    w = W.make_config(args.config)
+    case = harness.to_device(w)
+    out = torch.empty(case.out_shape_scores, dtype=torch.float32, device="cuda")
+    work = workload_work(w)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    for _ in range(args.warmup):
+        case.run(out=out, stream=stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        case.run(out=out, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ms_rank = start.elapsed_time(end) / args.steps
+    clocks = sampler.stop() if sampler else None
+    status = mx4.mx4_index_get_device_status()
+    if ws > 1:
+        t = torch.tensor([ms_rank], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    else:
+        ms = ms_rank
+
+    e2e_ms, h2d, d2h = measure_e2e(case, max(3, min(args.steps, 20)), stream)
+
+    line = None
+    if rank == 0:
+        us_per_call = ms * 1e3 / ws          # N independent calls per step across the job
+        if w.decode:
+            achieved = work["bytes"] / (ms * 1e-3) / 1e9
+            roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "traffic": profile_traffic("mx4_score_kernel", w.name),
+                    "peak_source": peaks["source"],
+                    "algorithmic_bytes_per_launch": work["bytes"],
+                    "index_cache_bytes_per_launch": work["k_bytes"],
+                    "index_cache_gbs": round(work["k_bytes"] / (ms * 1e-3) / 1e9, 1)}
+        else:
+            fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+            achieved = work["flops"] / (ms * 1e-3) / 1e12
+            roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / fp8_peak, 4),
+                    "traffic": profile_traffic("mx4_score_kernel", w.name),
+                    "peak_source": peaks["source"] + " bf16 x 2 (nominal fp8/bf16 ratio)",
+                    "algorithmic_flops_per_launch": work["flops"]}
+        line = {
+            "metric": "MXFP4 index-score us/call (decode B=64, ctx 131072)" if w.decode
+            else f"MXFP4 index-score us/call ({w.name})",
+            "value": round(us_per_call, 3), "unit": "us/call", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e2m1 -> f32",
+            "data": "synthetic (seeded; no dataset or weights)",
+            "config": {"workload": w.name, "description": w.description, "heads": W.HEADS, "head_dim": W.DIM,
+                       "page_tokens": W.PAGE, "rows": w.total_rows, "requests": w.num_seqs,
+                       "max_seq_len": w.max_seq_len, "q_dtype": "e4m3" if w.q_is_e4m3 else "bf16",
+                       "layout": w.layout, "l2": "inputs larger than L2 (no flush)" if work["k_bytes"] > 129e6
+                       else "K fits in L2: warm-L2 number",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "roofline": roof,
+            "e2e": {"value": round(e2e_ms * 1e3 / ws, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "device_status": status,
+        }
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_decode(w) if w.decode else None
+        if ws == 1 and not args.no_secondary:
+            del case, out
+            torch.cuda.empty_cache()
+            names = [n for n in W.CONFIG_NAMES if n != w.name]
+            line["secondary"] = secondary_configs(names, peaks, stream)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference arm --
+def run_reference(args):
+    """The fp64 oracle timed on the host cores, on a bounded sample of the
+    same workload per step: every request's first T tokens (all 64 heads),
+    T chosen so the whole run takes about two minutes; the per-call time is
+    extrapolated by live (row, token) pairs."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import dataclasses
+    import numpy as np
+    import torch
+    import oracle
+    from sparse_attention_mxfp4_gb300 import workloads as W
+
+    oracle.build()
+    w = W.make_config(args.config)
+    cores = os.cpu_count() or 1
+    work = workload_work(w)
+    budget_s = 120.0 / max(1, args.steps + args.warmup)
+    rows = np.arange(min(w.total_rows, cores), dtype=np.int64)
+    # ~1e9 multiply-adds per second per core for the oracle
+    tokens = int(budget_s * 1e9 / (W.HEADS * W.DIM))
+    tokens = max(W.PAGE, min(w.max_seq_len, tokens // W.PAGE * W.PAGE))
+    sub = dataclasses.replace(w, seq_lens=torch.clamp(w.seq_lens, max=tokens),
+                              max_seq_len=min(w.max_seq_len, tokens))
+    if not sub.decode:
+        sub = dataclasses.replace(sub, prefix_lens=torch.clamp(sub.prefix_lens, max=tokens))
+    kd, ks, sd, ss, bt, n = W.compact_host(sub)
+    sample_pairs = oracle.live_pairs(decode=sub.decode, seq_lens=sub.seq_lens.numpy(),
+                                     max_seq_len=sub.max_seq_len,
+                                     cu_seqlens_q=None if sub.decode else sub.cu_seqlens_q.numpy(),
+                                     prefix_lens=None if sub.decode else sub.prefix_lens.numpy(), rows=rows)
+
+    def step():
+        oracle.score(decode=sub.decode, q=W.q_numpy(sub), q_is_e4m3=sub.q_is_e4m3, k_data=kd, k_scale=ks,
+                     k_data_page_stride=sd, k_scale_page_stride=ss, block_table=bt,
+                     block_table_stride=sub.block_table_stride, seq_lens=sub.seq_lens.numpy(),
+                     cu_seqlens_q=None if sub.decode else sub.cu_seqlens_q.numpy(),
+                     prefix_lens=None if sub.decode else sub.prefix_lens.numpy(),
+                     max_seq_len=sub.max_seq_len, sm_scale=sub.sm_scale, rows=rows, num_pool_pages=n,
+                     num_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    scale = work["live_pairs"] / max(1, sample_pairs)
+    us = dt * scale * 1e6
+    sample = (f"per step: query rows 0..{len(rows) - 1} of the {w.name} workload, first {tokens} tokens "
+              f"of each context ({sample_pairs} live row-token pairs of {work['live_pairs']}); "
+              f"time extrapolated by live pairs")
+    line = {"impl": "reference",
+            "metric": "MXFP4 index-score us/call (decode B=64, ctx 131072)" if w.decode
+            else f"MXFP4 index-score us/call ({w.name})",
+            "value": round(us, 1), "unit": "us/call", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "description": w.description},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="decode",
+                    choices=("decode", "prefill-tiny", "prefill-long", "mtp", "chunked"))
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other configurations")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * mx4_index.h -- C ABI of the paged MXFP4 index-K scorer for GB300 (sm_103a).
+ *
+ * The scorer of a sparse-attention indexer: for every query row, head and
+ * 128-token page of the request's context it writes the largest causal-masked,
+ * sm_scale-scaled logit of the page (a "block score"), or -inf when the page
+ * has no live token.  An optional per-token mode writes the logits
+ * themselves.
+ *
+ * Sources (each entry point cites the passage that defines it):
+ *   [P1] aiter #7061, "MiniMax-M3 index score: MXFP4 index-cache prefill
+ *        scorer": sections "Format", "Kernels", "Tests".
+ *   [P2] ATOM #2770, "MiniMax-M3.1 MXFP4 sparse KV cache and index cache":
+ *        section "How it works" and the pa_decode MXFP4 commit message.
+ *   [P3] aiter #5518, "[FlyDSL][gfx950] explicit page strides and 64-bit
+ *        rebase for FP4 MQA logits": sections "Summary", decode auto-CTA
+ *        table, "Correctness / regression".
+ *
+ * Shapes and layouts (H = 64 heads, D = 128, 128-token pages):
+ *   q            [total_rows, 64, 128], contiguous; bf16 (q_is_e4m3 = 0) or
+ *                e4m3 bytes (q_is_e4m3 = 1).  16-byte aligned.
+ *   k_data       page p's e2m1 codes at k_data + p * k_data_page_stride:
+ *                [128 tokens][64 bytes]; element 2i in the low nibble of byte
+ *                i, element 2i+1 in the high nibble.  32-byte aligned;
+ *                k_data_page_stride >= 8192 and a multiple of 32 (a GB300
+ *                TMA rule for 4-bit data).
+ *   k_scale      page p's e8m0 bytes at k_scale + p * k_scale_page_stride:
+ *                [128 tokens][4 bytes], byte g scales elements 32g..32g+31.
+ *                16-byte aligned; k_scale_page_stride >= 512, multiple of 16.
+ *                The single-region page of [P1] is k_scale = k_data + 8192
+ *                with both strides 8704.
+ *   block_table  int32 [num_seqs, block_table_stride] physical page ids;
+ *                entries at or past ceil(seq_len/128) are never read.
+ *   out          fp32 [total_rows, 64, ceil(max_seq_len/128)] block scores,
+ *                or [total_rows, 64, max_seq_len] per-token logits.  Every
+ *                cell of every existing row is written (no pre-fill needed).
+ *                16-byte aligned.
+ *
+ * Ownership: every pointer is a borrowed device pointer owned by the caller.
+ * The library allocates no device memory; its only device state is one
+ * status word in a static device variable of the loaded module.
+ *
+ * Streams: calls enqueue on `stream` (a cudaStream_t; NULL = legacy default
+ * stream), never synchronise, and read no device data on the host, so a
+ * sequence of calls can be captured in a CUDA graph after a first
+ * (warm-up) call on the device.
+ *
+ * Errors: host-checkable faults return a status before anything is
+ * launched.  A call with no output cell (num_seqs, max_seq_len or, for
+ * prefill, max_query_len equal to 0) returns MX4_OK at once; its pointers
+ * are not checked.  Faults only the device can see (a page id outside
+ * [0, num_pool_pages) for a live page, an internal wait that ran out) set
+ * bits of the device status word and leave the affected outputs undefined;
+ * read them with mx4_index_get_device_status.  No C++ exception crosses
+ * this ABI.
+ */
+#ifndef MX4_INDEX_H
+#define MX4_INDEX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MX4_ABI_VERSION 1
+
+typedef enum {
+    MX4_OK = 0,
+    MX4_ERR_INVALID_ARG = 1, /* null pointer, negative size, narrow view or table, bad sm_scale */
+    MX4_ERR_MISALIGNED = 2,  /* pointer or stride alignment rule broken */
+    MX4_ERR_UNSUPPORTED = 3, /* size outside what the kernels support */
+    MX4_ERR_CUDA = 4         /* a CUDA runtime/driver call failed */
+} mx4_status;
+
+/* Device status bits (mx4_index_get_device_status). */
+#define MX4_DEV_BAD_PAGE 0x1u /* a live page id was outside [0, num_pool_pages) */
+#define MX4_DEV_TIMEOUT 0x2u  /* an internal wait gave up; the kernel returned early */
+/* With MX4_DEV_TIMEOUT, bit (8 + site) names the wait that gave up: site 0 =
+ * producer waiting for a free smem stage, 1 = MMA waiting for the query tile,
+ * 2 = MMA waiting for a page, 3 = MMA waiting for a free accumulator,
+ * 4 = epilogue waiting for a free query buffer, 5 = epilogue waiting for an
+ * accumulator.  Diagnostic only. */
+
+/*
+ * Block scores for ragged prefill (causal) rows.  [P1] "Kernels":
+ * score_prefill_flydsl_fp4(idx_q, k_data, k_scale, block_table, cu_seqlens_q,
+ * seq_lens, prefix_lens, max_query_len, max_seq_len, sm_scale, out); [P1]
+ * "Format" for the page, the value e2m1 x 2^(byte-127) and the block score
+ * (max over live tokens of the dot with Q); [P3] "Summary" for the page
+ * strides (bytes), the block-table stride (int32 elements) and 64-bit page
+ * offsets.
+ *
+ * Row r of request b (cu_seqlens_q[b] <= r < cu_seqlens_q[b+1]) sees token t
+ * iff t < min(seq_lens[b], prefix_lens[b] + (r - cu_seqlens_q[b]) + 1).
+ * out[r, h, j] = sm_scale * max over live t in [128j, 128j+128) of
+ *                sum_d Q8[r,h,d] * e2m1(K[t,d]) * 2^(S[t,d/32]-127),
+ * accumulated in fp32 on the tensor cores; -inf if page j has no live token.
+ * Q8 is the bf16 query rounded to e4m3 (nearest even, saturating to +-448),
+ * or the e4m3 query as stored.
+ *
+ * Appended scalars (not on the page, needed to size a launch without reading
+ * device memory): num_seqs = B (cu_seqlens_q has B+1 entries),
+ * block_table_stride in int32 elements (>= ceil(max_seq_len/128)),
+ * num_pool_pages = pages addressable through both views (>= 1, < 2^31).
+ * max_query_len must be >= every request's row count and max_seq_len >=
+ * every seq_len.  sm_scale must be finite and > 0.
+ */
+mx4_status mx4_index_score_prefill(const void *q, int q_is_e4m3, const uint8_t *k_data,
+                                   const uint8_t *k_scale, int64_t k_data_page_stride,
+                                   int64_t k_scale_page_stride, const int32_t *block_table,
+                                   const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                   const int32_t *prefix_lens, int max_query_len,
+                                   int max_seq_len, float sm_scale, float *out, void *stream,
+                                   int num_seqs, int64_t block_table_stride,
+                                   int64_t num_pool_pages);
+
+/*
+ * Block scores for decode: one query row per request (q [num_seqs, 64, 128]),
+ * token t live iff t < seq_lens[b].  Same arithmetic and output rule as the
+ * prefill call.  [P2] "How it works" (decode scoring inside the CUDA graph)
+ * and [P3] decode auto-CTA table: the context of each request is split over
+ * several CTAs by a grid chosen on the host from num_seqs and max_seq_len
+ * only, so the launch is stable under graph replay.
+ */
+mx4_status mx4_index_score_decode(const void *q, int q_is_e4m3, const uint8_t *k_data,
+                                  const uint8_t *k_scale, int64_t k_data_page_stride,
+                                  int64_t k_scale_page_stride, const int32_t *block_table,
+                                  const int32_t *seq_lens, int max_seq_len, float sm_scale,
+                                  float *out, void *stream, int num_seqs,
+                                  int64_t block_table_stride, int64_t num_pool_pages);
+
+/*
+ * Per-token logits for prefill rows ([P3] "Summary": paged MXFP4 MQA logits;
+ * "Correctness": -inf masks retained).  logits[r, h, t] = sm_scale *
+ * sum_d Q8[r,h,d] * K[t,d] for live t, -inf for every other t < max_seq_len.
+ * logits is fp32 [total_rows, 64, max_seq_len].  Arguments as for
+ * mx4_index_score_prefill.
+ */
+mx4_status mx4_index_logits_prefill(const void *q, int q_is_e4m3, const uint8_t *k_data,
+                                    const uint8_t *k_scale, int64_t k_data_page_stride,
+                                    int64_t k_scale_page_stride, const int32_t *block_table,
+                                    const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                    const int32_t *prefix_lens, int max_query_len,
+                                    int max_seq_len, float sm_scale, float *logits,
+                                    void *stream, int num_seqs, int64_t block_table_stride,
+                                    int64_t num_pool_pages);
+
+/*
+ * Per-token logits for decode rows: logits fp32 [num_seqs, 64, max_seq_len],
+ * -inf for t >= seq_lens[b].  Arguments as for mx4_index_score_decode.
+ */
+mx4_status mx4_index_logits_decode(const void *q, int q_is_e4m3, const uint8_t *k_data,
+                                   const uint8_t *k_scale, int64_t k_data_page_stride,
+                                   int64_t k_scale_page_stride, const int32_t *block_table,
+                                   const int32_t *seq_lens, int max_seq_len, float sm_scale,
+                                   float *logits, void *stream, int num_seqs,
+                                   int64_t block_table_stride, int64_t num_pool_pages);
+
+/*
+ * The query-preparation step on its own: n bf16 values (raw bits) rounded to
+ * e4m3 bytes, nearest even, saturating to +-448, signed zero kept ([P1]
+ * "Kernels": a bf16 query is rounded to e4m3 in-kernel; the scorers above do
+ * this inside the kernel with the same device function).  Both pointers are
+ * device pointers; n >= 0.
+ */
+mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t n, void *stream);
+
+/*
+ * Read the current device's status word (MX4_DEV_* bits, ORed by every call
+ * since the last read) after synchronising `stream`, then clear it.
+ */
+mx4_status mx4_index_get_device_status(void *stream, uint32_t *status_out);
+
+/* Human-readable name of a status code; never NULL. */
+const char *mx4_status_string(int status);
+
+/* MX4_ABI_VERSION of the loaded library. */
+int mx4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX4_INDEX_H */

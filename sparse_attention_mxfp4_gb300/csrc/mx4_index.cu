@@ -1,0 +1,317 @@
+// mx4_index.cu -- C ABI of the paged MXFP4 index-K scorer (declared in
+// include/mx4_index.h): argument validation, TMA tensor-map encoding, grid
+// choice and kernel launch.  No allocation, no synchronisation, no device
+// reads on the host path of the scoring calls.
+#include "mx4_index.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "score_kernel.cuh"
+
+namespace {
+
+using mx4::ScoreParams;
+using mx4::SmemLayout;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    int sm_count = 0;
+    bool smem_attr_set[4] = {false, false, false, false};
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+
+template <bool kDecode, bool kLogits>
+constexpr int kernel_index()
+{
+    return (kDecode ? 1 : 0) + (kLogits ? 2 : 0);
+}
+
+// Per-device one-time setup: SM count and the dynamic smem opt-in.
+template <bool kDecode, bool kLogits>
+mx4_status device_setup(int *sm_count)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &st = g_dev[dev];
+    if (st.sm_count == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return MX4_ERR_CUDA;
+        st.sm_count = n;
+    }
+    constexpr int ki = kernel_index<kDecode, kLogits>();
+    if (!st.smem_attr_set[ki]) {
+        if (cudaFuncSetAttribute(mx4::mx4_score_kernel<kDecode, kLogits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(SmemLayout::kAlloc)) != cudaSuccess)
+            return MX4_ERR_CUDA;
+        st.smem_attr_set[ki] = true;
+    }
+    *sm_count = st.sm_count;
+    return MX4_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Page data view as a 4-D tensor of 4-bit elements:
+//   dim0: 128 elements of one token (64 B), dim1: n0 in [0,32) (stride 256 B),
+//   dim2: n1 in [0,4) (stride 64 B), dim3: page id (stride = page stride).
+// A box {128, 32, 4, 1} lands token 4*n0 + n1 in smem row n0 + 32*n1, each
+// 16-element group padded to 16 B (the tensor core's 4-bit operand form) and
+// 128-byte swizzled.
+bool encode_kdata_map(CUtensorMap *m, const uint8_t *k_data, int64_t stride, int64_t pages)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {128, 32, 4, static_cast<cuuint64_t>(pages)};
+    const cuuint64_t strides[3] = {256, 64, static_cast<cuuint64_t>(stride)};
+    const cuuint32_t box[4] = {128, 32, 4, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t *>(k_data), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Page scale view: 128 words (4 e8m0 bytes of one token each) per page.
+bool encode_kscale_map(CUtensorMap *m, const uint8_t *k_scale, int64_t stride, int64_t pages)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(pages)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride)};
+    const cuuint32_t box[2] = {128, 1};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t *>(k_scale), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Args {
+    const void *q;
+    int q_is_e4m3;
+    const uint8_t *k_data;
+    const uint8_t *k_scale;
+    int64_t sd, ss;
+    const int32_t *block_table;
+    const int32_t *cu_seqlens_q;
+    const int32_t *seq_lens;
+    const int32_t *prefix_lens;
+    int max_query_len;
+    int max_seq_len;
+    float sm_scale;
+    float *out;
+    cudaStream_t stream;
+    int num_seqs;
+    int64_t bt_stride;
+    int64_t num_pool_pages;
+};
+
+// True when the call has no output cell (no request, no query row or no
+// page): such a call succeeds without touching any pointer.
+bool empty_call(const Args &a, bool decode)
+{
+    return a.num_seqs == 0 || a.max_seq_len == 0 || (!decode && a.max_query_len == 0);
+}
+
+mx4_status validate(const Args &a, bool decode)
+{
+    if (a.q_is_e4m3 != 0 && a.q_is_e4m3 != 1) return MX4_ERR_INVALID_ARG;
+    if (a.num_seqs < 0 || a.max_seq_len < 0 || (!decode && a.max_query_len < 0)) return MX4_ERR_INVALID_ARG;
+    if (!(std::isfinite(a.sm_scale) && a.sm_scale > 0.0f)) return MX4_ERR_INVALID_ARG;
+    if (empty_call(a, decode)) return MX4_OK;
+    if (!a.q || !a.k_data || !a.k_scale || !a.block_table || !a.seq_lens || !a.out) return MX4_ERR_INVALID_ARG;
+    if (!decode && (!a.cu_seqlens_q || !a.prefix_lens)) return MX4_ERR_INVALID_ARG;
+    if (a.sd < mx4::kDataBytes || a.ss < mx4::kScaleBytes) return MX4_ERR_INVALID_ARG;   // narrow views
+    if (a.num_pool_pages < 1) return MX4_ERR_INVALID_ARG;
+    if (a.num_pool_pages > INT32_MAX) return MX4_ERR_UNSUPPORTED;
+    const int64_t P = (static_cast<int64_t>(a.max_seq_len) + mx4::kPage - 1) / mx4::kPage;
+    if (a.bt_stride < P || a.bt_stride < 0) return MX4_ERR_INVALID_ARG;                  // narrow table
+    if (a.sd >= (int64_t(1) << 40) || a.ss >= (int64_t(1) << 40)) return MX4_ERR_UNSUPPORTED;
+    if (!aligned(a.k_data, 32) || (a.sd % 32) != 0) return MX4_ERR_MISALIGNED;
+    if (!aligned(a.k_scale, 16) || (a.ss % 16) != 0) return MX4_ERR_MISALIGNED;
+    if (!aligned(a.q, 16) || !aligned(a.out, 16)) return MX4_ERR_MISALIGNED;
+    if (!aligned(a.block_table, 4) || !aligned(a.seq_lens, 4)) return MX4_ERR_MISALIGNED;
+    if (!decode && (!aligned(a.cu_seqlens_q, 4) || !aligned(a.prefix_lens, 4))) return MX4_ERR_MISALIGNED;
+    return MX4_OK;
+}
+
+template <bool kDecode, bool kLogits>
+mx4_status launch(const Args &a)
+{
+    mx4_status st = validate(a, kDecode);
+    if (st != MX4_OK || empty_call(a, kDecode)) return st;
+    const int P = static_cast<int>((static_cast<int64_t>(a.max_seq_len) + mx4::kPage - 1) / mx4::kPage);
+    const int rows_per_tile = kDecode ? 1 : 2;
+    const int tiles_per_seq = kDecode ? 1 : (a.max_query_len + rows_per_tile - 1) / rows_per_tile;
+    if (a.num_seqs == 0 || P == 0 || tiles_per_seq == 0) return MX4_OK;   // no output cell exists
+    const int chunks_per_tile = (P + mx4::kChunk - 1) / mx4::kChunk;
+    const int64_t num_units = static_cast<int64_t>(a.num_seqs) * tiles_per_seq * chunks_per_tile;
+
+    int sm_count = 0;
+    st = device_setup<kDecode, kLogits>(&sm_count);
+    if (st != MX4_OK) return st;
+
+    alignas(64) CUtensorMap tmap_k;
+    alignas(64) CUtensorMap tmap_s;
+    if (!encode_kdata_map(&tmap_k, a.k_data, a.sd, a.num_pool_pages)) return MX4_ERR_CUDA;
+    if (!encode_kscale_map(&tmap_s, a.k_scale, a.ss, a.num_pool_pages)) return MX4_ERR_CUDA;
+
+    ScoreParams p{};
+    p.q = a.q;
+    p.block_table = a.block_table;
+    p.cu_seqlens_q = a.cu_seqlens_q;
+    p.seq_lens = a.seq_lens;
+    p.prefix_lens = a.prefix_lens;
+    p.out = a.out;
+    p.bt_stride = a.bt_stride;
+    p.num_pool_pages = a.num_pool_pages;
+    p.num_units = num_units;
+    p.out_row_stride = kLogits ? a.max_seq_len : P;
+    p.num_seqs = a.num_seqs;
+    p.max_seq_len = a.max_seq_len;
+    p.num_out_pages = P;
+    p.tiles_per_seq = tiles_per_seq;
+    p.chunks_per_tile = chunks_per_tile;
+    p.q_is_e4m3 = a.q_is_e4m3;
+    p.sm_scale = a.sm_scale;
+
+    // Host-known grid: one persistent CTA per SM (fewer when there are fewer
+    // units); each CTA takes a contiguous, equal share of the units.
+    const int64_t grid = num_units < sm_count ? num_units : sm_count;
+    cudaGetLastError();   // clear a stale error so the check below is ours
+    mx4::mx4_score_kernel<kDecode, kLogits>
+        <<<static_cast<unsigned>(grid), mx4::kThreads, SmemLayout::kAlloc, a.stream>>>(tmap_k, tmap_s, p);
+    return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+mx4_status mx4_index_score_prefill(const void *q, int q_is_e4m3, const uint8_t *k_data, const uint8_t *k_scale,
+                                   int64_t k_data_page_stride, int64_t k_scale_page_stride,
+                                   const int32_t *block_table, const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                   const int32_t *prefix_lens, int max_query_len, int max_seq_len, float sm_scale,
+                                   float *out, void *stream, int num_seqs, int64_t block_table_stride,
+                                   int64_t num_pool_pages)
+{
+    const Args a{q,           q_is_e4m3,     k_data,       k_scale,   k_data_page_stride, k_scale_page_stride,
+                 block_table, cu_seqlens_q,  seq_lens,     prefix_lens, max_query_len,    max_seq_len,
+                 sm_scale,    out,           static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+                 num_pool_pages};
+    return launch<false, false>(a);
+}
+
+mx4_status mx4_index_score_decode(const void *q, int q_is_e4m3, const uint8_t *k_data, const uint8_t *k_scale,
+                                  int64_t k_data_page_stride, int64_t k_scale_page_stride,
+                                  const int32_t *block_table, const int32_t *seq_lens, int max_seq_len,
+                                  float sm_scale, float *out, void *stream, int num_seqs,
+                                  int64_t block_table_stride, int64_t num_pool_pages)
+{
+    const Args a{q,           q_is_e4m3, k_data,   k_scale, k_data_page_stride, k_scale_page_stride,
+                 block_table, nullptr,   seq_lens, nullptr, 1,                  max_seq_len,
+                 sm_scale,    out,       static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+                 num_pool_pages};
+    return launch<true, false>(a);
+}
+
+mx4_status mx4_index_logits_prefill(const void *q, int q_is_e4m3, const uint8_t *k_data, const uint8_t *k_scale,
+                                    int64_t k_data_page_stride, int64_t k_scale_page_stride,
+                                    const int32_t *block_table, const int32_t *cu_seqlens_q,
+                                    const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
+                                    int max_seq_len, float sm_scale, float *logits, void *stream, int num_seqs,
+                                    int64_t block_table_stride, int64_t num_pool_pages)
+{
+    const Args a{q,           q_is_e4m3,    k_data,   k_scale,     k_data_page_stride, k_scale_page_stride,
+                 block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len,      max_seq_len,
+                 sm_scale,    logits,       static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+                 num_pool_pages};
+    return launch<false, true>(a);
+}
+
+mx4_status mx4_index_logits_decode(const void *q, int q_is_e4m3, const uint8_t *k_data, const uint8_t *k_scale,
+                                   int64_t k_data_page_stride, int64_t k_scale_page_stride,
+                                   const int32_t *block_table, const int32_t *seq_lens, int max_seq_len,
+                                   float sm_scale, float *logits, void *stream, int num_seqs,
+                                   int64_t block_table_stride, int64_t num_pool_pages)
+{
+    const Args a{q,           q_is_e4m3, k_data,   k_scale, k_data_page_stride, k_scale_page_stride,
+                 block_table, nullptr,   seq_lens, nullptr, 1,                  max_seq_len,
+                 sm_scale,    logits,    static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+                 num_pool_pages};
+    return launch<true, true>(a);
+}
+
+mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t n, void *stream)
+{
+    if (n < 0) return MX4_ERR_INVALID_ARG;
+    if (n == 0) return MX4_OK;
+    if (!q_bf16 || !q_e4m3) return MX4_ERR_INVALID_ARG;
+    if (!aligned(q_bf16, 2)) return MX4_ERR_MISALIGNED;
+    const int vec = aligned(q_bf16, 16) && aligned(q_e4m3, 8);
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MX4_ERR_CUDA;
+    const int64_t work = vec ? (n + 7) / 8 : n;
+    int64_t blocks = (work + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    cudaGetLastError();
+    mx4::mx4_quantize_q_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        q_bf16, q_e4m3, n, vec);
+    return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
+}
+
+mx4_status mx4_index_get_device_status(void *stream, uint32_t *status_out)
+{
+    if (!status_out) return MX4_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MX4_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, mx4::g_mx4_device_status, sizeof v) != cudaSuccess) return MX4_ERR_CUDA;
+    if (cudaMemcpyToSymbol(mx4::g_mx4_device_status, &zero, sizeof zero) != cudaSuccess) return MX4_ERR_CUDA;
+    *status_out = v;
+    return MX4_OK;
+}
+
+const char *mx4_status_string(int status)
+{
+    switch (status) {
+    case MX4_OK: return "MX4_OK";
+    case MX4_ERR_INVALID_ARG: return "MX4_ERR_INVALID_ARG";
+    case MX4_ERR_MISALIGNED: return "MX4_ERR_MISALIGNED";
+    case MX4_ERR_UNSUPPORTED: return "MX4_ERR_UNSUPPORTED";
+    case MX4_ERR_CUDA: return "MX4_ERR_CUDA";
+    default: return "MX4_ERR_UNKNOWN";
+    }
+}
+
+int mx4_abi_version(void) { return MX4_ABI_VERSION; }
+
+}  // extern "C"

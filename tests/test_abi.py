@@ -1,0 +1,122 @@
+"""The C-ABI library loads and exports every symbol include/mx4_index.h
+declares; host-side argument checks reject bad calls before any CUDA call.
+CPU only: no call here reaches a kernel launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_mxfp4_gb300 as mx4
+from sparse_attention_mxfp4_gb300.buildlib import LIB_PATH, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mx4_index.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return mx4.load_library()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return re.findall(r"\b(mx4_[a-z0-9_]+)\s*\(", src)
+
+
+def test_header_declarations_match_exports(lib):
+    declared = _declared()
+    assert declared, "no declarations parsed"
+    assert sorted(declared) == sorted(mx4.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.mx4_abi_version() == 1
+    names = [lib.mx4_status_string(i).decode() for i in range(5)]
+    assert names == ["MX4_OK", "MX4_ERR_INVALID_ARG", "MX4_ERR_MISALIGNED", "MX4_ERR_UNSUPPORTED",
+                     "MX4_ERR_CUDA"]
+    assert lib.mx4_status_string(99).decode() == "MX4_ERR_UNKNOWN"
+
+
+# Fake, never dereferenced device addresses: every call below fails host
+# validation before the library touches CUDA.
+A = 1 << 20          # 1 MiB: aligned to everything
+GOOD = dict(q=A, e4=0, kd=A, ks=A + 8192, sd=8704, ss=8704, bt=A, cu=A, sl=A, pl=A,
+            mq=4, ms=1024, sm=0.088, out=A, stream=None, B=1, bts=8, npool=16)
+
+
+def _prefill(lib, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return lib.mx4_index_score_prefill(a["q"], a["e4"], a["kd"], a["ks"], a["sd"], a["ss"], a["bt"], a["cu"],
+                                       a["sl"], a["pl"], a["mq"], a["ms"], a["sm"], a["out"], a["stream"],
+                                       a["B"], a["bts"], a["npool"])
+
+
+def _decode(lib, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return lib.mx4_index_score_decode(a["q"], a["e4"], a["kd"], a["ks"], a["sd"], a["ss"], a["bt"], a["sl"],
+                                      a["ms"], a["sm"], a["out"], a["stream"], a["B"], a["bts"], a["npool"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(kd=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(out=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(cu=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(e4=2), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sd=8191 + 1 - 32), mx4.MX4_ERR_INVALID_ARG),          # narrow data view
+    (dict(ss=8704, sd=8704, ks=A + 8192, npool=0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(ss=496), mx4.MX4_ERR_INVALID_ARG),                   # narrow scale view
+    (dict(bts=7), mx4.MX4_ERR_INVALID_ARG),                    # narrow block table
+    (dict(ms=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(mq=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(B=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sm=0.0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sm=-1.0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sm=float("inf")), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sm=float("nan")), mx4.MX4_ERR_INVALID_ARG),
+    (dict(npool=1 << 31), mx4.MX4_ERR_UNSUPPORTED),
+    (dict(kd=A + 16), mx4.MX4_ERR_MISALIGNED),                 # 4-bit TMA wants 32 B
+    (dict(sd=8704 + 16, ss=8704 + 16), mx4.MX4_ERR_MISALIGNED),
+    (dict(ks=A + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(q=A + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(out=A + 4), mx4.MX4_ERR_MISALIGNED),
+])
+def test_prefill_rejections(lib, kw, status):
+    assert _prefill(lib, **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(sl=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(bt=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(bts=3), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sd=4096), mx4.MX4_ERR_INVALID_ARG),
+    (dict(kd=A + 48), mx4.MX4_ERR_MISALIGNED),
+])
+def test_decode_rejections(lib, kw, status):
+    # decode does not need cu_seqlens / prefix_lens
+    assert _decode(lib, cu=None, pl=None, **kw) == status
+
+
+def test_quantize_rejections(lib):
+    assert lib.mx4_quantize_q_e4m3(A, A, -1, None) == mx4.MX4_ERR_INVALID_ARG
+    assert lib.mx4_quantize_q_e4m3(None, A, 16, None) == mx4.MX4_ERR_INVALID_ARG
+    assert lib.mx4_quantize_q_e4m3(A, A, 0, None) == mx4.MX4_OK       # nothing to do
+    assert lib.mx4_quantize_q_e4m3(A + 1, A, 16, None) == mx4.MX4_ERR_MISALIGNED
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    missing = str(tmp_path / "nope.so")
+    saved = mx4._lib
+    try:
+        mx4._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            mx4.load_library(missing)
+    finally:
+        mx4._lib = saved
