@@ -6,18 +6,22 @@
 // decode, where lanes 64..127 stay zero).
 //
 // Roles (warp-specialised, 192 threads):
-//   warps 0-3  epilogue: load Q (bf16 -> e4m3 in registers) into a swizzled
-//              smem A tile; per page read the fp32 accumulator from TMEM,
-//              apply the causal mask, take the page max (or emit per-token
-//              logits), scale by sm_scale and store.
+//   warps 0-3  epilogue: load Q, round bf16 -> e4m3 in registers and store it
+//              into TMEM as the MMA's A operand (thread m owns TMEM lane m);
+//              per page read the fp32 accumulator from TMEM (tcgen05.ld.red
+//              returns the page max of a fully live page in the load itself),
+//              apply the causal mask on partial pages, scale by sm_scale and
+//              store (or emit per-token logits).
 //   warp 4     producer: per live page, look up the physical page id in the
 //              block table and issue two TMA loads: the 8 KB of e2m1 codes
 //              (unpacked in flight to the 16 KB padded layout the tensor core
 //              reads) and the 512 B of e8m0 scales.
 //   warp 5     MMA issuer: copies the page's scales into TMEM (tcgen05.cp)
 //              and issues 4 block-scaled MMAs (K = 32 each) of
-//              kind::mxf8f6f4: A = Q (e4m3, unit scale), B = K page (e2m1 with
-//              its e8m0 bytes), D = 128 x 128 fp32 in TMEM.
+//              kind::mxf8f6f4: A = Q from TMEM (e4m3, unit scale), B = K page
+//              from smem (e2m1 with its e8m0 bytes), D = 128 x 128 fp32 in TMEM.
+//              Only B is read from shared memory, so the operand traffic is
+//              16 KB per 128x128x128 MMA group.
 //
 // Token order inside the B tile: MMA column n holds token 4*(n%32) + n/32.
 // The 4-D tensor map that gathers the page performs this permutation, and it
@@ -40,24 +44,31 @@ constexpr int kDim = 128;
 constexpr int kPage = 128;
 constexpr int kDataBytes = 8192;                // packed e2m1 codes per page
 constexpr int kScaleBytes = 512;                // e8m0 bytes per page
-constexpr int kTileBytes = 128 * 128;           // one 128 x 128 operand tile in smem (8-bit slots)
-constexpr int kStages = 8;                      // smem pipeline depth (pages in flight)
+constexpr int kTileBytes = 128 * 128;           // one page in the padded 4-bit smem form
+constexpr int kStages = 12;                     // smem pipeline depth (pages in flight)
 constexpr int kDBufs = 3;                       // TMEM accumulator buffers
 constexpr int kSfbBufs = 4;                     // TMEM scale-factor buffers for B
 constexpr int kChunk = 8;                       // pages per work unit
-constexpr int kThreads = 192;
+constexpr int kMmaWarps = 2;                    // MMA-issuing warps (alternate pages)
+constexpr int kThreads = 32 * (6 + kMmaWarps);  // 4 epilogue, TMA, scale copy, MMA issuers
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemSfaCol = kDBufs * 128;          // 384
-constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4;       // 388
+// TMEM columns: D[3] x 128 | A (query tile, e4m3) [2] x 32 | SFA 4 | SFB[4] x 4
+constexpr uint32_t kTmemACol = kDBufs * 128;                 // 384
+constexpr uint32_t kTmemSfaCol = kTmemACol + 2 * 32;         // 448
+constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4;            // 452
 // Transaction bytes of one page: the 4-bit TMA load counts the packed
 // global bytes (8192), not the 16 KB it writes in the padded smem form.
 constexpr uint32_t kStageTxBytes = kDataBytes + kScaleBytes;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;        // 1 s per wait
+constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s per wait
+
+static_assert(kTmemSfbCol + 4 * kSfbBufs <= kTmemCols, "TMEM budget");
+static_assert(kSfbBufs > kDBufs, "an SFB buffer is reused only after its MMA retired");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling:
 // A = E4M3 (0, bits 7..9), B = E2M1 (5, bits 10..12), both K-major,
 // N >> 3 in bits 17..22, scale type UE8M0 (bit 23), M >> 4 in bits 24..28,
-// B scale-factor id in bits 4..5, A scale-factor id in bits 29..30.
+// B scale-factor id in bits 4..5, A scale-factor id in bits 29..30 (the id
+// picks byte k of each 32-bit scale word for the k-th 32-element block).
 constexpr uint32_t kIdescBase = (0u << 7) | (5u << 10) | ((128u >> 3) << 17) | (1u << 23) |
                                 ((128u >> 4) << 24);
 
@@ -90,29 +101,29 @@ struct ScoreParams {
 // Shared memory carve-up (offsets from a 1024-aligned base).
 struct SmemLayout {
     static constexpr uint32_t kData = 0;                                   // kStages x 16 KB
-    static constexpr uint32_t kQ = kData + kStages * kTileBytes;           // 2 x 16 KB
-    static constexpr uint32_t kScale = kQ + 2 * kTileBytes;                // kStages x 512 B
+    static constexpr uint32_t kScale = kData + kStages * kTileBytes;       // kStages x 512 B
     static constexpr uint32_t kSfa = kScale + kStages * kScaleBytes;       // 512 B of 0x7F
     static constexpr uint32_t kStage = kSfa + kScaleBytes;                 // 128 x kChunk floats
     static constexpr uint32_t kBars = kStage + 128 * kChunk * 4;
-    // barriers: full[kStages], empty[kStages], dfull[kDBufs], dempty[kDBufs],
-    //           qfull[2], qempty[2], final
-    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kDBufs + 4 + 1;
+    // barriers: full[kStages], empty[kStages], sfready[kSfbBufs], sfempty[kSfbBufs],
+    //           dfull[kDBufs], dempty[kDBufs], qfull[2], qempty[2], final[kMmaWarps + 1]
+    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 4 + kMmaWarps + 1;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
     static constexpr uint32_t kAlloc = kEnd + 1024;                        // + alignment slack
 };
+static_assert(SmemLayout::kAlloc <= 227 * 1024, "shared memory budget");
 
-struct Unit {
-    int64_t tile;      // global tile id = b * tiles_per_seq + t
+// One tile: R query rows (R = 2 prefill, 1 decode) x 64 heads = 128 A rows.
+struct TileInfo {
+    int64_t tile;      // global tile id = b * tiles_per_seq + t (-1: none)
     int64_t row0;      // first global query row of the tile
     int b;
     int nrows;         // rows of the tile (0 = tile does not exist)
     int pos0;          // position of the tile's first row within its request
-    int j0, j1;        // page range of the unit [j0, j1)
     int live_end;      // pages [0, live_end) hold a live token for some row
-    int L0;            // live limit of the tile's first row
+    int L[2];          // live limit of each row of the tile
 };
 
 template <bool kDecode>
@@ -132,40 +143,35 @@ __device__ __forceinline__ int live_limit(const ScoreParams &p, int b, int row_p
 }
 
 template <bool kDecode>
-__device__ __forceinline__ Unit decode_unit(const ScoreParams &p, int64_t u)
+__device__ __forceinline__ TileInfo tile_info(const ScoreParams &p, int64_t tile)
 {
     constexpr int R = kDecode ? 1 : 2;
-    Unit w;
-    w.tile = u / p.chunks_per_tile;
-    const int chunk = static_cast<int>(u - w.tile * p.chunks_per_tile);
-    w.b = static_cast<int>(w.tile / p.tiles_per_seq);
-    const int t = static_cast<int>(w.tile - static_cast<int64_t>(w.b) * p.tiles_per_seq);
-    int first_pos;
+    TileInfo ti;
+    ti.tile = tile;
+    ti.b = static_cast<int>(tile / p.tiles_per_seq);
+    const int t = static_cast<int>(tile - static_cast<int64_t>(ti.b) * p.tiles_per_seq);
     if (kDecode) {
-        w.row0 = w.b;
-        w.nrows = 1;
-        first_pos = 0;
+        ti.row0 = ti.b;
+        ti.nrows = 1;
+        ti.pos0 = 0;
     } else {
-        const int qs = p.cu_seqlens_q[w.b];
-        const int ql = p.cu_seqlens_q[w.b + 1] - qs;
-        first_pos = t * R;
-        w.nrows = ql - first_pos;
-        if (w.nrows > R) w.nrows = R;
-        if (w.nrows < 0) w.nrows = 0;
-        w.row0 = static_cast<int64_t>(qs) + first_pos;
+        const int qs = p.cu_seqlens_q[ti.b];
+        const int ql = p.cu_seqlens_q[ti.b + 1] - qs;
+        ti.pos0 = t * R;
+        ti.nrows = ql - ti.pos0;
+        if (ti.nrows > R) ti.nrows = R;
+        if (ti.nrows < 0) ti.nrows = 0;
+        ti.row0 = static_cast<int64_t>(qs) + ti.pos0;
     }
-    w.pos0 = first_pos;
-    w.j0 = chunk * kChunk;
-    w.j1 = w.j0 + kChunk < p.num_out_pages ? w.j0 + kChunk : p.num_out_pages;
-    if (w.nrows > 0) {
-        w.L0 = live_limit<kDecode>(p, w.b, first_pos);
-        const int Llast = live_limit<kDecode>(p, w.b, first_pos + w.nrows - 1);
-        w.live_end = (Llast + kPage - 1) / kPage;
-    } else {
-        w.L0 = 0;
-        w.live_end = 0;
+    ti.L[0] = ti.L[1] = 0;
+    ti.live_end = 0;
+    if (ti.nrows > 0) {
+        ti.L[0] = live_limit<kDecode>(p, ti.b, ti.pos0);
+        ti.L[1] = ti.nrows > 1 ? live_limit<kDecode>(p, ti.b, ti.pos0 + 1) : ti.L[0];
+        const int Lmax = ti.L[0] > ti.L[1] ? ti.L[0] : ti.L[1];
+        ti.live_end = (Lmax + kPage - 1) / kPage;
     }
-    return w;
+    return ti;
 }
 
 // Wait sites, recorded as status bit (8 + site) when a wait gives up.
@@ -176,13 +182,15 @@ enum WaitSite : uint32_t {
     kSiteMmaDEmpty = 3,
     kSiteEpiQEmpty = 4,
     kSiteEpiDFull = 5,
+    kSiteScaleFull = 6,
+    kSiteScaleEmpty = 7,
 };
 
 // Bounded wait: true when the phase completed; false after the time limit or
 // when another role has aborted (then the status word carries the reason:
 // bit 1 = timeout, bit 8 + site = where the wait gave up).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                             unsigned int *status, uint32_t site)
+                                             uint32_t site)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -190,7 +198,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(status, 0x2u | (0x100u << site));
+            atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
             *abort_flag = 1;
             return false;
         }
@@ -206,56 +214,44 @@ __device__ __forceinline__ bool tile_has_rows(const ScoreParams &p, int64_t tile
     return p.cu_seqlens_q[b + 1] - p.cu_seqlens_q[b] > t * 2;
 }
 
-// Write one tile of Q (R rows x 64 heads, rounded to e4m3) into the swizzled
-// K-major smem A layout: row m at (m/8)*1024 + (m%8)*128, 16-byte chunk c
-// stored at chunk position c ^ (m%8).  Thread m owns A row m.
+// Round this thread's query row (A row m = row m/64 of the tile, head m%64)
+// to e4m3 and store it into TMEM lane m, 32 columns of 4 bytes (element 4c+i
+// in byte i of column c).  Rows past the tile's end are zero.
 template <bool kDecode>
-__device__ __forceinline__ void load_q_tile(const ScoreParams &p, int64_t tile, uint8_t *qbuf, int m)
+__device__ __forceinline__ void load_q_tile_tmem(const ScoreParams &p, const TileInfo &ti, uint32_t taddr,
+                                                 int m)
 {
-    constexpr int R = kDecode ? 1 : 2;
-    const int b = static_cast<int>(tile / p.tiles_per_seq);
-    const int t = static_cast<int>(tile - static_cast<int64_t>(b) * p.tiles_per_seq);
-    int64_t row0;
-    int nrows;
-    if (kDecode) {
-        row0 = b;
-        nrows = 1;
-    } else {
-        const int qs = p.cu_seqlens_q[b];
-        const int ql = p.cu_seqlens_q[b + 1] - qs;
-        nrows = ql - t * R;
-        if (nrows > R) nrows = R;
-        row0 = static_cast<int64_t>(qs) + t * R;
-    }
     const int ri = m / kHeads;
     const int h = m % kHeads;
-    uint4 chunks[8];
-    if (ri < nrows) {
-        const int64_t line = (row0 + ri) * kHeads + h;
+    uint32_t w[32];
+    if (ri < ti.nrows) {
+        const int64_t line = (ti.row0 + ri) * kHeads + h;
         if (p.q_is_e4m3) {
             const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(p.q) + line * kDim);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) chunks[c] = __ldg(src + c);
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = __ldg(src + c);
+                w[4 * c + 0] = x.x;
+                w[4 * c + 1] = x.y;
+                w[4 * c + 2] = x.z;
+                w[4 * c + 3] = x.w;
+            }
         } else {
             const uint4 *src =
                 reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(p.q) + line * kDim);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint2 lo = bf16x8_to_e4m3x8(__ldg(src + 2 * c));
-                const uint2 hi = bf16x8_to_e4m3x8(__ldg(src + 2 * c + 1));
-                chunks[c] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            for (int c = 0; c < 16; ++c) {
+                const uint2 e = bf16x8_to_e4m3x8(__ldg(src + c));
+                w[2 * c + 0] = e.x;
+                w[2 * c + 1] = e.y;
             }
         }
     } else {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) chunks[c] = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < 32; ++c) w[c] = 0u;
     }
-    uint8_t *row = qbuf + (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(row + ((c ^ (m & 7)) << 4)) = chunks[c];
+    tmem_st_32x32b_x32(taddr, w);
 }
-
-__device__ __forceinline__ float fmax3(float a, float b, float c) { return fmaxf(a, fmaxf(b, c)); }
 
 // MMA column n holds token 4*(n%32) + n/32.
 __device__ __forceinline__ int token_of_col(int n) { return ((n & 31) << 2) | (n >> 5); }
@@ -271,31 +267,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // Every role walks the same sequence of computed pages; page number pc
+    // uses smem stage pc % kStages, scale buffer pc % kSfbBufs and
+    // accumulator pc % kDBufs, and is issued by MMA warp pc % kMmaWarps.
     auto bar = [&](int i) { return sbase + SmemLayout::kBars + 8u * i; };
-    auto full_bar = [&](int s) { return bar(s); };
-    auto empty_bar = [&](int s) { return bar(kStages + s); };
-    auto dfull_bar = [&](int d) { return bar(2 * kStages + d); };
-    auto dempty_bar = [&](int d) { return bar(2 * kStages + kDBufs + d); };
-    auto qfull_bar = [&](int q) { return bar(2 * kStages + 2 * kDBufs + q); };
-    auto qempty_bar = [&](int q) { return bar(2 * kStages + 2 * kDBufs + 2 + q); };
-    const uint32_t final_bar = bar(2 * kStages + 2 * kDBufs + 4);
+    auto full_bar = [&](int i) { return bar(i); };
+    auto empty_bar = [&](int i) { return bar(kStages + i); };
+    auto sfready_bar = [&](int i) { return bar(2 * kStages + i); };
+    auto sfempty_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + i); };
+    auto dfull_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + i); };
+    auto dempty_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + kDBufs + i); };
+    auto qfull_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + 2 * kDBufs + i); };
+    auto qempty_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 2 + i); };
+    auto final_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 4 + i); };
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + SmemLayout::kAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::kTmemSlot);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(full_bar(i), 1);
+            mbar_init(empty_bar(i), 1);
         }
-        for (int d = 0; d < kDBufs; ++d) {
-            mbar_init(dfull_bar(d), 1);
-            mbar_init(dempty_bar(d), 4);
+        for (int i = 0; i < kSfbBufs; ++i) {
+            mbar_init(sfready_bar(i), 1);
+            mbar_init(sfempty_bar(i), 1);
         }
-        for (int q = 0; q < 2; ++q) {
-            mbar_init(qfull_bar(q), 4);
-            mbar_init(qempty_bar(q), 1);
+        for (int i = 0; i < kDBufs; ++i) {
+            mbar_init(dfull_bar(i), 1);
+            mbar_init(dempty_bar(i), 4);
         }
-        mbar_init(final_bar, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull_bar(i), 4);
+            mbar_init(qempty_bar(i), kMmaWarps);
+        }
+        for (int i = 0; i <= kMmaWarps; ++i) mbar_init(final_bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -322,31 +327,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 4) {
         // ------------------------------------------------------- producer --
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            for (int64_t u = u_begin; u < u_end && !*abort_flag; ++u) {
-                const Unit w = decode_unit<kDecode>(p, u);
-                if (w.nrows <= 0) continue;
-                const int jc = w.j1 < w.live_end ? w.j1 : w.live_end;
-                for (int j = w.j0; j < jc; ++j) {
-                    int64_t pid = p.block_table[static_cast<int64_t>(w.b) * p.bt_stride + j];
-                    if (pid < 0 || pid >= p.num_pool_pages) {
-                        atomicOr(&g_mx4_device_status, 0x1u);
-                        pid = 0;
-                    }
-                    if (!wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, &g_mx4_device_status, kSiteProducerEmpty)) break;
-                    mbar_arrive_expect_tx(full_bar(s), kStageTxBytes);
-                    tma_load_4d(sbase + SmemLayout::kData + s * kTileBytes, &tmap_k, full_bar(s), 0, 0, 0,
-                                static_cast<int>(pid));
-                    tma_load_2d(sbase + SmemLayout::kScale + s * kScaleBytes, &tmap_s, full_bar(s), 0,
-                                static_cast<int>(pid));
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
+        // The whole warp walks the units; lane i fetches the page id of the
+        // unit's i-th live page, lane 0 issues the TMA loads.
+        const uint64_t policy = kDecode ? l2_policy_evict_first() : l2_policy_evict_last();
+        int s = 0;
+        uint32_t ph = 0;
+        TileInfo ti;
+        ti.tile = -1;
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok; ++u) {
+            const int64_t tile = u / p.chunks_per_tile;
+            if (tile != ti.tile) ti = tile_info<kDecode>(p, tile);
+            if (ti.nrows <= 0) continue;
+            const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+            const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
+            const int jc = j1 < ti.live_end ? j1 : ti.live_end;
+            const int n = jc - j0;
+            if (n <= 0) continue;
+            int pid = 0;
+            if (lane < n) {
+                const int64_t v = p.block_table[static_cast<int64_t>(ti.b) * p.bt_stride + j0 + lane];
+                if (v < 0 || v >= p.num_pool_pages) {
+                    atomicOr(&g_mx4_device_status, 0x1u);
+                } else {
+                    pid = static_cast<int>(v);
                 }
             }
+            for (int i = 0; i < n; ++i) {
+                const int id = __shfl_sync(0xffffffffu, pid, i);
+                int go = 1;
+                if (lane == 0) {
+                    go = wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kSiteProducerEmpty);
+                    if (go) {
+                        mbar_arrive_expect_tx(full_bar(s), kStageTxBytes);
+                        tma_load_4d(sbase + SmemLayout::kData + s * kTileBytes, &tmap_k, full_bar(s), 0, 0, 0, id,
+                                    policy);
+                        tma_load_2d(sbase + SmemLayout::kScale + s * kScaleBytes, &tmap_s, full_bar(s), 0, id,
+                                    policy);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (++s == kStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (lane == 0) {
             // Do not leave while copies into this CTA's smem may be in flight:
             // every armed stage completes (bounded) before the CTA exits.
             for (int i = 0; i < kStages; ++i) {
@@ -357,66 +387,114 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        __syncwarp();
     } else if (warp == 5) {
-        // ----------------------------------------------------- MMA issuer --
+        // ------------------------------------------------ scale-factor copy --
+        // Per page: once its bytes have landed and its TMEM scale buffer is
+        // free, copy the 512 B scale block into TMEM (tcgen05.cp) and signal
+        // the MMA warps.  The constant unit scale of A is copied first.
+        if (lane == 0) {
+            tc_cp_32x128b_warpx4(tmem_base + kTmemSfaCol, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
+            int s = 0, x = 0;
+            uint32_t ph = 0, xph = 0;
+            TileInfo ti;
+            ti.tile = -1;
+            bool ok = true;
+            for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u) {
+                const int64_t tile = u / p.chunks_per_tile;
+                if (tile != ti.tile) ti = tile_info<kDecode>(p, tile);
+                if (ti.nrows <= 0) continue;
+                const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+                const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
+                const int jc = j1 < ti.live_end ? j1 : ti.live_end;
+                for (int j = j0; j < jc; ++j) {
+                    if (!wait_bounded(full_bar(s), ph, abort_flag, kSiteScaleFull) ||
+                        !wait_bounded(sfempty_bar(x), xph ^ 1u, abort_flag, kSiteScaleEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tc_cp_32x128b_warpx4(tmem_base + kTmemSfbCol + 4u * x,
+                                         smem_desc(sbase + SmemLayout::kScale + s * kScaleBytes, 16, 128, 0));
+                    tc_commit(sfready_bar(x));
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (++x == kSfbBufs) {
+                        x = 0;
+                        xph ^= 1u;
+                    }
+                }
+            }
+            tc_commit(final_bar(kMmaWarps));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(final_bar(kMmaWarps), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ----------------------------------------------------- MMA issuers --
+        // Issuer i takes the computed pages with pc % kMmaWarps == i; each
+        // tcgen05 instruction costs its issuing thread tens of cycles, so the
+        // pages are spread over several issuing warps.
+        const int issuer = warp - 6;
         if (lane == 0) {
             const uint32_t tmem_sfa = tmem_base + kTmemSfaCol;
-            tc_cp_32x128b_warpx4(tmem_sfa, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
-            int s = 0, d = 0, x = 0;
-            uint32_t ph = 0, dph = 0;
-            int64_t cur_tile = -1, qcount = 0;
+            int64_t pc = 0, qcount = 0;
             uint32_t qbuf = 0;
-            for (int64_t u = u_begin; u < u_end && !*abort_flag; ++u) {
-                const Unit w = decode_unit<kDecode>(p, u);
-                if (w.nrows <= 0) continue;
-                if (w.tile != cur_tile) {
-                    if (cur_tile >= 0) tc_commit(qempty_bar(static_cast<int>((qcount - 1) & 1)));
-                    cur_tile = w.tile;
-                    const int64_t qi = qcount++;
-                    qbuf = static_cast<uint32_t>(qi & 1);
-                    if (!wait_bounded(qfull_bar(qbuf), static_cast<uint32_t>((qi >> 1) & 1), abort_flag, &g_mx4_device_status,
-                                      kSiteMmaQFull))
-                        break;
-                    tc_fence_after();
+            TileInfo ti;
+            ti.tile = -1;
+            bool ok = true, holding_q = false;
+            for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u) {
+                const int64_t tile = u / p.chunks_per_tile;
+                if (tile != ti.tile) {
+                    ti = tile_info<kDecode>(p, tile);
+                    if (ti.nrows > 0) {
+                        // the previous query tile's buffer is free once its MMAs retire
+                        if (holding_q) tc_commit(qempty_bar(static_cast<int>((qcount - 1) & 1)));
+                        const int64_t qi = qcount++;
+                        qbuf = static_cast<uint32_t>(qi & 1);
+                        holding_q = true;
+                        if (!wait_bounded(qfull_bar(qbuf), static_cast<uint32_t>((qi >> 1) & 1), abort_flag,
+                                          kSiteMmaQFull))
+                            break;
+                        tc_fence_after();
+                    }
                 }
-                const int jc = w.j1 < w.live_end ? w.j1 : w.live_end;
-                bool ok = true;
-                for (int j = w.j0; j < jc; ++j) {
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, &g_mx4_device_status, kSiteMmaFull) ||
-                        !wait_bounded(dempty_bar(d), dph ^ 1u, abort_flag, &g_mx4_device_status, kSiteMmaDEmpty)) {
+                if (ti.nrows <= 0) continue;
+                const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+                const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
+                const int jc = j1 < ti.live_end ? j1 : ti.live_end;
+                const uint32_t a_tmem = tmem_base + kTmemACol + qbuf * 32u;
+                for (int j = j0; j < jc; ++j, ++pc) {
+                    if (static_cast<int>(pc % kMmaWarps) != issuer) continue;
+                    const int s = static_cast<int>(pc % kStages);
+                    const int x = static_cast<int>(pc % kSfbBufs);
+                    const int d = static_cast<int>(pc % kDBufs);
+                    const uint32_t xph = static_cast<uint32_t>((pc / kSfbBufs) & 1);
+                    const uint32_t dph = static_cast<uint32_t>((pc / kDBufs) & 1);
+                    if (!wait_bounded(sfready_bar(x), xph, abort_flag, kSiteMmaFull) ||
+                        !wait_bounded(dempty_bar(d), dph ^ 1u, abort_flag, kSiteMmaDEmpty)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * x;
-                    tc_cp_32x128b_warpx4(tmem_sfb, smem_desc(sbase + SmemLayout::kScale + s * kScaleBytes, 16, 128, 0));
-                    const uint32_t a_addr = sbase + SmemLayout::kQ + qbuf * kTileBytes;
                     const uint32_t b_addr = sbase + SmemLayout::kData + s * kTileBytes;
                     const uint32_t d_tmem = tmem_base + d * 128u;
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k) {
-                        tc_mma_mx_ss(d_tmem, smem_desc(a_addr + 32u * k, 16, 1024, 2),
-                                     smem_desc(b_addr + 32u * k, 16, 1024, 2), idesc_for_k(k), tmem_sfa, tmem_sfb,
-                                     k > 0 ? 1u : 0u);
+                        tc_mma_mx_ts(d_tmem, a_tmem + 8u * k, smem_desc(b_addr + 32u * k, 16, 1024, 2),
+                                     idesc_for_k(k), tmem_sfa, tmem_sfb, k > 0 ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(s));
                     tc_commit(dfull_bar(d));
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                    if (++d == kDBufs) {
-                        d = 0;
-                        dph ^= 1u;
-                    }
-                    if (++x == kSfbBufs) x = 0;
                 }
-                if (!ok) break;
             }
-            // all MMAs and copies retire before TMEM is released
-            tc_commit(final_bar);
+            // all MMAs retire before TMEM is released
+            tc_commit(final_bar(issuer));
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(final_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(final_bar(issuer), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
             }
         }
         __syncwarp();
@@ -428,101 +506,121 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
         float *stage = reinterpret_cast<float *>(smem + SmemLayout::kStage) + m * kChunk;
         const float sm_scale = p.sm_scale;
-        int d = 0;
+        int d = 0, s = 0, x = 0;
         uint32_t dph = 0;
-        int64_t cur_tile = -1, qcount = 0;
+        int64_t qcount = 0;
+        TileInfo ti;
+        ti.tile = -1;
 
-        auto q_load = [&](int64_t tile, int64_t qi) -> bool {
+        // Load the query tile of `t` into A buffer qi & 1 once the MMAs of the
+        // tile that used that buffer before have retired.
+        auto q_load = [&](const TileInfo &t, int64_t qi) -> bool {
             const int buf = static_cast<int>(qi & 1);
             // warp-uniform outcome, so the .sync.aligned operations below never diverge
             if (!__all_sync(0xffffffffu, wait_bounded(qempty_bar(buf), static_cast<uint32_t>(((qi >> 1) & 1) ^ 1),
-                                                      abort_flag, &g_mx4_device_status, kSiteEpiQEmpty)))
+                                                      abort_flag, kSiteEpiQEmpty)))
                 return false;
-            load_q_tile<kDecode>(p, tile, smem + SmemLayout::kQ + buf * kTileBytes, m);
-            fence_proxy_async_smem();
+            tc_fence_after();
+            load_q_tile_tmem<kDecode>(p, t, tmem_base + lane_addr + kTmemACol + buf * 32u, m);
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(qfull_bar(buf));
             return true;
         };
 
-        for (int64_t u = u_begin; u < u_end && !__any_sync(0xffffffffu, *abort_flag != 0); ++u) {
-            const Unit w = decode_unit<kDecode>(p, u);
-            if (w.nrows <= 0) continue;
-            if (w.tile != cur_tile) {
-                if (qcount == 0 && !q_load(w.tile, 0)) break;
-                cur_tile = w.tile;
+        bool ok = true;
+        for (int64_t u = u_begin; u < u_end && ok && !__any_sync(0xffffffffu, *abort_flag != 0); ++u) {
+            const int64_t tile = u / p.chunks_per_tile;
+            if (tile != ti.tile) {
+                const TileInfo nt_info = tile_info<kDecode>(p, tile);
+                if (nt_info.nrows <= 0) continue;   // keeps ti: units of this tile are skipped below
+                ti = nt_info;
+                if (qcount == 0 && !q_load(ti, 0)) break;
                 const int64_t qi = qcount++;
                 // prefetch the next tile with rows in this CTA's range
-                int64_t nt = w.tile + 1;
+                int64_t nt = tile + 1;
                 while (nt * p.chunks_per_tile < u_end && !tile_has_rows<kDecode>(p, nt)) ++nt;
                 if (nt * p.chunks_per_tile < u_end) {
-                    if (!q_load(nt, qi + 1)) break;
+                    if (!q_load(tile_info<kDecode>(p, nt), qi + 1)) break;
                 }
             }
-            const bool has_row = ri < w.nrows;
-            const int L = has_row ? (ri == 0 ? w.L0 : live_limit<kDecode>(p, w.b, w.pos0 + ri)) : 0;
-            const int64_t line = (w.row0 + ri) * kHeads + h;
-            bool ok = true;
-            for (int j = w.j0; j < w.j1; ++j) {
+            const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+            const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
+            const bool has_row = ri < ti.nrows;     // uniform per warp
+            const int L = has_row ? (ri == 0 ? ti.L[0] : ti.L[1]) : 0;
+            const int64_t line = (ti.row0 + ri) * kHeads + h;
+            for (int j = j0; j < j1; ++j) {
                 const int lim = L - j * kPage;   // live tokens of page j for this row
-                if (j < w.live_end) {
-                    if (!__all_sync(0xffffffffu, wait_bounded(dfull_bar(d), dph, abort_flag, &g_mx4_device_status, kSiteEpiDFull))) {
+                if (j < ti.live_end) {
+                    if (!__all_sync(0xffffffffu, wait_bounded(dfull_bar(d), dph, abort_flag, kSiteEpiDFull))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t v[128];
-                    tmem_ld_32x32b_x128(tmem_base + lane_addr + d * 128u, v);
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(dempty_bar(d));
+                    // the page's MMAs have retired: its smem stage and scale
+                    // buffer can be refilled
+                    if (m == 0) {
+                        mbar_arrive(empty_bar(s));
+                        mbar_arrive(sfempty_bar(x));
+                    }
+                    if (++s == kStages) s = 0;
+                    if (++x == kSfbBufs) x = 0;
+                    const uint32_t taddr = tmem_base + lane_addr + d * 128u;
+                    if (has_row) {
+                        uint32_t v[128];
+                        if (!kLogits) {
+                            float mx;
+                            if (lim >= kPage) {
+                                mx = tmem_ld_max_32x32b_x128(taddr, v);
+                            } else {
+                                tmem_ld_32x32b_x128(taddr, v);
+                                mx = -INFINITY;
+#pragma unroll
+                                for (int n = 0; n < 128; ++n)
+                                    if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
+                            }
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(dempty_bar(d));
+                            stage[j - j0] = mx * sm_scale;
+                        } else {
+                            tmem_ld_32x32b_x128(taddr, v);
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(dempty_bar(d));
+                            float *dst = p.out + line * p.out_row_stride + static_cast<int64_t>(j) * kPage;
+                            const int valid = p.max_seq_len - j * kPage;   // columns that exist
+                            const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
+#pragma unroll
+                            for (int g = 0; g < 32; ++g) {
+                                float4 o;
+                                o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
+                                o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
+                                o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
+                                o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
+                                if (vec) {
+                                    __stcs(reinterpret_cast<float4 *>(dst + 4 * g), o);
+                                } else {
+                                    if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
+                                    if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
+                                    if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
+                                    if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
+                                }
+                            }
+                        }
+                    } else {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dempty_bar(d));
+                    }
                     if (++d == kDBufs) {
                         d = 0;
                         dph ^= 1u;
                     }
-                    if (!has_row) continue;
-                    if (!kLogits) {
-                        float mx;
-                        if (lim >= kPage) {
-                            float a = __uint_as_float(v[0]), b2 = __uint_as_float(v[1]);
-#pragma unroll
-                            for (int n = 2; n < 128; n += 2) {
-                                a = fmaxf(a, __uint_as_float(v[n]));
-                                b2 = fmaxf(b2, __uint_as_float(v[n + 1]));
-                            }
-                            mx = fmaxf(a, b2);
-                        } else {
-                            mx = -INFINITY;
-#pragma unroll
-                            for (int n = 0; n < 128; ++n)
-                                if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
-                        }
-                        stage[j - w.j0] = mx * sm_scale;
-                    } else {
-                        float *dst = p.out + line * p.out_row_stride + static_cast<int64_t>(j) * kPage;
-                        const int valid = p.max_seq_len - j * kPage;   // columns that exist
-                        const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
-#pragma unroll
-                        for (int g = 0; g < 32; ++g) {
-                            float4 o;
-                            o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
-                            o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
-                            o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
-                            o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
-                            if (vec) {
-                                *reinterpret_cast<float4 *>(dst + 4 * g) = o;
-                            } else {
-                                if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
-                                if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
-                                if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
-                                if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
-                            }
-                        }
-                    }
                 } else if (has_row) {
                     // no row of the tile sees this page: nothing was computed
                     if (!kLogits) {
-                        stage[j - w.j0] = -INFINITY;
+                        stage[j - j0] = -INFINITY;
                     } else {
                         float *dst = p.out + line * p.out_row_stride + static_cast<int64_t>(j) * kPage;
                         const int valid = p.max_seq_len - j * kPage;
@@ -532,16 +630,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             if (!kLogits && has_row) {
-                float *dst = p.out + line * p.out_row_stride + w.j0;
-                const int n = w.j1 - w.j0;
+                float *dst = p.out + line * p.out_row_stride + j0;
+                const int n = j1 - j0;
                 if (n == kChunk && (p.out_row_stride & 3) == 0) {
                     const float4 *src = reinterpret_cast<const float4 *>(stage);
-                    reinterpret_cast<float4 *>(dst)[0] = src[0];
-                    reinterpret_cast<float4 *>(dst)[1] = src[1];
+                    __stcs(reinterpret_cast<float4 *>(dst), src[0]);
+                    __stcs(reinterpret_cast<float4 *>(dst) + 1, src[1]);
                 } else if (n == kChunk && (p.out_row_stride & 1) == 0) {
                     const float2 *src = reinterpret_cast<const float2 *>(stage);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) reinterpret_cast<float2 *>(dst)[i] = src[i];
+                    for (int i = 0; i < 4; ++i) __stcs(reinterpret_cast<float2 *>(dst) + i, src[i]);
                 } else {
                     for (int i = 0; i < n; ++i) dst[i] = stage[i];
                 }
