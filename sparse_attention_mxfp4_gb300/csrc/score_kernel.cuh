@@ -47,12 +47,21 @@ constexpr int kScaleBytes = 512;                // e8m0 bytes per page
 constexpr int kTileBytes = 128 * 128;           // one page in the padded 4-bit smem form
 constexpr int kStages = 12;                     // smem pipeline depth (pages in flight)
 constexpr int kDBufs = 3;                       // TMEM accumulator buffers
-constexpr int kSfbBufs = 4;                     // TMEM scale-factor buffers for B
+constexpr int kSfbBufs = 12;                    // TMEM scale-factor buffers for B
 constexpr int kChunk = 8;                       // pages per work unit
-constexpr int kMmaWarps = 2;                    // MMA-issuing warps (alternate pages)
-constexpr int kThreads = 32 * (6 + kMmaWarps);  // 4 epilogue, TMA, scale copy, MMA issuers
+// Warp roles: two epilogue warpgroups (warps 0-3 and 4-7; warp w reads TMEM
+// lane quadrant w % 4) take alternate pages; two TMA producer warps take
+// alternate pages; one warp copies scales into TMEM (and owns the TMEM
+// allocation); the MMA warps take alternate pages.
+constexpr int kEpiSets = 2;
+constexpr int kProdWarps = 2;
+constexpr int kMmaWarps = 1;
+constexpr int kProdWarp0 = 4 * kEpiSets;                 // 8
+constexpr int kScaleWarp = kProdWarp0 + kProdWarps;      // 10
+constexpr int kMmaWarp0 = kScaleWarp + 1;                // 11
+constexpr int kThreads = 32 * (kMmaWarp0 + kMmaWarps);
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D[3] x 128 | A (query tile, e4m3) [2] x 32 | SFA 4 | SFB[4] x 4
+// TMEM columns: D[3] x 128 | A (query tile, e4m3) [2] x 32 | SFA 4 | SFB[12] x 4
 constexpr uint32_t kTmemACol = kDBufs * 128;                 // 384
 constexpr uint32_t kTmemSfaCol = kTmemACol + 2 * 32;         // 448
 constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4;            // 452
@@ -63,6 +72,7 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s per wait
 
 static_assert(kTmemSfbCol + 4 * kSfbBufs <= kTmemCols, "TMEM budget");
 static_assert(kSfbBufs > kDBufs, "an SFB buffer is reused only after its MMA retired");
+static_assert(kStages % kProdWarps == 0, "each producer warp owns a fixed set of stages");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling:
 // A = E4M3 (0, bits 7..9), B = E2M1 (5, bits 10..12), both K-major,
@@ -103,8 +113,7 @@ struct SmemLayout {
     static constexpr uint32_t kData = 0;                                   // kStages x 16 KB
     static constexpr uint32_t kScale = kData + kStages * kTileBytes;       // kStages x 512 B
     static constexpr uint32_t kSfa = kScale + kStages * kScaleBytes;       // 512 B of 0x7F
-    static constexpr uint32_t kStage = kSfa + kScaleBytes;                 // 128 x kChunk floats
-    static constexpr uint32_t kBars = kStage + 128 * kChunk * 4;
+    static constexpr uint32_t kBars = kSfa + kScaleBytes;
     // barriers: full[kStages], empty[kStages], sfready[kSfbBufs], sfempty[kSfbBufs],
     //           dfull[kDBufs], dempty[kDBufs], qfull[2], qempty[2], final[kMmaWarps + 1]
     static constexpr uint32_t kNumBars = 2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 4 + kMmaWarps + 1;
@@ -253,6 +262,47 @@ __device__ __forceinline__ void load_q_tile_tmem(const ScoreParams &p, const Til
     tmem_st_32x32b_x32(taddr, w);
 }
 
+// Walks a CTA's contiguous unit range as (tile, chunk) without a division
+// per unit.
+struct UnitCursor {
+    int64_t tile;
+    int chunk;
+    int64_t left;   // units remaining, this one included
+};
+
+__device__ __forceinline__ UnitCursor cursor_begin(const ScoreParams &p, int64_t u_begin, int64_t u_end)
+{
+    UnitCursor c;
+    c.tile = u_begin / p.chunks_per_tile;
+    c.chunk = static_cast<int>(u_begin - c.tile * p.chunks_per_tile);
+    c.left = u_end - u_begin;
+    return c;
+}
+
+__device__ __forceinline__ void cursor_next(const ScoreParams &p, UnitCursor &c)
+{
+    --c.left;
+    if (++c.chunk == p.chunks_per_tile) {
+        c.chunk = 0;
+        ++c.tile;
+    }
+}
+
+// Position in a ring of N slots and the parity of the slot's current use.
+struct Ring {
+    int idx = 0;
+    uint32_t ph = 0;
+};
+
+template <int N>
+__device__ __forceinline__ void ring_next(Ring &r)
+{
+    if (++r.idx == N) {
+        r.idx = 0;
+        r.ph ^= 1u;
+    }
+}
+
 // MMA column n holds token 4*(n%32) + n/32.
 __device__ __forceinline__ int token_of_col(int n) { return ((n & 31) << 2) | (n >> 5); }
 
@@ -309,11 +359,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<uint32_t *>(smem + SmemLayout::kSfa)[threadIdx.x] = 0x7F7F7F7Fu;
         fence_proxy_async_smem();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kProdWarp0 && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_s);
     }
-    if (warp == 5) {
+    if (warp == kScaleWarp) {
         tmem_alloc(sbase + SmemLayout::kTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -325,174 +375,207 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * p.num_units / gridDim.x;
     const int64_t u_end = static_cast<int64_t>(blockIdx.x + 1) * p.num_units / gridDim.x;
 
-    if (warp == 4) {
-        // ------------------------------------------------------- producer --
-        // The whole warp walks the units; lane i fetches the page id of the
-        // unit's i-th live page, lane 0 issues the TMA loads.
+    if (warp >= kProdWarp0 && warp < kScaleWarp) {
+        // ------------------------------------------------------ producers --
+        // Each producer warp walks all units; lane i fetches the page id of
+        // the unit's i-th live page one unit ahead (so the block-table latency
+        // overlaps the current unit's copies); producer pw issues the TMA
+        // loads of the computed pages pc with pc % kProdWarps == pw.
+        const int pw = warp - kProdWarp0;
+        int turn = 0;
         const uint64_t policy = kDecode ? l2_policy_evict_first() : l2_policy_evict_last();
-        int s = 0;
-        uint32_t ph = 0;
+        Ring st;
         TileInfo ti;
         ti.tile = -1;
-        bool ok = true;
-        for (int64_t u = u_begin; u < u_end && ok; ++u) {
-            const int64_t tile = u / p.chunks_per_tile;
-            if (tile != ti.tile) ti = tile_info<kDecode>(p, tile);
-            if (ti.nrows <= 0) continue;
-            const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
-            const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
-            const int jc = j1 < ti.live_end ? j1 : ti.live_end;
-            const int n = jc - j0;
-            if (n <= 0) continue;
+        // next unit at or after c with live pages: tile info, first page, page count
+        auto next_unit = [&](UnitCursor &c, TileInfo &t, int &j0, int &n) -> bool {
+            for (; c.left > 0; cursor_next(p, c)) {
+                if (c.tile != t.tile) t = tile_info<kDecode>(p, c.tile);
+                if (t.nrows <= 0) continue;
+                j0 = c.chunk * kChunk;
+                const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
+                const int jc = j1 < t.live_end ? j1 : t.live_end;
+                n = jc - j0;
+                if (n > 0) return true;
+            }
+            return false;
+        };
+        auto fetch_id = [&](const TileInfo &t, int j0, int n) -> int64_t {
+            return lane < n ? static_cast<int64_t>(p.block_table[static_cast<int64_t>(t.b) * p.bt_stride + j0 + lane])
+                            : 0;
+        };
+        UnitCursor cur = cursor_begin(p, u_begin, u_end);
+        int j0 = 0, n = 0;
+        bool have = next_unit(cur, ti, j0, n);
+        int64_t raw = have ? fetch_id(ti, j0, n) : 0;
+        while (have) {
+            UnitCursor c2 = cur;
+            cursor_next(p, c2);
+            TileInfo ti2 = ti;
+            int j02 = 0, n2 = 0;
+            const bool have2 = next_unit(c2, ti2, j02, n2);
+            const int64_t raw2 = have2 ? fetch_id(ti2, j02, n2) : 0;
             int pid = 0;
             if (lane < n) {
-                const int64_t v = p.block_table[static_cast<int64_t>(ti.b) * p.bt_stride + j0 + lane];
-                if (v < 0 || v >= p.num_pool_pages) {
+                if (raw < 0 || raw >= p.num_pool_pages)
                     atomicOr(&g_mx4_device_status, 0x1u);
-                } else {
-                    pid = static_cast<int>(v);
-                }
+                else
+                    pid = static_cast<int>(raw);
             }
+            bool go = true;
             for (int i = 0; i < n; ++i) {
                 const int id = __shfl_sync(0xffffffffu, pid, i);
-                int go = 1;
-                if (lane == 0) {
-                    go = wait_bounded(empty_bar(s), ph ^ 1u, abort_flag, kSiteProducerEmpty);
-                    if (go) {
-                        mbar_arrive_expect_tx(full_bar(s), kStageTxBytes);
-                        tma_load_4d(sbase + SmemLayout::kData + s * kTileBytes, &tmap_k, full_bar(s), 0, 0, 0, id,
-                                    policy);
-                        tma_load_2d(sbase + SmemLayout::kScale + s * kScaleBytes, &tmap_s, full_bar(s), 0, id,
-                                    policy);
+                if (turn == pw) {
+                    go = __all_sync(0xffffffffu, wait_bounded(empty_bar(st.idx), st.ph ^ 1u, abort_flag,
+                                                              kSiteProducerEmpty));
+                    if (!go) break;
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(full_bar(st.idx), kStageTxBytes);
+                        tma_load_4d(sbase + SmemLayout::kData + st.idx * kTileBytes, &tmap_k, full_bar(st.idx), 0,
+                                    0, 0, id, policy);
+                        tma_load_2d(sbase + SmemLayout::kScale + st.idx * kScaleBytes, &tmap_s, full_bar(st.idx), 0,
+                                    id, policy);
                     }
+                    __syncwarp();
                 }
-                if (!__shfl_sync(0xffffffffu, go, 0)) {
-                    ok = false;
-                    break;
-                }
-                if (++s == kStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                if (++turn == kProdWarps) turn = 0;
+                ring_next<kStages>(st);
             }
+            if (!go) break;
+            cur = c2;
+            ti = ti2;
+            j0 = j02;
+            n = n2;
+            raw = raw2;
+            have = have2;
         }
         if (lane == 0) {
             // Do not leave while copies into this CTA's smem may be in flight:
             // every armed stage completes (bounded) before the CTA exits.
-            for (int i = 0; i < kStages; ++i) {
-                // stages < s were armed in phase ph, the others in ph^1 (if ever)
-                const uint32_t par = (i < s) ? ph : (ph ^ 1u);
+            for (int i = pw; i < kStages; i += kProdWarps) {
+                // stages before st.idx were armed in phase ph, the others in ph^1 (if ever)
+                const uint32_t par = (i < st.idx) ? st.ph : (st.ph ^ 1u);
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(full_bar(i), par) && globaltimer_ns() - t0 < 2000000ull) {
                 }
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == kScaleWarp) {
         // ------------------------------------------------ scale-factor copy --
         // Per page: once its bytes have landed and its TMEM scale buffer is
         // free, copy the 512 B scale block into TMEM (tcgen05.cp) and signal
         // the MMA warps.  The constant unit scale of A is copied first.
-        if (lane == 0) {
-            tc_cp_32x128b_warpx4(tmem_base + kTmemSfaCol, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
-            int s = 0, x = 0;
-            uint32_t ph = 0, xph = 0;
+        {
+            if (elect_one())
+                tc_cp_32x128b_warpx4(tmem_base + kTmemSfaCol, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
+            __syncwarp();
+            const uint64_t sdesc0 = smem_desc(sbase + SmemLayout::kScale, 16, 128, 0);
+            Ring st, sf;
             TileInfo ti;
             ti.tile = -1;
             bool ok = true;
-            for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u) {
-                const int64_t tile = u / p.chunks_per_tile;
-                if (tile != ti.tile) ti = tile_info<kDecode>(p, tile);
+            for (UnitCursor c = cursor_begin(p, u_begin, u_end); c.left > 0 && ok; cursor_next(p, c)) {
+                if (c.tile != ti.tile) ti = tile_info<kDecode>(p, c.tile);
                 if (ti.nrows <= 0) continue;
-                const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+                const int j0 = c.chunk * kChunk;
                 const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
                 const int jc = j1 < ti.live_end ? j1 : ti.live_end;
                 for (int j = j0; j < jc; ++j) {
-                    if (!wait_bounded(full_bar(s), ph, abort_flag, kSiteScaleFull) ||
-                        !wait_bounded(sfempty_bar(x), xph ^ 1u, abort_flag, kSiteScaleEmpty)) {
+                    if (!__all_sync(0xffffffffu,
+                                    wait_bounded(full_bar(st.idx), st.ph, abort_flag, kSiteScaleFull) &&
+                                        wait_bounded(sfempty_bar(sf.idx), sf.ph ^ 1u, abort_flag, kSiteScaleEmpty))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    tc_cp_32x128b_warpx4(tmem_base + kTmemSfbCol + 4u * x,
-                                         smem_desc(sbase + SmemLayout::kScale + s * kScaleBytes, 16, 128, 0));
-                    tc_commit(sfready_bar(x));
-                    if (++s == kStages) {
-                        s = 0;
-                        ph ^= 1u;
+                    if (elect_one()) {
+                        // start-address field of the descriptor counts 16-byte units
+                        tc_cp_32x128b_warpx4(tmem_base + kTmemSfbCol + 4u * sf.idx,
+                                             sdesc0 + static_cast<uint64_t>(st.idx * (kScaleBytes >> 4)));
+                        tc_commit(sfready_bar(sf.idx));
                     }
-                    if (++x == kSfbBufs) {
-                        x = 0;
-                        xph ^= 1u;
-                    }
+                    __syncwarp();
+                    ring_next<kStages>(st);
+                    ring_next<kSfbBufs>(sf);
                 }
             }
-            tc_commit(final_bar(kMmaWarps));
+            if (elect_one()) tc_commit(final_bar(kMmaWarps));
+            __syncwarp();
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(final_bar(kMmaWarps), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
             }
         }
         __syncwarp();
-    } else if (warp >= 6) {
+    } else if (warp >= kMmaWarp0) {
         // ----------------------------------------------------- MMA issuers --
-        // Issuer i takes the computed pages with pc % kMmaWarps == i; each
+        // Issuer i takes every kMmaWarps-th computed page starting at i; each
         // tcgen05 instruction costs its issuing thread tens of cycles, so the
-        // pages are spread over several issuing warps.
-        const int issuer = warp - 6;
-        if (lane == 0) {
+        // pages are spread over several issuing warps.  All ring positions
+        // advance once per computed page, so the control loop has no division.
+        const int issuer = warp - kMmaWarp0;
+        {
             const uint32_t tmem_sfa = tmem_base + kTmemSfaCol;
-            int64_t pc = 0, qcount = 0;
-            uint32_t qbuf = 0;
+            const uint64_t bdesc0 = smem_desc(sbase + SmemLayout::kData, 16, 1024, 2);
+            Ring sf, dr;
+            int st_idx = 0, turn = 0;
+            int64_t qcount = 0;
+            uint32_t a_tmem = tmem_base + kTmemACol;
             TileInfo ti;
             ti.tile = -1;
             bool ok = true, holding_q = false;
-            for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u) {
-                const int64_t tile = u / p.chunks_per_tile;
-                if (tile != ti.tile) {
-                    ti = tile_info<kDecode>(p, tile);
+            for (UnitCursor c = cursor_begin(p, u_begin, u_end); c.left > 0 && ok; cursor_next(p, c)) {
+                if (c.tile != ti.tile) {
+                    ti = tile_info<kDecode>(p, c.tile);
                     if (ti.nrows > 0) {
                         // the previous query tile's buffer is free once its MMAs retire
-                        if (holding_q) tc_commit(qempty_bar(static_cast<int>((qcount - 1) & 1)));
+                        if (holding_q && elect_one()) tc_commit(qempty_bar(static_cast<int>((qcount - 1) & 1)));
+                        __syncwarp();
                         const int64_t qi = qcount++;
-                        qbuf = static_cast<uint32_t>(qi & 1);
+                        a_tmem = tmem_base + kTmemACol + static_cast<uint32_t>(qi & 1) * 32u;
                         holding_q = true;
-                        if (!wait_bounded(qfull_bar(qbuf), static_cast<uint32_t>((qi >> 1) & 1), abort_flag,
-                                          kSiteMmaQFull))
+                        if (!__all_sync(0xffffffffu, wait_bounded(qfull_bar(static_cast<int>(qi & 1)),
+                                                                  static_cast<uint32_t>((qi >> 1) & 1), abort_flag,
+                                                                  kSiteMmaQFull)))
                             break;
                         tc_fence_after();
                     }
                 }
                 if (ti.nrows <= 0) continue;
-                const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+                const int j0 = c.chunk * kChunk;
                 const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
                 const int jc = j1 < ti.live_end ? j1 : ti.live_end;
-                const uint32_t a_tmem = tmem_base + kTmemACol + qbuf * 32u;
-                for (int j = j0; j < jc; ++j, ++pc) {
-                    if (static_cast<int>(pc % kMmaWarps) != issuer) continue;
-                    const int s = static_cast<int>(pc % kStages);
-                    const int x = static_cast<int>(pc % kSfbBufs);
-                    const int d = static_cast<int>(pc % kDBufs);
-                    const uint32_t xph = static_cast<uint32_t>((pc / kSfbBufs) & 1);
-                    const uint32_t dph = static_cast<uint32_t>((pc / kDBufs) & 1);
-                    if (!wait_bounded(sfready_bar(x), xph, abort_flag, kSiteMmaFull) ||
-                        !wait_bounded(dempty_bar(d), dph ^ 1u, abort_flag, kSiteMmaDEmpty)) {
-                        ok = false;
-                        break;
+                for (int j = j0; j < jc; ++j) {
+                    if (turn == issuer) {
+                        if (!__all_sync(0xffffffffu,
+                                        wait_bounded(sfready_bar(sf.idx), sf.ph, abort_flag, kSiteMmaFull) &&
+                                            wait_bounded(dempty_bar(dr.idx), dr.ph ^ 1u, abort_flag, kSiteMmaDEmpty))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (elect_one()) {
+                            const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sf.idx;
+                            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(st_idx * (kTileBytes >> 4));
+                            const uint32_t d_tmem = tmem_base + dr.idx * 128u;
+                            // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
+                            tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
+                            tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k(1), tmem_sfa, tmem_sfb, 1u);
+                            tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k(2), tmem_sfa, tmem_sfb, 1u);
+                            tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k(3), tmem_sfa, tmem_sfb, 1u);
+                            tc_commit(dfull_bar(dr.idx));
+                        }
+                        __syncwarp();
                     }
-                    tc_fence_after();
-                    const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * x;
-                    const uint32_t b_addr = sbase + SmemLayout::kData + s * kTileBytes;
-                    const uint32_t d_tmem = tmem_base + d * 128u;
-#pragma unroll
-                    for (uint32_t k = 0; k < 4; ++k) {
-                        tc_mma_mx_ts(d_tmem, a_tmem + 8u * k, smem_desc(b_addr + 32u * k, 16, 1024, 2),
-                                     idesc_for_k(k), tmem_sfa, tmem_sfb, k > 0 ? 1u : 0u);
-                    }
-                    tc_commit(dfull_bar(d));
+                    if (++turn == kMmaWarps) turn = 0;
+                    if (++st_idx == kStages) st_idx = 0;
+                    ring_next<kSfbBufs>(sf);
+                    ring_next<kDBufs>(dr);
                 }
             }
             // all MMAs retire before TMEM is released
-            tc_commit(final_bar(issuer));
+            if (elect_one()) tc_commit(final_bar(issuer));
+            __syncwarp();
             const uint64_t t0 = globaltimer_ns();
             while (!mbar_try_wait(final_bar(issuer), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
             }
@@ -500,20 +583,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------- epilogue --
-        const int m = threadIdx.x;                 // A row / TMEM lane 0..127
+        // Set `set` (warps 4*set .. 4*set+3) takes the computed pages pc with
+        // pc % kEpiSets == set; set 0 also loads the query tiles and writes
+        // the pages no row can see.
+        const int set = warp / 4;
+        const int quad = warp % 4;
+        const int m = quad * 32 + lane;            // A row / TMEM lane 0..127
         const int ri = m / kHeads;                 // row within the tile
         const int h = m % kHeads;
-        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-        float *stage = reinterpret_cast<float *>(smem + SmemLayout::kStage) + m * kChunk;
+        const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
+        int turn = 0;
         const float sm_scale = p.sm_scale;
-        int d = 0, s = 0, x = 0;
-        uint32_t dph = 0;
+        Ring dr;
+        int st_idx = 0, sf_idx = 0;
         int64_t qcount = 0;
         TileInfo ti;
         ti.tile = -1;
 
         // Load the query tile of `t` into A buffer qi & 1 once the MMAs of the
-        // tile that used that buffer before have retired.
+        // tile that used that buffer before have retired (set 0 only).
         auto q_load = [&](const TileInfo &t, int64_t qi) -> bool {
             const int buf = static_cast<int>(qi & 1);
             // warp-uniform outcome, so the .sync.aligned operations below never diverge
@@ -529,119 +617,108 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
 
         bool ok = true;
-        for (int64_t u = u_begin; u < u_end && ok && !__any_sync(0xffffffffu, *abort_flag != 0); ++u) {
-            const int64_t tile = u / p.chunks_per_tile;
-            if (tile != ti.tile) {
-                const TileInfo nt_info = tile_info<kDecode>(p, tile);
+        for (UnitCursor c = cursor_begin(p, u_begin, u_end);
+             c.left > 0 && ok && !__any_sync(0xffffffffu, *abort_flag != 0); cursor_next(p, c)) {
+            if (c.tile != ti.tile) {
+                const TileInfo nt_info = tile_info<kDecode>(p, c.tile);
                 if (nt_info.nrows <= 0) continue;   // keeps ti: units of this tile are skipped below
                 ti = nt_info;
-                if (qcount == 0 && !q_load(ti, 0)) break;
-                const int64_t qi = qcount++;
-                // prefetch the next tile with rows in this CTA's range
-                int64_t nt = tile + 1;
-                while (nt * p.chunks_per_tile < u_end && !tile_has_rows<kDecode>(p, nt)) ++nt;
-                if (nt * p.chunks_per_tile < u_end) {
-                    if (!q_load(tile_info<kDecode>(p, nt), qi + 1)) break;
+                if (set == 0) {
+                    if (qcount == 0 && !q_load(ti, 0)) break;
+                    const int64_t qi = qcount++;
+                    // prefetch the next tile with rows in this CTA's range
+                    int64_t nt = c.tile + 1;
+                    while (nt * p.chunks_per_tile < u_end && !tile_has_rows<kDecode>(p, nt)) ++nt;
+                    if (nt * p.chunks_per_tile < u_end) {
+                        if (!q_load(tile_info<kDecode>(p, nt), qi + 1)) break;
+                    }
                 }
             }
-            const int j0 = static_cast<int>(u - tile * p.chunks_per_tile) * kChunk;
+            const int j0 = c.chunk * kChunk;
             const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
             const bool has_row = ri < ti.nrows;     // uniform per warp
             const int L = has_row ? (ri == 0 ? ti.L[0] : ti.L[1]) : 0;
             const int64_t line = (ti.row0 + ri) * kHeads + h;
+            float *row_out = p.out + line * p.out_row_stride;
             for (int j = j0; j < j1; ++j) {
                 const int lim = L - j * kPage;   // live tokens of page j for this row
                 if (j < ti.live_end) {
-                    if (!__all_sync(0xffffffffu, wait_bounded(dfull_bar(d), dph, abort_flag, kSiteEpiDFull))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // the page's MMAs have retired: its smem stage and scale
-                    // buffer can be refilled
-                    if (m == 0) {
-                        mbar_arrive(empty_bar(s));
-                        mbar_arrive(sfempty_bar(x));
-                    }
-                    if (++s == kStages) s = 0;
-                    if (++x == kSfbBufs) x = 0;
-                    const uint32_t taddr = tmem_base + lane_addr + d * 128u;
-                    if (has_row) {
-                        uint32_t v[128];
-                        if (!kLogits) {
-                            float mx;
-                            if (lim >= kPage) {
-                                mx = tmem_ld_max_32x32b_x128(taddr, v);
+                    const bool mine = turn == set;
+                    if (++turn == kEpiSets) turn = 0;
+                    if (mine) {
+                        if (!__all_sync(0xffffffffu,
+                                        wait_bounded(dfull_bar(dr.idx), dr.ph, abort_flag, kSiteEpiDFull))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t taddr = tmem_base + lane_addr + dr.idx * 128u;
+                        if (has_row) {
+                            uint32_t v[128];
+                            if (!kLogits) {
+                                float mx;
+                                if (lim >= kPage) {
+                                    mx = tmem_ld_max_32x32b_x128(taddr, v);
+                                } else {
+                                    tmem_ld_32x32b_x128(taddr, v);
+                                    mx = -INFINITY;
+#pragma unroll
+                                    for (int n = 0; n < 128; ++n)
+                                        if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
+                                }
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
+                                __stcs(row_out + j, mx * sm_scale);
                             } else {
                                 tmem_ld_32x32b_x128(taddr, v);
-                                mx = -INFINITY;
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
+                                float *dst = row_out + static_cast<int64_t>(j) * kPage;
+                                const int valid = p.max_seq_len - j * kPage;   // columns that exist
+                                const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
 #pragma unroll
-                                for (int n = 0; n < 128; ++n)
-                                    if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
-                            }
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(dempty_bar(d));
-                            stage[j - j0] = mx * sm_scale;
-                        } else {
-                            tmem_ld_32x32b_x128(taddr, v);
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(dempty_bar(d));
-                            float *dst = p.out + line * p.out_row_stride + static_cast<int64_t>(j) * kPage;
-                            const int valid = p.max_seq_len - j * kPage;   // columns that exist
-                            const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
-#pragma unroll
-                            for (int g = 0; g < 32; ++g) {
-                                float4 o;
-                                o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
-                                o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
-                                o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
-                                o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
-                                if (vec) {
-                                    __stcs(reinterpret_cast<float4 *>(dst + 4 * g), o);
-                                } else {
-                                    if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
-                                    if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
-                                    if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
-                                    if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
+                                for (int g = 0; g < 32; ++g) {
+                                    float4 o;
+                                    o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
+                                    o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
+                                    o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
+                                    o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
+                                    if (vec) {
+                                        __stcs(reinterpret_cast<float4 *>(dst + 4 * g), o);
+                                    } else {
+                                        if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
+                                        if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
+                                        if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
+                                        if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
+                                    }
                                 }
                             }
+                        } else {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
                         }
-                    } else {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(dempty_bar(d));
+                        // the page's MMAs have retired, so its smem stage and
+                        // scale buffer can be refilled
+                        if (quad == 0 && lane == 0) {
+                            mbar_arrive(empty_bar(st_idx));
+                            mbar_arrive(sfempty_bar(sf_idx));
+                        }
                     }
-                    if (++d == kDBufs) {
-                        d = 0;
-                        dph ^= 1u;
-                    }
-                } else if (has_row) {
+                    if (++st_idx == kStages) st_idx = 0;
+                    if (++sf_idx == kSfbBufs) sf_idx = 0;
+                    ring_next<kDBufs>(dr);
+                } else if (has_row && set == 0) {
                     // no row of the tile sees this page: nothing was computed
                     if (!kLogits) {
-                        stage[j - j0] = -INFINITY;
+                        __stcs(row_out + j, -INFINITY);
                     } else {
-                        float *dst = p.out + line * p.out_row_stride + static_cast<int64_t>(j) * kPage;
+                        float *dst = row_out + static_cast<int64_t>(j) * kPage;
                         const int valid = p.max_seq_len - j * kPage;
-                        for (int c = 0; c < kPage && c < valid; ++c) dst[c] = -INFINITY;
+                        for (int cc = 0; cc < kPage && cc < valid; ++cc) dst[cc] = -INFINITY;
                     }
-                }
-            }
-            if (!ok) break;
-            if (!kLogits && has_row) {
-                float *dst = p.out + line * p.out_row_stride + j0;
-                const int n = j1 - j0;
-                if (n == kChunk && (p.out_row_stride & 3) == 0) {
-                    const float4 *src = reinterpret_cast<const float4 *>(stage);
-                    __stcs(reinterpret_cast<float4 *>(dst), src[0]);
-                    __stcs(reinterpret_cast<float4 *>(dst) + 1, src[1]);
-                } else if (n == kChunk && (p.out_row_stride & 1) == 0) {
-                    const float2 *src = reinterpret_cast<const float2 *>(stage);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) __stcs(reinterpret_cast<float2 *>(dst) + i, src[i]);
-                } else {
-                    for (int i = 0; i < n; ++i) dst[i] = stage[i];
                 }
             }
         }
@@ -649,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kScaleWarp) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }

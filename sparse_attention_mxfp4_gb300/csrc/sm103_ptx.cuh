@@ -21,6 +21,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// One lane of a converged warp (elect.sync): the single-thread async
+// instructions (TMA, tcgen05.mma/cp/commit) are issued from a converged warp
+// rather than from a lone lane.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ------------------------------------------------------------- mbarriers --
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
