@@ -51,6 +51,18 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, world_size: int, device="cpu") -> float:
+    """Largest per-rank value over the job (the slowest rank sets the step
+    time); identity on one rank."""
+    if world_size <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -316,12 +328,7 @@ def run_ours(args):
     ms_rank = start.elapsed_time(end) / args.steps
     clocks = sampler.stop() if sampler else None
     status = mx4.mx4_index_get_device_status()
-    if ws > 1:
-        t = torch.tensor([ms_rank], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    else:
-        ms = ms_rank
+    ms = max_over_ranks(ms_rank, ws, "cuda")
 
     e2e_ms, h2d, d2h = measure_e2e(case, max(3, min(args.steps, 20)), stream)
 
