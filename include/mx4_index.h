@@ -78,10 +78,10 @@ typedef enum {
 #define MX4_DEV_TIMEOUT 0x2u  /* an internal wait gave up; the kernel returned early */
 /* With MX4_DEV_TIMEOUT, bit (8 + site) names the wait that gave up: site 0 =
  * producer waiting for a free smem stage, 1 = MMA waiting for the query tile,
- * 2 = MMA waiting for a page's scales, 3 = MMA waiting for a free
+ * 2 = MMA waiting for a page's bytes, 3 = MMA waiting for a free
  * accumulator, 4 = epilogue waiting for a free query buffer, 5 = epilogue
- * waiting for an accumulator, 6 = scale copy waiting for a page, 7 = scale
- * copy waiting for a free scale buffer.  Diagnostic only. */
+ * waiting for an accumulator, 6 = MMA waiting for a free scale buffer.
+ * Diagnostic only. */
 
 /*
  * Block scores for ragged prefill (causal) rows.  [P1] "Kernels":

@@ -46,25 +46,25 @@ constexpr int kDataBytes = 8192;                // packed e2m1 codes per page
 constexpr int kScaleBytes = 512;                // e8m0 bytes per page
 constexpr int kTileBytes = 128 * 128;           // one page in the padded 4-bit smem form
 constexpr int kStages = 12;                     // smem pipeline depth (pages in flight)
-constexpr int kDBufs = 3;                       // TMEM accumulator buffers
+constexpr int kDBufs = 2;                       // TMEM accumulator buffers (one per page parity)
 constexpr int kSfbBufs = 12;                    // TMEM scale-factor buffers for B
 constexpr int kChunk = 8;                       // pages per work unit
-// Warp roles: two epilogue warpgroups (warps 0-3 and 4-7; warp w reads TMEM
-// lane quadrant w % 4) take alternate pages; two TMA producer warps take
-// alternate pages; one warp copies scales into TMEM (and owns the TMEM
-// allocation); the MMA warps take alternate pages.
+// Warp roles, as two lanes by page parity: two epilogue warpgroups (warps 0-3
+// and 4-7; warp w reads TMEM lane quadrant w % 4), two TMA producer warps and
+// two MMA warps each take the pages of one parity; an MMA warp copies its
+// pages' scales into TMEM right before their MMAs (the first MMA warp also
+// owns the TMEM allocation).
 constexpr int kEpiSets = 2;
 constexpr int kProdWarps = 2;
-constexpr int kMmaWarps = 1;
+constexpr int kMmaWarps = 2;
 constexpr int kProdWarp0 = 4 * kEpiSets;                 // 8
-constexpr int kScaleWarp = kProdWarp0 + kProdWarps;      // 10
-constexpr int kMmaWarp0 = kScaleWarp + 1;                // 11
+constexpr int kMmaWarp0 = kProdWarp0 + kProdWarps;       // 10
 constexpr int kThreads = 32 * (kMmaWarp0 + kMmaWarps);
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D[3] x 128 | A (query tile, e4m3) [2] x 32 | SFA 4 | SFB[12] x 4
-constexpr uint32_t kTmemACol = kDBufs * 128;                 // 384
-constexpr uint32_t kTmemSfaCol = kTmemACol + 2 * 32;         // 448
-constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4;            // 452
+// TMEM columns: D[2] x 128 | A (query tile, e4m3) [2] x 32 | SFA[kMmaWarps] x 4 | SFB[12] x 4
+constexpr uint32_t kTmemACol = kDBufs * 128;
+constexpr uint32_t kTmemSfaCol = kTmemACol + 2 * 32;
+constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4 * kMmaWarps;
 // Transaction bytes of one page: the 4-bit TMA load counts the packed
 // global bytes (8192), not the 16 KB it writes in the padded smem form.
 constexpr uint32_t kStageTxBytes = kDataBytes + kScaleBytes;
@@ -73,6 +73,15 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s per wait
 static_assert(kTmemSfbCol + 4 * kSfbBufs <= kTmemCols, "TMEM budget");
 static_assert(kSfbBufs > kDBufs, "an SFB buffer is reused only after its MMA retired");
 static_assert(kStages % kProdWarps == 0, "each producer warp owns a fixed set of stages");
+// Pages are split by parity into independent lanes of the pipeline: page pc is
+// loaded by producer pc % 2, issued by MMA warp pc % 2, read by epilogue set
+// pc % 2, and uses the accumulator, scale buffer and smem stage of the same
+// parity.  Every mbarrier therefore has one waiting side and one arriving side
+// that walk its phases in order, so a parity wait never runs two phases ahead
+// of its barrier (which a parity test could not tell apart from done).
+static_assert(kMmaWarps == kEpiSets && kProdWarps == kEpiSets && kDBufs % kMmaWarps == 0 &&
+                  kSfbBufs % kMmaWarps == 0 && kStages % kMmaWarps == 0,
+              "page-parity pipeline lanes");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling:
 // A = E4M3 (0, bits 7..9), B = E2M1 (5, bits 10..12), both K-major,
@@ -114,9 +123,9 @@ struct SmemLayout {
     static constexpr uint32_t kScale = kData + kStages * kTileBytes;       // kStages x 512 B
     static constexpr uint32_t kSfa = kScale + kStages * kScaleBytes;       // 512 B of 0x7F
     static constexpr uint32_t kBars = kSfa + kScaleBytes;
-    // barriers: full[kStages], empty[kStages], sfready[kSfbBufs], sfempty[kSfbBufs],
-    //           dfull[kDBufs], dempty[kDBufs], qfull[2], qempty[2], final[kMmaWarps + 1]
-    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 4 + kMmaWarps + 1;
+    // barriers: full[kStages], empty[kStages], sfempty[kSfbBufs], dfull[kDBufs],
+    //           dempty[kDBufs], qfull[2], qempty[2], final[kMmaWarps]
+    static constexpr uint32_t kNumBars = 2 * kStages + kSfbBufs + 2 * kDBufs + 4 + kMmaWarps;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -191,8 +200,7 @@ enum WaitSite : uint32_t {
     kSiteMmaDEmpty = 3,
     kSiteEpiQEmpty = 4,
     kSiteEpiDFull = 5,
-    kSiteScaleFull = 6,
-    kSiteScaleEmpty = 7,
+    kSiteMmaScaleEmpty = 6,
 };
 
 // Bounded wait: true when the phase completed; false after the time limit or
@@ -323,13 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) { return sbase + SmemLayout::kBars + 8u * i; };
     auto full_bar = [&](int i) { return bar(i); };
     auto empty_bar = [&](int i) { return bar(kStages + i); };
-    auto sfready_bar = [&](int i) { return bar(2 * kStages + i); };
-    auto sfempty_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + i); };
-    auto dfull_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + i); };
-    auto dempty_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + kDBufs + i); };
-    auto qfull_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + 2 * kDBufs + i); };
-    auto qempty_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 2 + i); };
-    auto final_bar = [&](int i) { return bar(2 * kStages + 2 * kSfbBufs + 2 * kDBufs + 4 + i); };
+    auto sfempty_bar = [&](int i) { return bar(2 * kStages + i); };
+    auto dfull_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + i); };
+    auto dempty_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + kDBufs + i); };
+    auto qfull_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + 2 * kDBufs + i); };
+    auto qempty_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + 2 * kDBufs + 2 + i); };
+    auto final_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + 2 * kDBufs + 4 + i); };
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + SmemLayout::kAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::kTmemSlot);
 
@@ -338,10 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(i), 1);
             mbar_init(empty_bar(i), 1);
         }
-        for (int i = 0; i < kSfbBufs; ++i) {
-            mbar_init(sfready_bar(i), 1);
-            mbar_init(sfempty_bar(i), 1);
-        }
+        for (int i = 0; i < kSfbBufs; ++i) mbar_init(sfempty_bar(i), 1);
         for (int i = 0; i < kDBufs; ++i) {
             mbar_init(dfull_bar(i), 1);
             mbar_init(dempty_bar(i), 4);
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(qfull_bar(i), 4);
             mbar_init(qempty_bar(i), kMmaWarps);
         }
-        for (int i = 0; i <= kMmaWarps; ++i) mbar_init(final_bar(i), 1);
+        for (int i = 0; i < kMmaWarps; ++i) mbar_init(final_bar(i), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -363,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_s);
     }
-    if (warp == kScaleWarp) {
+    if (warp == kMmaWarp0) {
         tmem_alloc(sbase + SmemLayout::kTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -375,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * p.num_units / gridDim.x;
     const int64_t u_end = static_cast<int64_t>(blockIdx.x + 1) * p.num_units / gridDim.x;
 
-    if (warp >= kProdWarp0 && warp < kScaleWarp) {
+    if (warp >= kProdWarp0 && warp < kMmaWarp0) {
         // ------------------------------------------------------ producers --
         // Each producer warp walks all units; lane i fetches the page id of
         // the unit's i-th live page one unit ahead (so the block-table latency
@@ -461,52 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == kScaleWarp) {
-        // ------------------------------------------------ scale-factor copy --
-        // Per page: once its bytes have landed and its TMEM scale buffer is
-        // free, copy the 512 B scale block into TMEM (tcgen05.cp) and signal
-        // the MMA warps.  The constant unit scale of A is copied first.
-        {
-            if (elect_one())
-                tc_cp_32x128b_warpx4(tmem_base + kTmemSfaCol, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
-            __syncwarp();
-            const uint64_t sdesc0 = smem_desc(sbase + SmemLayout::kScale, 16, 128, 0);
-            Ring st, sf;
-            TileInfo ti;
-            ti.tile = -1;
-            bool ok = true;
-            for (UnitCursor c = cursor_begin(p, u_begin, u_end); c.left > 0 && ok; cursor_next(p, c)) {
-                if (c.tile != ti.tile) ti = tile_info<kDecode>(p, c.tile);
-                if (ti.nrows <= 0) continue;
-                const int j0 = c.chunk * kChunk;
-                const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
-                const int jc = j1 < ti.live_end ? j1 : ti.live_end;
-                for (int j = j0; j < jc; ++j) {
-                    if (!__all_sync(0xffffffffu,
-                                    wait_bounded(full_bar(st.idx), st.ph, abort_flag, kSiteScaleFull) &&
-                                        wait_bounded(sfempty_bar(sf.idx), sf.ph ^ 1u, abort_flag, kSiteScaleEmpty))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (elect_one()) {
-                        // start-address field of the descriptor counts 16-byte units
-                        tc_cp_32x128b_warpx4(tmem_base + kTmemSfbCol + 4u * sf.idx,
-                                             sdesc0 + static_cast<uint64_t>(st.idx * (kScaleBytes >> 4)));
-                        tc_commit(sfready_bar(sf.idx));
-                    }
-                    __syncwarp();
-                    ring_next<kStages>(st);
-                    ring_next<kSfbBufs>(sf);
-                }
-            }
-            if (elect_one()) tc_commit(final_bar(kMmaWarps));
-            __syncwarp();
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(final_bar(kMmaWarps), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-        }
-        __syncwarp();
     } else if (warp >= kMmaWarp0) {
         // ----------------------------------------------------- MMA issuers --
         // Issuer i takes every kMmaWarps-th computed page starting at i; each
@@ -515,10 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // advance once per computed page, so the control loop has no division.
         const int issuer = warp - kMmaWarp0;
         {
-            const uint32_t tmem_sfa = tmem_base + kTmemSfaCol;
+            // this warp's copy of the unit scale of A (e8m0 127 everywhere)
+            const uint32_t tmem_sfa = tmem_base + kTmemSfaCol + 4u * issuer;
+            if (elect_one()) tc_cp_32x128b_warpx4(tmem_sfa, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
+            __syncwarp();
             const uint64_t bdesc0 = smem_desc(sbase + SmemLayout::kData, 16, 1024, 2);
-            Ring sf, dr;
-            int st_idx = 0, turn = 0;
+            const uint64_t sdesc0 = smem_desc(sbase + SmemLayout::kScale, 16, 128, 0);
+            Ring st, sf, dr;
+            int turn = 0;
             int64_t qcount = 0;
             uint32_t a_tmem = tmem_base + kTmemACol;
             TileInfo ti;
@@ -548,15 +510,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = j0; j < jc; ++j) {
                     if (turn == issuer) {
                         if (!__all_sync(0xffffffffu,
-                                        wait_bounded(sfready_bar(sf.idx), sf.ph, abort_flag, kSiteMmaFull) &&
+                                        wait_bounded(full_bar(st.idx), st.ph, abort_flag, kSiteMmaFull) &&
+                                            wait_bounded(sfempty_bar(sf.idx), sf.ph ^ 1u, abort_flag,
+                                                         kSiteMmaScaleEmpty) &&
                                             wait_bounded(dempty_bar(dr.idx), dr.ph ^ 1u, abort_flag, kSiteMmaDEmpty))) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         if (elect_one()) {
+                            // scales first: the tcgen05 operations of one thread run in issue
+                            // order, so the MMAs below see them with no commit/wait in between
                             const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sf.idx;
-                            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(st_idx * (kTileBytes >> 4));
+                            tc_cp_32x128b_warpx4(tmem_sfb,
+                                                 sdesc0 + static_cast<uint64_t>(st.idx * (kScaleBytes >> 4)));
+                            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(st.idx * (kTileBytes >> 4));
                             const uint32_t d_tmem = tmem_base + dr.idx * 128u;
                             // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
                             tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
@@ -568,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                     if (++turn == kMmaWarps) turn = 0;
-                    if (++st_idx == kStages) st_idx = 0;
+                    ring_next<kStages>(st);
                     ring_next<kSfbBufs>(sf);
                     ring_next<kDBufs>(dr);
                 }
@@ -726,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kScaleWarp) {
+    if (warp == kMmaWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
