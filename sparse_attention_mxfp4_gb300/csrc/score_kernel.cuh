@@ -637,7 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tc_fence_before();
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
-                                __stcs(row_out + j, mx * sm_scale);
+                                // default write-back policy: the two epilogue sets fill one 32-byte
+                                // sector 4 bytes at a time, so it must stay in L2 until complete
+                                row_out[j] = mx * sm_scale;
                             } else {
                                 tmem_ld_32x32b_x128(taddr, v);
                                 tc_fence_before();
@@ -681,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (has_row && set == 0) {
                     // no row of the tile sees this page: nothing was computed
                     if (!kLogits) {
-                        __stcs(row_out + j, -INFINITY);
+                        row_out[j] = -INFINITY;
                     } else {
                         float *dst = row_out + static_cast<int64_t>(j) * kPage;
                         const int valid = p.max_seq_len - j * kPage;
