@@ -45,23 +45,34 @@ constexpr int kPage = 128;
 constexpr int kDataBytes = 8192;                // packed e2m1 codes per page
 constexpr int kScaleBytes = 512;                // e8m0 bytes per page
 constexpr int kTileBytes = 128 * 128;           // one page in the padded 4-bit smem form
-constexpr int kStages = 12;                     // smem pipeline depth (pages in flight)
-constexpr int kDBufs = 2;                       // TMEM accumulator buffers (one per page parity)
-constexpr int kSfbBufs = 12;                    // TMEM scale-factor buffers for B
+// The CTA runs two independent pipeline lanes; a CTA's units alternate between
+// them.  Each lane has its own TMA producer warp, MMA warp, epilogue warpgroup,
+// smem stages, TMEM scale buffers and TMEM accumulator, so every mbarrier has
+// one waiting and one arriving side that walk its phases in order (a parity
+// wait never runs two phases ahead of its barrier, where the parity test
+// could not tell it from done), and each epilogue warpgroup writes whole
+// 8-page units (full 32-byte sectors of the output).  The lanes share only
+// the double-buffered query tile.
+constexpr int kLanes = 2;
+constexpr int kStagesPerLane = 6;               // smem pages in flight per lane
+constexpr int kStages = kLanes * kStagesPerLane;
+constexpr int kSfbPerLane = 6;                  // TMEM scale-factor buffers for B per lane
+constexpr int kSfbBufs = kLanes * kSfbPerLane;
+constexpr int kDBufs = kLanes;                  // one TMEM accumulator per lane
 constexpr int kChunk = 8;                       // pages per work unit
-// Warp roles, as two lanes by page parity: two epilogue warpgroups (warps 0-3
-// and 4-7; warp w reads TMEM lane quadrant w % 4), two TMA producer warps and
-// two MMA warps each take the pages of one parity; an MMA warp copies its
-// pages' scales into TMEM right before their MMAs (the first MMA warp also
-// owns the TMEM allocation).
-constexpr int kEpiSets = 2;
-constexpr int kProdWarps = 2;
-constexpr int kMmaWarps = 2;
+// Warp roles: warps 0-3 and 4-7 are the epilogue warpgroups of lanes 0 and 1
+// (warp w reads TMEM lane quadrant w % 4; lane 0's group also loads the query
+// tiles), warps 8-9 the TMA producers, warps 10-11 the MMA warps (each copies
+// its pages' scales into TMEM right before their MMAs; warp 10 owns the TMEM
+// allocation).
+constexpr int kEpiSets = kLanes;
+constexpr int kProdWarps = kLanes;
+constexpr int kMmaWarps = kLanes;
 constexpr int kProdWarp0 = 4 * kEpiSets;                 // 8
 constexpr int kMmaWarp0 = kProdWarp0 + kProdWarps;       // 10
 constexpr int kThreads = 32 * (kMmaWarp0 + kMmaWarps);
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D[2] x 128 | A (query tile, e4m3) [2] x 32 | SFA[kMmaWarps] x 4 | SFB[12] x 4
+// TMEM columns: D[lanes] x 128 | A (query tile, e4m3) [2] x 32 | SFA[lanes] x 4 | SFB[lanes x 6] x 4
 constexpr uint32_t kTmemACol = kDBufs * 128;
 constexpr uint32_t kTmemSfaCol = kTmemACol + 2 * 32;
 constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4 * kMmaWarps;
@@ -71,17 +82,6 @@ constexpr uint32_t kStageTxBytes = kDataBytes + kScaleBytes;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s per wait
 
 static_assert(kTmemSfbCol + 4 * kSfbBufs <= kTmemCols, "TMEM budget");
-static_assert(kSfbBufs > kDBufs, "an SFB buffer is reused only after its MMA retired");
-static_assert(kStages % kProdWarps == 0, "each producer warp owns a fixed set of stages");
-// Pages are split by parity into independent lanes of the pipeline: page pc is
-// loaded by producer pc % 2, issued by MMA warp pc % 2, read by epilogue set
-// pc % 2, and uses the accumulator, scale buffer and smem stage of the same
-// parity.  Every mbarrier therefore has one waiting side and one arriving side
-// that walk its phases in order, so a parity wait never runs two phases ahead
-// of its barrier (which a parity test could not tell apart from done).
-static_assert(kMmaWarps == kEpiSets && kProdWarps == kEpiSets && kDBufs % kMmaWarps == 0 &&
-                  kSfbBufs % kMmaWarps == 0 && kStages % kMmaWarps == 0,
-              "page-parity pipeline lanes");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling:
 // A = E4M3 (0, bits 7..9), B = E2M1 (5, bits 10..12), both K-major,
@@ -122,7 +122,8 @@ struct SmemLayout {
     static constexpr uint32_t kData = 0;                                   // kStages x 16 KB
     static constexpr uint32_t kScale = kData + kStages * kTileBytes;       // kStages x 512 B
     static constexpr uint32_t kSfa = kScale + kStages * kScaleBytes;       // 512 B of 0x7F
-    static constexpr uint32_t kBars = kSfa + kScaleBytes;
+    static constexpr uint32_t kOut = kSfa + kScaleBytes;                   // lanes x 128 x kChunk floats
+    static constexpr uint32_t kBars = kOut + kLanes * 128 * kChunk * 4;
     // barriers: full[kStages], empty[kStages], sfempty[kSfbBufs], dfull[kDBufs],
     //           dempty[kDBufs], qfull[2], qempty[2], final[kMmaWarps]
     static constexpr uint32_t kNumBars = 2 * kStages + kSfbBufs + 2 * kDBufs + 4 + kMmaWarps;
@@ -325,9 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Every role walks the same sequence of computed pages; page number pc
-    // uses smem stage pc % kStages, scale buffer pc % kSfbBufs and
-    // accumulator pc % kDBufs, and is issued by MMA warp pc % kMmaWarps.
+    // Every role walks the same units in the same order; the units of tiles
+    // with query rows alternate between the two lanes.  Lane l's page stages
+    // are l*kStagesPerLane.., its scale buffers l*kSfbPerLane.., its
+    // accumulator l.
     auto bar = [&](int i) { return sbase + SmemLayout::kBars + 8u * i; };
     auto full_bar = [&](int i) { return bar(i); };
     auto empty_bar = [&](int i) { return bar(kStages + i); };
@@ -381,21 +383,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= kProdWarp0 && warp < kMmaWarp0) {
         // ------------------------------------------------------ producers --
-        // Each producer warp walks all units; lane i fetches the page id of
-        // the unit's i-th live page one unit ahead (so the block-table latency
-        // overlaps the current unit's copies); producer pw issues the TMA
-        // loads of the computed pages pc with pc % kProdWarps == pw.
+        // Producer pw walks its lane's units; lane i of the warp fetches the
+        // page id of the unit's i-th live page one unit ahead (so the
+        // block-table latency overlaps the current unit's copies), one elected
+        // lane issues the TMA loads.
         const int pw = warp - kProdWarp0;
-        int turn = 0;
         const uint64_t policy = kDecode ? l2_policy_evict_first() : l2_policy_evict_last();
         Ring st;
         TileInfo ti;
         ti.tile = -1;
-        // next unit at or after c with live pages: tile info, first page, page count
-        auto next_unit = [&](UnitCursor &c, TileInfo &t, int &j0, int &n) -> bool {
+        // next unit of this lane at or after c with live pages: tile info, first
+        // page, page count; uc counts the units with rows (it picks the lane)
+        auto next_unit = [&](UnitCursor &c, TileInfo &t, int64_t &uc, int &j0, int &n) -> bool {
             for (; c.left > 0; cursor_next(p, c)) {
                 if (c.tile != t.tile) t = tile_info<kDecode>(p, c.tile);
                 if (t.nrows <= 0) continue;
+                const bool mine = (uc & 1) == pw;
+                ++uc;
+                if (!mine) continue;
                 j0 = c.chunk * kChunk;
                 const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
                 const int jc = j1 < t.live_end ? j1 : t.live_end;
@@ -409,15 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             : 0;
         };
         UnitCursor cur = cursor_begin(p, u_begin, u_end);
+        int64_t uc = 0;
         int j0 = 0, n = 0;
-        bool have = next_unit(cur, ti, j0, n);
+        bool have = next_unit(cur, ti, uc, j0, n);
         int64_t raw = have ? fetch_id(ti, j0, n) : 0;
         while (have) {
             UnitCursor c2 = cur;
             cursor_next(p, c2);
             TileInfo ti2 = ti;
+            int64_t uc2 = uc;
             int j02 = 0, n2 = 0;
-            const bool have2 = next_unit(c2, ti2, j02, n2);
+            const bool have2 = next_unit(c2, ti2, uc2, j02, n2);
             const int64_t raw2 = have2 ? fetch_id(ti2, j02, n2) : 0;
             int pid = 0;
             if (lane < n) {
@@ -429,25 +436,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool go = true;
             for (int i = 0; i < n; ++i) {
                 const int id = __shfl_sync(0xffffffffu, pid, i);
-                if (turn == pw) {
-                    go = __all_sync(0xffffffffu, wait_bounded(empty_bar(st.idx), st.ph ^ 1u, abort_flag,
-                                                              kSiteProducerEmpty));
-                    if (!go) break;
-                    if (elect_one()) {
-                        mbar_arrive_expect_tx(full_bar(st.idx), kStageTxBytes);
-                        tma_load_4d(sbase + SmemLayout::kData + st.idx * kTileBytes, &tmap_k, full_bar(st.idx), 0,
-                                    0, 0, id, policy);
-                        tma_load_2d(sbase + SmemLayout::kScale + st.idx * kScaleBytes, &tmap_s, full_bar(st.idx), 0,
-                                    id, policy);
-                    }
-                    __syncwarp();
+                const int stage = pw * kStagesPerLane + st.idx;
+                go = __all_sync(0xffffffffu, wait_bounded(empty_bar(stage), st.ph ^ 1u, abort_flag,
+                                                          kSiteProducerEmpty));
+                if (!go) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(full_bar(stage), kStageTxBytes);
+                    tma_load_4d(sbase + SmemLayout::kData + stage * kTileBytes, &tmap_k, full_bar(stage), 0, 0, 0,
+                                id, policy);
+                    tma_load_2d(sbase + SmemLayout::kScale + stage * kScaleBytes, &tmap_s, full_bar(stage), 0, id,
+                                policy);
                 }
-                if (++turn == kProdWarps) turn = 0;
-                ring_next<kStages>(st);
+                __syncwarp();
+                ring_next<kStagesPerLane>(st);
             }
             if (!go) break;
             cur = c2;
             ti = ti2;
+            uc = uc2;
             j0 = j02;
             n = n2;
             raw = raw2;
@@ -455,22 +461,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
             // Do not leave while copies into this CTA's smem may be in flight:
-            // every armed stage completes (bounded) before the CTA exits.
-            for (int i = pw; i < kStages; i += kProdWarps) {
+            // every armed stage of this lane completes (bounded) before the CTA exits.
+            for (int i = 0; i < kStagesPerLane; ++i) {
                 // stages before st.idx were armed in phase ph, the others in ph^1 (if ever)
                 const uint32_t par = (i < st.idx) ? st.ph : (st.ph ^ 1u);
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(full_bar(i), par) && globaltimer_ns() - t0 < 2000000ull) {
+                while (!mbar_try_wait(full_bar(pw * kStagesPerLane + i), par) &&
+                       globaltimer_ns() - t0 < 2000000ull) {
                 }
             }
         }
         __syncwarp();
     } else if (warp >= kMmaWarp0) {
-        // ----------------------------------------------------- MMA issuers --
-        // Issuer i takes every kMmaWarps-th computed page starting at i; each
-        // tcgen05 instruction costs its issuing thread tens of cycles, so the
-        // pages are spread over several issuing warps.  All ring positions
-        // advance once per computed page, so the control loop has no division.
+        // ------------------------------------------------------ MMA warps --
+        // MMA warp i issues its lane's pages: the page's scales into a TMEM
+        // scale buffer (tcgen05.cp), then 4 block-scaled MMAs (K = 32 each)
+        // into the lane's accumulator, then one commit.  The tcgen05 operations
+        // of one thread run in issue order, so the MMAs see the copied scales
+        // without a commit/wait in between.
         const int issuer = warp - kMmaWarp0;
         {
             // this warp's copy of the unit scale of A (e8m0 127 everywhere)
@@ -479,9 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             const uint64_t bdesc0 = smem_desc(sbase + SmemLayout::kData, 16, 1024, 2);
             const uint64_t sdesc0 = smem_desc(sbase + SmemLayout::kScale, 16, 128, 0);
+            const uint32_t d_tmem = tmem_base + issuer * 128u;
             Ring st, sf, dr;
-            int turn = 0;
-            int64_t qcount = 0;
+            int64_t qcount = 0, uc = 0;
             uint32_t a_tmem = tmem_base + kTmemACol;
             TileInfo ti;
             ti.tile = -1;
@@ -504,41 +512,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (ti.nrows <= 0) continue;
+                const bool mine = (uc & 1) == issuer;
+                ++uc;
+                if (!mine) continue;
                 const int j0 = c.chunk * kChunk;
                 const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
                 const int jc = j1 < ti.live_end ? j1 : ti.live_end;
                 for (int j = j0; j < jc; ++j) {
-                    if (turn == issuer) {
-                        if (!__all_sync(0xffffffffu,
-                                        wait_bounded(full_bar(st.idx), st.ph, abort_flag, kSiteMmaFull) &&
-                                            wait_bounded(sfempty_bar(sf.idx), sf.ph ^ 1u, abort_flag,
-                                                         kSiteMmaScaleEmpty) &&
-                                            wait_bounded(dempty_bar(dr.idx), dr.ph ^ 1u, abort_flag, kSiteMmaDEmpty))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (elect_one()) {
-                            // scales first: the tcgen05 operations of one thread run in issue
-                            // order, so the MMAs below see them with no commit/wait in between
-                            const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sf.idx;
-                            tc_cp_32x128b_warpx4(tmem_sfb,
-                                                 sdesc0 + static_cast<uint64_t>(st.idx * (kScaleBytes >> 4)));
-                            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(st.idx * (kTileBytes >> 4));
-                            const uint32_t d_tmem = tmem_base + dr.idx * 128u;
-                            // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
-                            tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
-                            tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k(1), tmem_sfa, tmem_sfb, 1u);
-                            tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k(2), tmem_sfa, tmem_sfb, 1u);
-                            tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k(3), tmem_sfa, tmem_sfb, 1u);
-                            tc_commit(dfull_bar(dr.idx));
-                        }
-                        __syncwarp();
+                    const int stage = issuer * kStagesPerLane + st.idx;
+                    const int sfb = issuer * kSfbPerLane + sf.idx;
+                    if (!__all_sync(0xffffffffu,
+                                    wait_bounded(full_bar(stage), st.ph, abort_flag, kSiteMmaFull) &&
+                                        wait_bounded(sfempty_bar(sfb), sf.ph ^ 1u, abort_flag, kSiteMmaScaleEmpty) &&
+                                        wait_bounded(dempty_bar(issuer), dr.ph ^ 1u, abort_flag, kSiteMmaDEmpty))) {
+                        ok = false;
+                        break;
                     }
-                    if (++turn == kMmaWarps) turn = 0;
-                    ring_next<kStages>(st);
-                    ring_next<kSfbBufs>(sf);
-                    ring_next<kDBufs>(dr);
+                    tc_fence_after();
+                    if (elect_one()) {
+                        const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sfb;
+                        // descriptor start addresses count 16-byte units
+                        tc_cp_32x128b_warpx4(tmem_sfb, sdesc0 + static_cast<uint64_t>(stage * (kScaleBytes >> 4)));
+                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
+                        // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
+                        tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
+                        tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k(1), tmem_sfa, tmem_sfb, 1u);
+                        tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k(2), tmem_sfa, tmem_sfb, 1u);
+                        tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k(3), tmem_sfa, tmem_sfb, 1u);
+                        tc_commit(dfull_bar(issuer));
+                    }
+                    __syncwarp();
+                    ring_next<kStagesPerLane>(st);
+                    ring_next<kSfbPerLane>(sf);
+                    ring_next<1>(dr);
                 }
             }
             // all MMAs retire before TMEM is released
@@ -551,25 +557,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------- epilogue --
-        // Set `set` (warps 4*set .. 4*set+3) takes the computed pages pc with
-        // pc % kEpiSets == set; set 0 also loads the query tiles and writes
-        // the pages no row can see.
+        // Warpgroup `set` (warps 4*set .. 4*set+3) reads lane `set`'s
+        // accumulator; warpgroup 0 also loads the query tiles.
         const int set = warp / 4;
         const int quad = warp % 4;
         const int m = quad * 32 + lane;            // A row / TMEM lane 0..127
         const int ri = m / kHeads;                 // row within the tile
         const int h = m % kHeads;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        int turn = 0;
+        const uint32_t d_taddr = tmem_base + lane_addr + set * 128u;
+        float *stg = reinterpret_cast<float *>(smem + SmemLayout::kOut) + (set * 128 + m) * kChunk;
         const float sm_scale = p.sm_scale;
         Ring dr;
         int st_idx = 0, sf_idx = 0;
-        int64_t qcount = 0;
+        int64_t qcount = 0, uc = 0;
         TileInfo ti;
         ti.tile = -1;
 
         // Load the query tile of `t` into A buffer qi & 1 once the MMAs of the
-        // tile that used that buffer before have retired (set 0 only).
+        // tile that used that buffer before have retired (warpgroup 0 only).
         auto q_load = [&](const TileInfo &t, int64_t qi) -> bool {
             const int buf = static_cast<int>(qi & 1);
             // warp-uniform outcome, so the .sync.aligned operations below never diverge
@@ -602,6 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            const bool mine = (uc & 1) == set;
+            ++uc;
+            if (!mine) continue;
             const int j0 = c.chunk * kChunk;
             const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
             const bool has_row = ri < ti.nrows;     // uniform per warp
@@ -611,84 +620,93 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = j0; j < j1; ++j) {
                 const int lim = L - j * kPage;   // live tokens of page j for this row
                 if (j < ti.live_end) {
-                    const bool mine = turn == set;
-                    if (++turn == kEpiSets) turn = 0;
-                    if (mine) {
-                        if (!__all_sync(0xffffffffu,
-                                        wait_bounded(dfull_bar(dr.idx), dr.ph, abort_flag, kSiteEpiDFull))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t taddr = tmem_base + lane_addr + dr.idx * 128u;
-                        if (has_row) {
-                            uint32_t v[128];
-                            if (!kLogits) {
-                                float mx;
-                                if (lim >= kPage) {
-                                    mx = tmem_ld_max_32x32b_x128(taddr, v);
-                                } else {
-                                    tmem_ld_32x32b_x128(taddr, v);
-                                    mx = -INFINITY;
-#pragma unroll
-                                    for (int n = 0; n < 128; ++n)
-                                        if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
-                                }
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
-                                // default write-back policy: the two epilogue sets fill one 32-byte
-                                // sector 4 bytes at a time, so it must stay in L2 until complete
-                                row_out[j] = mx * sm_scale;
+                    if (!__all_sync(0xffffffffu, wait_bounded(dfull_bar(set), dr.ph, abort_flag, kSiteEpiDFull))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (has_row) {
+                        uint32_t v[128];
+                        if (!kLogits) {
+                            float mx;
+                            if (lim >= kPage) {
+                                mx = tmem_ld_max_32x32b_x128(d_taddr, v);
                             } else {
-                                tmem_ld_32x32b_x128(taddr, v);
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
-                                float *dst = row_out + static_cast<int64_t>(j) * kPage;
-                                const int valid = p.max_seq_len - j * kPage;   // columns that exist
-                                const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
+                                tmem_ld_32x32b_x128(d_taddr, v);
+                                mx = -INFINITY;
 #pragma unroll
-                                for (int g = 0; g < 32; ++g) {
-                                    float4 o;
-                                    o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
-                                    o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
-                                    o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
-                                    o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
-                                    if (vec) {
-                                        __stcs(reinterpret_cast<float4 *>(dst + 4 * g), o);
-                                    } else {
-                                        if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
-                                        if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
-                                        if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
-                                        if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
-                                    }
-                                }
+                                for (int n = 0; n < 128; ++n)
+                                    if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
                             }
-                        } else {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(dempty_bar(dr.idx));
+                            if (lane == 0) mbar_arrive(dempty_bar(set));
+                            stg[j - j0] = mx * sm_scale;
+                        } else {
+                            tmem_ld_32x32b_x128(d_taddr, v);
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(dempty_bar(set));
+                            float *dst = row_out + static_cast<int64_t>(j) * kPage;
+                            const int valid = p.max_seq_len - j * kPage;   // columns that exist
+                            const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
+#pragma unroll
+                            for (int g = 0; g < 32; ++g) {
+                                float4 o;
+                                o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
+                                o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
+                                o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
+                                o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
+                                if (vec) {
+                                    __stcs(reinterpret_cast<float4 *>(dst + 4 * g), o);
+                                } else {
+                                    if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
+                                    if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
+                                    if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
+                                    if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
+                                }
+                            }
                         }
-                        // the page's MMAs have retired, so its smem stage and
-                        // scale buffer can be refilled
-                        if (quad == 0 && lane == 0) {
-                            mbar_arrive(empty_bar(st_idx));
-                            mbar_arrive(sfempty_bar(sf_idx));
-                        }
+                    } else {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(dempty_bar(set));
                     }
-                    if (++st_idx == kStages) st_idx = 0;
-                    if (++sf_idx == kSfbBufs) sf_idx = 0;
-                    ring_next<kDBufs>(dr);
-                } else if (has_row && set == 0) {
+                    // the page's MMAs have retired, so its smem stage and
+                    // scale buffer can be refilled
+                    if (quad == 0 && lane == 0) {
+                        mbar_arrive(empty_bar(set * kStagesPerLane + st_idx));
+                        mbar_arrive(sfempty_bar(set * kSfbPerLane + sf_idx));
+                    }
+                    if (++st_idx == kStagesPerLane) st_idx = 0;
+                    if (++sf_idx == kSfbPerLane) sf_idx = 0;
+                    ring_next<1>(dr);
+                } else if (has_row) {
                     // no row of the tile sees this page: nothing was computed
                     if (!kLogits) {
-                        row_out[j] = -INFINITY;
+                        stg[j - j0] = -INFINITY;
                     } else {
                         float *dst = row_out + static_cast<int64_t>(j) * kPage;
                         const int valid = p.max_seq_len - j * kPage;
                         for (int cc = 0; cc < kPage && cc < valid; ++cc) dst[cc] = -INFINITY;
                     }
+                }
+            }
+            if (!ok) break;
+            if (!kLogits && has_row) {
+                // the whole unit (up to 8 pages, one 32-byte sector) at once
+                float *dst = row_out + j0;
+                const int n = j1 - j0;
+                if (n == kChunk && (p.out_row_stride & 3) == 0) {
+                    const float4 *src = reinterpret_cast<const float4 *>(stg);
+                    __stcs(reinterpret_cast<float4 *>(dst), src[0]);
+                    __stcs(reinterpret_cast<float4 *>(dst) + 1, src[1]);
+                } else if (n == kChunk && (p.out_row_stride & 1) == 0) {
+                    const float2 *src = reinterpret_cast<const float2 *>(stg);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) __stcs(reinterpret_cast<float2 *>(dst) + i, src[i]);
+                } else {
+                    for (int i = 0; i < n; ++i) dst[i] = stg[i];
                 }
             }
         }
