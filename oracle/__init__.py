@@ -82,6 +82,14 @@ def _load():
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int64,
             c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.orc_e2m1_from_double.restype = ctypes.c_int
+        lib.orc_e2m1_from_double.argtypes = [ctypes.c_double]
+        lib.orc_quantize_group.restype = ctypes.c_int
+        lib.orc_quantize_group.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        lib.orc_write_index_k.restype = ctypes.c_int64
+        lib.orc_write_index_k.argtypes = [
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
         lib.orc_live_pairs.restype = ctypes.c_int64
         lib.orc_live_pairs.argtypes = [
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -210,3 +218,39 @@ def live_pairs(*, decode: bool, seq_lens, max_seq_len: int, cu_seqlens_q=None,
                                   int(sl.shape[0]), int(max_seq_len),
                                   rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
                                   rows.shape[0]))
+
+
+# ------------------------------------------------------------------ writer --
+def e2m1_from_double(x: float) -> int:
+    """Round a real to an e2m1 code: nearest value, ties to the even code,
+    saturating at 6, sign kept (the writer reading in ``mx4_oracle.c``)."""
+    return _load().orc_e2m1_from_double(float(x))
+
+
+def quantize_group(x) -> tuple[int, np.ndarray]:
+    """One 32-element group -> (e8m0 scale byte, 32 e2m1 codes), following the
+    OCP MX conversion reading stated in ``mx4_oracle.c``."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    assert a.shape == (32,)
+    codes = np.empty(32, dtype=np.uint8)
+    byte = _load().orc_quantize_group(_ptr(a), _ptr(codes))
+    return int(byte), codes
+
+
+def write_index_k(*, k_bits: np.ndarray, slot_mapping, k_data: np.ndarray, k_scale: np.ndarray,
+                  k_data_page_stride: int, k_scale_page_stride: int, num_pool_pages: int = 0) -> int:
+    """Quantise bf16 keys (uint16 bit patterns [num_tokens, W], W >= 128; the
+    key is the first 128 elements of each row) into the page slots of
+    ``slot_mapping`` (int64; slot s = token s % 128 of page s // 128,
+    negative = skip).  ``k_data`` / ``k_scale`` are flat uint8 buffers written
+    in place.  Returns the count of slots outside the pool (skipped)."""
+    k = np.ascontiguousarray(np.asarray(k_bits))
+    assert k.dtype == np.uint16 and k.ndim == 2 and k.shape[1] >= DIM
+    n = k.shape[0]
+    assert k_data.dtype == np.uint8 and k_data.flags.c_contiguous
+    assert k_scale.dtype == np.uint8 and k_scale.flags.c_contiguous
+    sm = np.ascontiguousarray(np.asarray(slot_mapping, dtype=np.int64))
+    assert sm.shape == (n,)
+    return int(_load().orc_write_index_k(_ptr(k), n, int(k.shape[1]), _ptr(sm), _ptr(k_data),
+                                         _ptr(k_scale), int(k_data_page_stride),
+                                         int(k_scale_page_stride), int(num_pool_pages)))

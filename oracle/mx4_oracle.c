@@ -324,3 +324,120 @@ int64_t orc_live_pairs(int decode, const int32_t *cu_seqlens_q, const int32_t *s
     }
     return total;
 }
+
+/* ------------------------------------------------------- the page writer -- */
+/*
+ * Quantising a bf16 index key into an MXFP4 page slot.  The pages say only
+ * that the index key is quantised straight into the 8704 B pool page (ATOM
+ * #2770 "MiniMax-M3.1 MXFP4 sparse KV cache and index cache", section "How it
+ * works", item "Write") with a per-1x32 MXFP4 quantiser (aiter #7061,
+ * section "Tests": the cache is built with per_1x32_f4_quant).  They do not
+ * state the rounding rule.  READING, from the OCP Microscaling Formats (MX)
+ * v1.0 conversion rule:
+ *   - shared exponent of a 32-element group: E = floor(log2(amax)) - 2, where
+ *     2 is the largest exponent of e2m1 (its top value 6 = 1.5 x 2^2);
+ *   - scale byte = E + 127, clamped to [1, 254] (the scorer's contract
+ *     excludes bytes 0 and 255); an all-zero group takes byte 127;
+ *   - element = x / 2^(byte-127) rounded to the nearest e2m1 value, ties to
+ *     the even code, magnitudes past 6 saturate to 6, sign kept (also for a
+ *     result of zero).
+ * Inputs are finite (bf16 Inf/NaN are outside the contract).
+ */
+
+/* Round a real value to an e2m1 code: nearest of {0,.5,1,1.5,2,3,4,6} in
+ * magnitude, ties to the even code, saturating at 6, sign bit kept. */
+int orc_e2m1_from_double(double x)
+{
+    int sign = signbit(x) ? 8 : 0;
+    double a = fabs(x), q, n, fl, frac, r, v;
+    int e, E;
+
+    if (a >= 6.0)
+        return sign | 7;
+    if (a == 0.0)
+        return sign;
+    frexp(a, &e);
+    E = e - 1;             /* floor(log2(a)) */
+    if (E < 0)
+        E = 0;             /* below 1 the spacing stays 1/2 (subnormal 0.5) */
+    q = ldexp(1.0, E - 1); /* spacing of e2m1 values in this binade */
+    n = a / q;
+    fl = floor(n);
+    frac = n - fl;
+    if (frac > 0.5)
+        r = fl + 1.0;
+    else if (frac < 0.5)
+        r = fl;
+    else
+        r = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+    v = r * q;             /* at most 6: 5.x rounds to 4 or 6 */
+    if (v == 0.0)
+        return sign;
+    if (v < 1.0)
+        return sign | 1;                       /* 0.5 */
+    frexp(v, &e);
+    E = e - 1;                                 /* 0, 1 or 2 */
+    return sign | ((E + 1) << 1) | (int)(ldexp(v, 1 - E) - 2.0);
+}
+
+/* One 32-element group: its scale byte and 32 codes (code i for element i). */
+int orc_quantize_group(const double *x, uint8_t *codes)
+{
+    double amax = 0.0;
+    int e, byte;
+    for (int i = 0; i < 32; ++i)
+        if (fabs(x[i]) > amax)
+            amax = fabs(x[i]);
+    if (amax == 0.0) {
+        byte = 127;
+    } else {
+        frexp(amax, &e);
+        byte = (e - 1) - 2 + 127;
+        if (byte < 1)
+            byte = 1;
+        if (byte > 254)
+            byte = 254;
+    }
+    for (int i = 0; i < 32; ++i)
+        codes[i] = (uint8_t)orc_e2m1_from_double(x[i] / ldexp(1.0, byte - 127));
+    return byte;
+}
+
+/*
+ * Write num_tokens bf16 keys (row t at k + t*k_row_stride elements, 128
+ * elements each) into the page slots named by slot_mapping: slot s is token
+ * s % 128 of physical page s / 128.  Token i of page p keeps its 64 code bytes
+ * at k_data[p*sd + i*64] (element 2c in the low nibble of byte c, 2c+1 in the
+ * high nibble) and its 4 scale bytes at k_scale[p*ss + i*4] (byte g for
+ * elements 32g..32g+31).  Negative slots are skipped (padding); a slot whose
+ * page is outside [0, num_pool_pages) (when num_pool_pages > 0) is skipped
+ * and counted.  Returns the number of such out-of-pool slots.
+ */
+int64_t orc_write_index_k(const uint16_t *k, int64_t num_tokens, int64_t k_row_stride,
+                          const int64_t *slot_mapping, uint8_t *k_data, uint8_t *k_scale,
+                          int64_t sd, int64_t ss, int64_t num_pool_pages)
+{
+    int64_t bad = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        int64_t p = s / ORC_PAGE, i = s % ORC_PAGE;
+        if (num_pool_pages > 0 && p >= num_pool_pages) {
+            ++bad;
+            continue;
+        }
+        uint8_t *dst = k_data + p * sd + i * ORC_TOKEN_DATA_BYTES;
+        uint8_t *sdst = k_scale + p * ss + i * ORC_TOKEN_SCALE_BYTES;
+        for (int g = 0; g < 4; ++g) {
+            double x[32];
+            uint8_t codes[32];
+            for (int j = 0; j < 32; ++j)
+                x[j] = orc_bf16_value(k[t * k_row_stride + 32 * g + j]);
+            sdst[g] = (uint8_t)orc_quantize_group(x, codes);
+            for (int c = 0; c < 16; ++c)
+                dst[16 * g + c] = (uint8_t)(codes[2 * c] | (codes[2 * c + 1] << 4));
+        }
+    }
+    return bad;
+}

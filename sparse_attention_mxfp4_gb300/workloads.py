@@ -338,3 +338,139 @@ def sample_rows(w: Workload, n: int, seed: int = 0) -> np.ndarray:
     pick = torch.randperm(total, generator=g)[: max(0, n - 2)].tolist()
     s = sorted(set(pick) | {0, total - 1})
     return np.array(s[:n] if len(s) > n else s, dtype=np.int64)
+
+
+# ------------------------------------------------------------ index-K writes --
+@dataclasses.dataclass
+class WriteCase:
+    """Keys to quantise into pool page slots.
+
+    ``k`` is [num_tokens, row_width] bfloat16; the key of token t is
+    ``k[t, :128]`` (``row_width`` > 128 models a key that is a slice of a wider
+    projection output).  ``slot_mapping[t]`` = page * 128 + token-in-page, or
+    -1 for a padding token that is not written."""
+    name: str
+    k: torch.Tensor
+    slot_mapping: torch.Tensor      # [num_tokens] int64
+    num_pool_pages: int
+    layout: str                     # "single" or "split"
+    k_data_page_stride: int
+    k_scale_page_stride: int
+    description: str = ""
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.k.shape[0])
+
+    @property
+    def k_row_stride(self) -> int:
+        return int(self.k.stride(0))
+
+    def pool_view(self) -> Workload:
+        """A Workload shell carrying only the pool geometry (for pool_nbytes)."""
+        return Workload(name=self.name, decode=True, q=torch.empty(0, HEADS, DIM, dtype=torch.bfloat16),
+                        q_is_e4m3=False, pages_data=torch.empty(0, PAGE, DIM // 2, dtype=torch.uint8),
+                        pages_scale=torch.empty(0, PAGE, DIM // 32, dtype=torch.uint8),
+                        page_ids=torch.empty(0, dtype=torch.int64), num_pool_pages=self.num_pool_pages,
+                        layout=self.layout, k_data_page_stride=self.k_data_page_stride,
+                        k_scale_page_stride=self.k_scale_page_stride,
+                        block_table=torch.empty(0, 1, dtype=torch.int32),
+                        seq_lens=torch.empty(0, dtype=torch.int32), cu_seqlens_q=None, prefix_lens=None,
+                        max_query_len=0, max_seq_len=0)
+
+
+def _keys(g, n, width, dist):
+    """bf16 keys.  "normal": N(0, 1).  "wide": N(0, 1) times 2^u per 32-element
+    group with u uniform in [-60, 60], plus all-zero groups, signed zeros,
+    groups near the bottom of the bf16 range (subnormals included) and near the
+    top, so every scale byte branch and rounding tie occurs."""
+    x = torch.randn((n, width), generator=g, dtype=torch.float32)
+    if dist == "wide":
+        grp = x[:, :DIM].view(n, DIM // 32, 32)
+        u = torch.randint(-60, 61, (n, DIM // 32, 1), generator=g).to(torch.float32)
+        grp.mul_(torch.exp2(u))
+        sel = torch.rand((n, DIM // 32), generator=g)
+        grp[sel < 0.03] = 0.0
+        tiny = (sel >= 0.03) & (sel < 0.06)
+        grp[tiny] = torch.randn((int(tiny.sum()), 32), generator=g) * 2.0 ** -128
+        huge = (sel >= 0.06) & (sel < 0.08)
+        grp[huge] = torch.randn((int(huge.sum()), 32), generator=g) * 2.0 ** 120
+        z = torch.rand((n, DIM), generator=g) < 0.01
+        x[:, :DIM][z] = 0.0
+        negz = torch.rand((n, DIM), generator=g) < 0.005
+        x[:, :DIM][negz] = -0.0
+    elif dist != "normal":
+        raise ValueError(dist)
+    return x.to(torch.bfloat16)
+
+
+def make_write_case(name, *, seed, num_tokens, num_pool_pages, row_width=DIM, layout="single",
+                    k_data_page_stride=None, k_scale_page_stride=None, dist="normal",
+                    pad_every=0, block_table=None, positions=None, description="") -> WriteCase:
+    """Seeded write case.  Slots come from ``block_table`` [B, width] and
+    ``positions`` (pairs (b, pos): slot = block_table[b, pos // 128] * 128 +
+    pos % 128) when given, else from a seeded draw of distinct slots of the
+    pool.  Every ``pad_every``-th token (when > 0) is padding (slot -1)."""
+    g = _gen(seed)
+    k = _keys(g, num_tokens, row_width, dist)
+    if block_table is not None:
+        b, pos = positions
+        slot = block_table[b, pos // PAGE].to(torch.int64) * PAGE + pos % PAGE
+    else:
+        slot = torch.randperm(num_pool_pages * PAGE, generator=g)[:num_tokens].to(torch.int64)
+    slot = slot.clone()
+    if pad_every > 0:
+        slot[::pad_every] = -1
+    if layout == "single":
+        sd = ss = k_data_page_stride or PAGE_BYTES
+    else:
+        sd = k_data_page_stride or DATA_BYTES
+        ss = k_scale_page_stride or SCALE_BYTES
+    return WriteCase(name=name, k=k, slot_mapping=slot, num_pool_pages=num_pool_pages, layout=layout,
+                     k_data_page_stride=sd, k_scale_page_stride=ss, description=description)
+
+
+def write_pool(c: WriteCase, device="cpu", fill_seed: Optional[int] = 4321):
+    """Pool buffers for a write case, filled with seeded random bytes (so a
+    test can see which bytes a write touched).  Returns (buffers, (data_buf,
+    data_offset), (scale_buf, scale_offset)) like ``build_pool``."""
+    nd, ns = pool_nbytes(c.pool_view())
+
+    def alloc(n):
+        t = torch.randint(0, 256, (n,), generator=_gen(fill_seed), dtype=torch.uint8)
+        return t.to(device)
+    if c.layout == "single":
+        buf = alloc(nd)
+        return [buf], (buf, 0), (buf, DATA_BYTES)
+    dbuf = alloc(nd)
+    sbuf = alloc(ns)
+    return [dbuf, sbuf], (dbuf, 0), (sbuf, 0)
+
+
+WRITE_CONFIG_NAMES = ("write-decode", "write-chunk")
+
+
+def make_write_config(name: str, seed: Optional[int] = None) -> WriteCase:
+    """Index-K writes of the measured workloads: one new key per request of
+    the decode workload (64 tokens), and the 32768 new keys of the chunked
+    prefill (positions 100000..132767 of its request)."""
+    if name == "write-decode":
+        seed = 10 if seed is None else seed
+        g = _gen(seed + 1000)
+        bt = torch.randperm(70000, generator=g)[: 64 * 1025].view(64, 1025).to(torch.int32)
+        pos = torch.full((64,), 131072, dtype=torch.int64)
+        return make_write_case(name, seed=seed, num_tokens=64, num_pool_pages=70000, layout="split",
+                               k_data_page_stride=8320, k_scale_page_stride=576, block_table=bt,
+                               positions=(torch.arange(64), pos),
+                               description="64 requests x 1 new key at position 131072, split views, "
+                                           "70000-page pool")
+    if name == "write-chunk":
+        seed = 11 if seed is None else seed
+        g = _gen(seed + 1000)
+        bt = torch.randperm(1200, generator=g)[:1038].view(1, 1038).to(torch.int32)
+        pos = torch.arange(100000, 132768, dtype=torch.int64)
+        return make_write_case(name, seed=seed, num_tokens=32768, num_pool_pages=1200, layout="single",
+                               block_table=bt, positions=(torch.zeros_like(pos), pos),
+                               description="32768 keys at positions 100000..132767 of one request, "
+                                           "1200-page pool")
+    raise KeyError(name)
