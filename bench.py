@@ -131,10 +131,16 @@ class ClockSampler:
 
 
 def library_source_hash():
+    """Hash of the CUDA sources' code (comments and blank lines removed), so a
+    committed ncu summary stays matched to the code it measured."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_attention_mxfp4_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, name), "rb").read())
+        text = open(os.path.join(csrc, name)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update(name.encode() + b"\0" + "\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 
@@ -286,6 +292,58 @@ def secondary_configs(names, peaks, stream):
     return res
 
 
+def writer_work(case):
+    """Algorithmic bytes of one index-K write: per written token 256 B of bf16
+    key read, 64 + 4 B of page bytes written, 8 B of slot read."""
+    n = int((case.slot_mapping >= 0).sum())
+    return {"tokens": n, "bytes": n * (2 * 128 + 64 + 4 + 8)}
+
+
+def secondary_writer(peaks, stream, steps=20):
+    """The index-K page writer on its measured workloads, each call timed
+    alone with CUDA events after a 256 MiB L2 flush (the keys and pages of one
+    call fit in L2)."""
+    import torch
+    import sparse_attention_mxfp4_gb300 as mx4
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    res = {}
+    for name in W.WRITE_CONFIG_NAMES:
+        case = W.make_write_config(name)
+        bufs, (dbuf, doff), (sbuf, soff) = W.write_pool(case, device="cuda")
+        k = case.k.cuda()
+        sm = case.slot_mapping.cuda()
+
+        def call():
+            mx4.mx4_index_k_write(k, sm, dbuf[doff:], sbuf[soff:], case.k_data_page_stride,
+                                  case.k_scale_page_stride, num_pool_pages=case.num_pool_pages, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+            evs = []
+            for _ in range(steps):
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        work = writer_work(case)
+        gbs = work["bytes"] / (us * 1e-6) / 1e9
+        res[name] = {"us_per_call": round(us, 3), "steps": steps, "tokens": work["tokens"],
+                     "bytes_per_call": work["bytes"], "hbm_gbs_algorithmic": round(gbs, 1),
+                     "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                     "l2": "flushed before each call (256 MiB write)",
+                     "description": case.description}
+        del bufs, dbuf, sbuf, k, sm
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -379,6 +437,7 @@ def run_ours(args):
             torch.cuda.empty_cache()
             names = [n for n in W.CONFIG_NAMES if n != w.name]
             line["secondary"] = secondary_configs(names, peaks, stream)
+            line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()

@@ -74,7 +74,7 @@ typedef enum {
 } mx4_status;
 
 /* Device status bits (mx4_index_get_device_status). */
-#define MX4_DEV_BAD_PAGE 0x1u /* a live page id was outside [0, num_pool_pages) */
+#define MX4_DEV_BAD_PAGE 0x1u /* a live page id (scorer) or a slot's page (writer) was outside [0, num_pool_pages) */
 #define MX4_DEV_TIMEOUT 0x2u  /* an internal wait gave up; the kernel returned early */
 /* With MX4_DEV_TIMEOUT, bit (8 + site) names the wait that gave up: site 0 =
  * producer waiting for a free smem stage, 1 = MMA waiting for the query tile,
@@ -166,6 +166,42 @@ mx4_status mx4_index_logits_decode(const void *q, int q_is_e4m3, const uint8_t *
  * device pointers; n >= 0.
  */
 mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t n, void *stream);
+
+/*
+ * Index-K page writer: quantise num_tokens bf16 keys into MXFP4 page slots.
+ * [P2] "How it works", item "Write": the index key is quantised straight
+ * into its 8704 B pool page, no bf16 stage; [P1] "Tests": the cache is built
+ * by a per-1x32 MXFP4 quantiser; [P1] "Format" for the page.  The rounding
+ * rule is not stated by the sources; this call implements the OCP MX v1.0
+ * conversion: per 32-element group, scale byte = floor(log2 amax) - 2 + 127
+ * clamped to [1, 254] (127 for an all-zero group), each element rounded to
+ * the nearest e2m1 value of x / 2^(byte-127), ties to the even code,
+ * saturating at 6, its sign bit kept.
+ *
+ *   k             bf16 bits, key of token t = 128 elements at
+ *                 k + t * k_row_stride (elements); k_row_stride >= 128.
+ *                 2-byte aligned (rows 16-byte aligned take 128-bit loads).
+ *   slot_mapping  int64 [num_tokens]: slot s = token s % 128 of page s / 128;
+ *                 a negative slot is padding and writes nothing.
+ *   k_data, k_scale, strides   the page views of the scorer calls: token i
+ *                 of page p gets its 64 code bytes at k_data + p *
+ *                 k_data_page_stride + 64 i and its 4 scale bytes at k_scale
+ *                 + p * k_scale_page_stride + 4 i.  k_data 16-byte aligned,
+ *                 k_data_page_stride >= 8192 and a multiple of 16; k_scale
+ *                 4-byte aligned, k_scale_page_stride >= 512 and a multiple
+ *                 of 4.
+ *   num_pool_pages  > 0: a slot whose page is >= num_pool_pages is skipped
+ *                 and sets MX4_DEV_BAD_PAGE; <= 0: unchecked.
+ *
+ * All pointers are caller-owned device pointers.  num_tokens == 0 returns
+ * MX4_OK without checking pointers.  Bytes of slots not named are not
+ * touched; two tokens naming one slot race (either result may remain).
+ * Keys must be finite (Inf/NaN give unspecified codes, no fault).
+ */
+mx4_status mx4_index_k_write(const void *k, int64_t num_tokens, int64_t k_row_stride,
+                             const int64_t *slot_mapping, uint8_t *k_data, uint8_t *k_scale,
+                             int64_t k_data_page_stride, int64_t k_scale_page_stride,
+                             int64_t num_pool_pages, void *stream);
 
 /*
  * Read the current device's status word (MX4_DEV_* bits, ORed by every call

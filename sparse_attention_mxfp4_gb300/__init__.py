@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "mx4_index_logits_prefill",
     "mx4_index_logits_decode",
     "mx4_quantize_q_e4m3",
+    "mx4_index_k_write",
     "mx4_index_get_device_status",
     "mx4_status_string",
     "mx4_abi_version",
@@ -80,6 +81,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             f.argtypes = args
         lib.mx4_quantize_q_e4m3.restype = i32
         lib.mx4_quantize_q_e4m3.argtypes = [vp, vp, i64, vp]
+        lib.mx4_index_k_write.restype = i32
+        lib.mx4_index_k_write.argtypes = [vp, i64, i64, vp, vp, vp, i64, i64, i64, vp]
         lib.mx4_index_get_device_status.restype = i32
         lib.mx4_index_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.mx4_status_string.restype = ctypes.c_char_p
@@ -199,6 +202,30 @@ def mx4_quantize_q_e4m3(q_bf16, out=None, *, stream=None):
     _check("mx4_quantize_q_e4m3",
            lib.mx4_quantize_q_e4m3(_ptr(q_bf16), _ptr(out), q_bf16.numel(), _stream(stream)))
     return out
+
+
+def mx4_index_k_write(k, slot_mapping, k_data, k_scale, k_data_page_stride, k_scale_page_stride, *,
+                      num_pool_pages=0, stream=None):
+    """Quantise bf16 keys into MXFP4 page slots (``mx4_index_k_write``).
+
+    ``k``: bfloat16 [num_tokens, >=128] with unit inner stride (the key is the
+    first 128 elements of each row); ``slot_mapping``: int64 [num_tokens]
+    (page * 128 + token-in-page, negative = padding); ``k_data`` /
+    ``k_scale``: uint8 tensors whose first byte is page 0 of each view.
+    Writes in place; returns nothing."""
+    import torch
+    lib = load_library()
+    if k.dtype != torch.bfloat16 or k.dim() != 2 or k.stride(1) != 1:
+        raise ValueError("k must be a 2-D bfloat16 tensor with unit inner stride")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous() \
+            or tuple(slot_mapping.shape) != (k.shape[0],):
+        raise ValueError("slot_mapping must be a contiguous int64 tensor of shape [num_tokens]")
+    if k_data.dtype != torch.uint8 or k_scale.dtype != torch.uint8:
+        raise ValueError("k_data and k_scale must be uint8 tensors")
+    _check("mx4_index_k_write",
+           lib.mx4_index_k_write(_ptr(k), k.shape[0], k.stride(0), _ptr(slot_mapping), _ptr(k_data),
+                                 _ptr(k_scale), int(k_data_page_stride), int(k_scale_page_stride),
+                                 int(num_pool_pages), _stream(stream)))
 
 
 def mx4_index_get_device_status(stream=None) -> int:

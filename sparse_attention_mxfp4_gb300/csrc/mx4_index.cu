@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "score_kernel.cuh"
+#include "writer_kernel.cuh"
 
 namespace {
 
@@ -286,6 +287,44 @@ mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t 
     cudaGetLastError();
     mx4::mx4_quantize_q_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         q_bf16, q_e4m3, n, vec);
+    return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
+}
+
+mx4_status mx4_index_k_write(const void *k, int64_t num_tokens, int64_t k_row_stride,
+                             const int64_t *slot_mapping, uint8_t *k_data, uint8_t *k_scale,
+                             int64_t k_data_page_stride, int64_t k_scale_page_stride, int64_t num_pool_pages,
+                             void *stream)
+{
+    if (num_tokens < 0) return MX4_ERR_INVALID_ARG;
+    if (num_tokens == 0) return MX4_OK;
+    if (!k || !slot_mapping || !k_data || !k_scale) return MX4_ERR_INVALID_ARG;
+    if (k_row_stride < mx4::kDim) return MX4_ERR_INVALID_ARG;
+    if (k_data_page_stride < mx4::kDataBytes || k_scale_page_stride < mx4::kScaleBytes) return MX4_ERR_INVALID_ARG;
+    if (!aligned(k, 2) || !aligned(slot_mapping, 8)) return MX4_ERR_MISALIGNED;
+    if (!aligned(k_data, 16) || (k_data_page_stride % 16) != 0) return MX4_ERR_MISALIGNED;
+    if (!aligned(k_scale, 4) || (k_scale_page_stride % 4) != 0) return MX4_ERR_MISALIGNED;
+    if (num_tokens > (INT64_MAX / 4) / k_row_stride) return MX4_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MX4_ERR_CUDA;
+    mx4::WriteParams p;
+    p.k = static_cast<const uint16_t *>(k);
+    p.slot_mapping = slot_mapping;
+    p.k_data = k_data;
+    p.k_scale = k_scale;
+    p.num_tokens = num_tokens;
+    p.k_row_stride = k_row_stride;
+    p.k_data_page_stride = k_data_page_stride;
+    p.k_scale_page_stride = k_scale_page_stride;
+    p.num_pool_pages = num_pool_pages;
+    p.vec = aligned(k, 16) && (k_row_stride % 8) == 0;
+    // four threads per token; at most 8 resident 256-thread blocks per SM,
+    // the rest of the tokens by a grid-stride loop
+    int64_t blocks = (num_tokens * 4 + 255) / 256;
+    if (blocks > 8LL * sms) blocks = 8LL * sms;
+    cudaGetLastError();
+    mx4::mx4_write_index_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 

@@ -5,18 +5,21 @@
 // rows x 64 heads = 128 rows of the MMA A operand (R = 2 for prefill, 1 for
 // decode, where lanes 64..127 stay zero).
 //
-// Roles (warp-specialised, 192 threads):
-//   warps 0-3  epilogue: load Q, round bf16 -> e4m3 in registers and store it
-//              into TMEM as the MMA's A operand (thread m owns TMEM lane m);
-//              per page read the fp32 accumulator from TMEM (tcgen05.ld.red
-//              returns the page max of a fully live page in the load itself),
-//              apply the causal mask on partial pages, scale by sm_scale and
-//              store (or emit per-token logits).
-//   warp 4     producer: per live page, look up the physical page id in the
-//              block table and issue two TMA loads: the 8 KB of e2m1 codes
-//              (unpacked in flight to the 16 KB padded layout the tensor core
-//              reads) and the 512 B of e8m0 scales.
-//   warp 5     MMA issuer: copies the page's scales into TMEM (tcgen05.cp)
+// Roles (warp-specialised, 384 threads, two independent pipeline lanes that
+// take alternate units; the constants below give the warp numbers):
+//   epilogue warpgroup (one per lane): warpgroup 0 also loads Q, rounds bf16
+//              -> e4m3 in registers and stores it into TMEM as the MMA's A
+//              operand (thread m owns TMEM lane m); per page each thread reads
+//              its fp32 accumulator row from TMEM (tcgen05.ld.red returns the
+//              page max of a fully live page in the load itself), applies the
+//              causal mask on partial pages and sm_scale, stages the unit's 8
+//              page maxima in smem and writes them as one 32-byte sector (or
+//              emits per-token logits).
+//   producer warp (one per lane): per live page, look up the physical page
+//              id in the block table and issue two TMA loads: the 8 KB of e2m1
+//              codes (unpacked in flight to the 16 KB padded layout the tensor
+//              core reads) and the 512 B of e8m0 scales.
+//   MMA warp (one per lane): copies the page's scales into TMEM (tcgen05.cp)
 //              and issues 4 block-scaled MMAs (K = 32 each) of
 //              kind::mxf8f6f4: A = Q from TMEM (e4m3, unit scale), B = K page
 //              from smem (e2m1 with its e8m0 bytes), D = 128 x 128 fp32 in TMEM.

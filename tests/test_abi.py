@@ -110,6 +110,30 @@ def test_quantize_rejections(lib):
     assert lib.mx4_quantize_q_e4m3(A + 1, A, 16, None) == mx4.MX4_ERR_MISALIGNED
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(n=0, k=None, slots=None), mx4.MX4_OK),                  # nothing to do
+    (dict(k=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(slots=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(kd=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(ks=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(row=127), mx4.MX4_ERR_INVALID_ARG),                     # narrow key rows
+    (dict(sd=8176), mx4.MX4_ERR_INVALID_ARG),                     # narrow data view
+    (dict(ss=508), mx4.MX4_ERR_INVALID_ARG),                      # narrow scale view
+    (dict(k=A + 1), mx4.MX4_ERR_MISALIGNED),
+    (dict(slots=A + 4), mx4.MX4_ERR_MISALIGNED),
+    (dict(kd=A + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(sd=8192 + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(ks=A + 2), mx4.MX4_ERR_MISALIGNED),
+    (dict(ss=514), mx4.MX4_ERR_MISALIGNED),
+])
+def test_writer_rejections(lib, kw, status):
+    a = dict(k=A, n=16, row=128, slots=A, kd=A, ks=A, sd=8704, ss=8704, pages=4)
+    a.update(kw)
+    assert lib.mx4_index_k_write(a["k"], a["n"], a["row"], a["slots"], a["kd"], a["ks"], a["sd"], a["ss"],
+                                 a["pages"], None) == status
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import importlib
     missing = str(tmp_path / "nope.so")
