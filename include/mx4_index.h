@@ -80,8 +80,7 @@ typedef enum {
  * producer waiting for a free smem stage, 1 = MMA waiting for the query tile,
  * 2 = MMA waiting for a page's bytes, 3 = MMA waiting for a free
  * accumulator, 4 = epilogue waiting for a free query buffer, 5 = epilogue
- * waiting for an accumulator, 6 = MMA waiting for a free scale buffer.
- * Diagnostic only. */
+ * waiting for an accumulator.  Diagnostic only. */
 
 /*
  * Block scores for ragged prefill (causal) rows.  [P1] "Kernels":

@@ -5,8 +5,8 @@
 // rows x 64 heads = 128 rows of the MMA A operand (R = 2 for prefill, 1 for
 // decode, where lanes 64..127 stay zero).
 //
-// Roles (warp-specialised, 384 threads, two independent pipeline lanes that
-// take alternate units; the constants below give the warp numbers):
+// Roles (warp-specialised, 480 threads, three independent pipeline lanes
+// that take the units in rotation; the constants below give the warp numbers):
 //   epilogue warpgroup (one per lane): warpgroup 0 also loads Q, rounds bf16
 //              -> e4m3 in registers and stores it into TMEM as the MMA's A
 //              operand (thread m owns TMEM lane m); per page each thread reads
@@ -15,11 +15,11 @@
 //              causal mask on partial pages and sm_scale, stages the unit's 8
 //              page maxima in smem and writes them as one 32-byte sector (or
 //              emits per-token logits).
-//   producer warp (one per lane): per live page, look up the physical page
-//              id in the block table and issue two TMA loads: the 8 KB of e2m1
-//              codes (unpacked in flight to the 16 KB padded layout the tensor
-//              core reads) and the 512 B of e8m0 scales.
-//   MMA warp (one per lane): copies the page's scales into TMEM (tcgen05.cp)
+//   lane warp (one per lane), TMA side: per live page, look up the physical
+//              page id in the block table and issue two TMA loads: the 8 KB of
+//              e2m1 codes (unpacked in flight to the 16 KB padded layout the
+//              tensor core reads) and the 512 B of e8m0 scales.
+//   lane warp, MMA side: copies the page's scales into TMEM (tcgen05.cp)
 //              and issues 4 block-scaled MMAs (K = 32 each) of
 //              kind::mxf8f6f4: A = Q from TMEM (e4m3, unit scale), B = K page
 //              from smem (e2m1 with its e8m0 bytes), D = 128 x 128 fp32 in TMEM.
@@ -48,34 +48,40 @@ constexpr int kPage = 128;
 constexpr int kDataBytes = 8192;                // packed e2m1 codes per page
 constexpr int kScaleBytes = 512;                // e8m0 bytes per page
 constexpr int kTileBytes = 128 * 128;           // one page in the padded 4-bit smem form
-// The CTA runs two independent pipeline lanes; a CTA's units alternate between
-// them.  Each lane has its own TMA producer warp, MMA warp, epilogue warpgroup,
-// smem stages, TMEM scale buffers and TMEM accumulator, so every mbarrier has
-// one waiting and one arriving side that walk its phases in order (a parity
-// wait never runs two phases ahead of its barrier, where the parity test
-// could not tell it from done), and each epilogue warpgroup writes whole
-// 8-page units (full 32-byte sectors of the output).  The lanes share only
-// the double-buffered query tile.
-constexpr int kLanes = 2;
-constexpr int kStagesPerLane = 6;               // smem pages in flight per lane
+// The CTA runs three independent pipeline lanes; a CTA's units go to them in
+// rotation.  Each lane has its own lane warp (TMA loads and MMAs), epilogue
+// warpgroup, smem stages, TMEM scale buffers and TMEM accumulator, so every
+// mbarrier has one waiting and one arriving side that walk its phases in
+// order (a parity wait never runs two phases ahead of its barrier, where the
+// parity test could not tell it from done), and each epilogue warpgroup
+// writes whole 8-page units (full 32-byte sectors of the output).  With one
+// accumulator per lane, a lane's page period is the serial chain MMA issue ->
+// MMA completion -> epilogue TMEM read -> accumulator release; three lanes
+// overlap three such chains on the tensor pipe.  The lanes share only the
+// double-buffered query tile.
+constexpr int kLanes = 3;
+constexpr int kStagesPerLane = 4;               // smem pages in flight per lane
 constexpr int kStages = kLanes * kStagesPerLane;
-constexpr int kSfbPerLane = 6;                  // TMEM scale-factor buffers for B per lane
+// TMEM scale-factor buffers for B per lane.  They need no barrier of their
+// own: a lane's MMA warp copies page j+1's scales only after the epilogue has
+// released the accumulator of page j, i.e. after page j's MMAs (and all
+// earlier ones of the lane, the readers of the buffer being overwritten)
+// completed.
+constexpr int kSfbPerLane = 2;
 constexpr int kSfbBufs = kLanes * kSfbPerLane;
 constexpr int kDBufs = kLanes;                  // one TMEM accumulator per lane
 constexpr int kChunk = 8;                       // pages per work unit
-// Warp roles: warps 0-3 and 4-7 are the epilogue warpgroups of lanes 0 and 1
-// (warp w reads TMEM lane quadrant w % 4; lane 0's group also loads the query
-// tiles), warps 8-9 the TMA producers, warps 10-11 the MMA warps (each copies
-// its pages' scales into TMEM right before their MMAs; warp 10 owns the TMEM
-// allocation).
+// Warp roles: warps 4l .. 4l+3 are the epilogue warpgroup of lane l (warp w
+// reads TMEM lane quadrant w % 4; lane 0's group also loads the query tiles),
+// then one lane warp per lane that issues both the lane's TMA page loads and
+// its MMAs (the first lane warp owns the TMEM allocation).
 constexpr int kEpiSets = kLanes;
-constexpr int kProdWarps = kLanes;
 constexpr int kMmaWarps = kLanes;
-constexpr int kProdWarp0 = 4 * kEpiSets;                 // 8
-constexpr int kMmaWarp0 = kProdWarp0 + kProdWarps;       // 10
-constexpr int kThreads = 32 * (kMmaWarp0 + kMmaWarps);
+constexpr int kLaneWarp0 = 4 * kEpiSets;                 // 12
+constexpr int kThreads = 32 * (kLaneWarp0 + kMmaWarps);  // 15 warps: at most 4 per SM sub-partition
+constexpr int kLookahead = kStagesPerLane - 1;           // TMA pages in flight ahead of the MMA stream
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D[lanes] x 128 | A (query tile, e4m3) [2] x 32 | SFA[lanes] x 4 | SFB[lanes x 6] x 4
+// TMEM columns: D[lanes] x 128 | A (query tile, e4m3) [2] x 32 | SFA[lanes] x 4 | SFB[lanes x 2] x 4
 constexpr uint32_t kTmemACol = kDBufs * 128;
 constexpr uint32_t kTmemSfaCol = kTmemACol + 2 * 32;
 constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4 * kMmaWarps;
@@ -127,9 +133,9 @@ struct SmemLayout {
     static constexpr uint32_t kSfa = kScale + kStages * kScaleBytes;       // 512 B of 0x7F
     static constexpr uint32_t kOut = kSfa + kScaleBytes;                   // lanes x 128 x kChunk floats
     static constexpr uint32_t kBars = kOut + kLanes * 128 * kChunk * 4;
-    // barriers: full[kStages], empty[kStages], sfempty[kSfbBufs], dfull[kDBufs],
+    // barriers: full[kStages], empty[kStages], dfull[kDBufs],
     //           dempty[kDBufs], qfull[2], qempty[2], final[kMmaWarps]
-    static constexpr uint32_t kNumBars = 2 * kStages + kSfbBufs + 2 * kDBufs + 4 + kMmaWarps;
+    static constexpr uint32_t kNumBars = 2 * kStages + 2 * kDBufs + 4 + kMmaWarps;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -204,7 +210,6 @@ enum WaitSite : uint32_t {
     kSiteMmaDEmpty = 3,
     kSiteEpiQEmpty = 4,
     kSiteEpiDFull = 5,
-    kSiteMmaScaleEmpty = 6,
 };
 
 // Bounded wait: true when the phase completed; false after the time limit or
@@ -315,6 +320,18 @@ __device__ __forceinline__ void ring_next(Ring &r)
     }
 }
 
+// Whose turn a unit is: the units of tiles with query rows go to the lanes
+// in rotation.
+struct LaneTurn {
+    int next = 0;
+    __device__ __forceinline__ bool take(int me)
+    {
+        const bool mine = next == me;
+        next = next + 1 == kLanes ? 0 : next + 1;
+        return mine;
+    }
+};
+
 // MMA column n holds token 4*(n%32) + n/32.
 __device__ __forceinline__ int token_of_col(int n) { return ((n & 31) << 2) | (n >> 5); }
 
@@ -330,18 +347,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
 
     // Every role walks the same units in the same order; the units of tiles
-    // with query rows alternate between the two lanes.  Lane l's page stages
+    // with query rows go to the lanes in rotation.  Lane l's page stages
     // are l*kStagesPerLane.., its scale buffers l*kSfbPerLane.., its
     // accumulator l.
     auto bar = [&](int i) { return sbase + SmemLayout::kBars + 8u * i; };
     auto full_bar = [&](int i) { return bar(i); };
     auto empty_bar = [&](int i) { return bar(kStages + i); };
-    auto sfempty_bar = [&](int i) { return bar(2 * kStages + i); };
-    auto dfull_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + i); };
-    auto dempty_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + kDBufs + i); };
-    auto qfull_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + 2 * kDBufs + i); };
-    auto qempty_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + 2 * kDBufs + 2 + i); };
-    auto final_bar = [&](int i) { return bar(2 * kStages + kSfbBufs + 2 * kDBufs + 4 + i); };
+    auto dfull_bar = [&](int i) { return bar(2 * kStages + i); };
+    auto dempty_bar = [&](int i) { return bar(2 * kStages + kDBufs + i); };
+    auto qfull_bar = [&](int i) { return bar(2 * kStages + 2 * kDBufs + i); };
+    auto qempty_bar = [&](int i) { return bar(2 * kStages + 2 * kDBufs + 2 + i); };
+    auto final_bar = [&](int i) { return bar(2 * kStages + 2 * kDBufs + 4 + i); };
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + SmemLayout::kAbort);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SmemLayout::kTmemSlot);
 
@@ -350,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full_bar(i), 1);
             mbar_init(empty_bar(i), 1);
         }
-        for (int i = 0; i < kSfbBufs; ++i) mbar_init(sfempty_bar(i), 1);
         for (int i = 0; i < kDBufs; ++i) {
             mbar_init(dfull_bar(i), 1);
             mbar_init(dempty_bar(i), 4);
@@ -368,11 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<uint32_t *>(smem + SmemLayout::kSfa)[threadIdx.x] = 0x7F7F7F7Fu;
         fence_proxy_async_smem();
     }
-    if (warp == kProdWarp0 && lane == 0) {
+    if (warp == kLaneWarp0 && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_s);
     }
-    if (warp == kMmaWarp0) {
+    if (warp == kLaneWarp0) {
         tmem_alloc(sbase + SmemLayout::kTmemSlot, kTmemCols);
         tmem_relinquish();
     }
@@ -384,26 +399,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * p.num_units / gridDim.x;
     const int64_t u_end = static_cast<int64_t>(blockIdx.x + 1) * p.num_units / gridDim.x;
 
-    if (warp >= kProdWarp0 && warp < kMmaWarp0) {
-        // ------------------------------------------------------ producers --
-        // Producer pw walks its lane's units; lane i of the warp fetches the
-        // page id of the unit's i-th live page one unit ahead (so the
-        // block-table latency overlaps the current unit's copies), one elected
-        // lane issues the TMA loads.
-        const int pw = warp - kProdWarp0;
+    if (warp >= kLaneWarp0) {
+        // -------------------------------------------- lane warps (TMA + MMA) --
+        // Lane warp ln runs its lane's two page streams.  The TMA stream looks
+        // up each page id in the block table (lane i of the warp holds the id
+        // of the unit's i-th page, fetched one unit ahead so the lookup latency
+        // overlaps the copies) and issues two TMA loads into the lane's smem
+        // stage ring, kLookahead pages ahead of the MMA stream.  The MMA stream
+        // copies the page's scales into a TMEM scale buffer (tcgen05.cp), issues
+        // 4 block-scaled MMAs (K = 32 each) into the lane's accumulator and one
+        // commit.  The tcgen05 operations of one thread run in issue order, so
+        // the MMAs see the copied scales without a commit/wait in between.
+        // Each page's TMA loads are issued right after the MMAs of the page
+        // before it, into the stage that page's predecessor used: by then the
+        // epilogue has read that predecessor's accumulator, so the stage is
+        // free or about to be, and the copy stays off the MMA -> epilogue ->
+        // MMA chain.
+        const int ln = warp - kLaneWarp0;
         const uint64_t policy = kDecode ? l2_policy_evict_first() : l2_policy_evict_last();
-        Ring st;
-        TileInfo ti;
-        ti.tile = -1;
+
         // next unit of this lane at or after c with live pages: tile info, first
-        // page, page count; uc counts the units with rows (it picks the lane)
-        auto next_unit = [&](UnitCursor &c, TileInfo &t, int64_t &uc, int &j0, int &n) -> bool {
+        // page, page count; t rotates over the units with rows (it picks the lane)
+        auto next_unit = [&](UnitCursor &c, TileInfo &t, LaneTurn &turn, int &j0, int &n) -> bool {
             for (; c.left > 0; cursor_next(p, c)) {
                 if (c.tile != t.tile) t = tile_info<kDecode>(p, c.tile);
                 if (t.nrows <= 0) continue;
-                const bool mine = (uc & 1) == pw;
-                ++uc;
-                if (!mine) continue;
+                if (!turn.take(ln)) continue;
                 j0 = c.chunk * kChunk;
                 const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
                 const int jc = j1 < t.live_end ? j1 : t.live_end;
@@ -412,150 +433,187 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return false;
         };
-        auto fetch_id = [&](const TileInfo &t, int j0, int n) -> int64_t {
-            return lane < n ? static_cast<int64_t>(p.block_table[static_cast<int64_t>(t.b) * p.bt_stride + j0 + lane])
-                            : 0;
+        // Start the load of the ids of pages j0 .. j0+n-1 (n >= 1) of tile t's
+        // request into lane i's `raw`.  Lanes past n re-read the last id, so the
+        // load is unconditional: nothing here consumes the value and the warp
+        // does not wait for it.
+        auto fetch_id = [&](const TileInfo &t, int j0, int n, int &raw) {
+            raw = p.block_table[static_cast<int64_t>(t.b) * p.bt_stride + j0 + (lane < n ? lane : n - 1)];
         };
-        UnitCursor cur = cursor_begin(p, u_begin, u_end);
-        int64_t uc = 0;
-        int j0 = 0, n = 0;
-        bool have = next_unit(cur, ti, uc, j0, n);
-        int64_t raw = have ? fetch_id(ti, j0, n) : 0;
-        while (have) {
-            UnitCursor c2 = cur;
-            cursor_next(p, c2);
-            TileInfo ti2 = ti;
-            int64_t uc2 = uc;
-            int j02 = 0, n2 = 0;
-            const bool have2 = next_unit(c2, ti2, uc2, j02, n2);
-            const int64_t raw2 = have2 ? fetch_id(ti2, j02, n2) : 0;
+        // First use of a fetched id (one unit later): range check.
+        auto checked_id = [&](int raw, int n) -> int {
             int pid = 0;
             if (lane < n) {
                 if (raw < 0 || raw >= p.num_pool_pages)
                     atomicOr(&g_mx4_device_status, 0x1u);
                 else
-                    pid = static_cast<int>(raw);
+                    pid = raw;
             }
-            bool go = true;
-            for (int i = 0; i < n; ++i) {
-                const int id = __shfl_sync(0xffffffffu, pid, i);
-                const int stage = pw * kStagesPerLane + st.idx;
-                go = __all_sync(0xffffffffu, wait_bounded(empty_bar(stage), st.ph ^ 1u, abort_flag,
-                                                          kSiteProducerEmpty));
-                if (!go) break;
-                if (elect_one()) {
-                    mbar_arrive_expect_tx(full_bar(stage), kStageTxBytes);
-                    tma_load_4d(sbase + SmemLayout::kData + stage * kTileBytes, &tmap_k, full_bar(stage), 0, 0, 0,
-                                id, policy);
-                    tma_load_2d(sbase + SmemLayout::kScale + stage * kScaleBytes, &tmap_s, full_bar(stage), 0, id,
-                                policy);
-                }
-                __syncwarp();
-                ring_next<kStagesPerLane>(st);
+            return pid;
+        };
+
+        // TMA stream state: current unit (cursor, tile, turn, pages) and the
+        // prefetched next one
+        UnitCursor tc_cur = cursor_begin(p, u_begin, u_end);
+        TileInfo tc_ti;
+        tc_ti.tile = -1;
+        LaneTurn tc_turn;
+        int tc_j0 = 0, tc_n = 0, tc_i = 0;
+        bool tc_have = next_unit(tc_cur, tc_ti, tc_turn, tc_j0, tc_n);
+        int tc_raw = 0;
+        if (tc_have) fetch_id(tc_ti, tc_j0, tc_n, tc_raw);
+        int tc_pid = checked_id(tc_raw, tc_n);
+        UnitCursor nx_cur = tc_cur;
+        TileInfo nx_ti = tc_ti;
+        LaneTurn nx_turn = tc_turn;
+        int nx_j0 = 0, nx_n = 0;
+        bool nx_have = false;
+        int nx_raw = 0;
+        auto prefetch_next = [&]() {
+            nx_cur = tc_cur;
+            cursor_next(p, nx_cur);
+            nx_ti = tc_ti;
+            nx_turn = tc_turn;
+            nx_have = next_unit(nx_cur, nx_ti, nx_turn, nx_j0, nx_n);
+            if (nx_have) fetch_id(nx_ti, nx_j0, nx_n, nx_raw);
+        };
+        if (tc_have) prefetch_next();
+        Ring pst;
+        // issue the TMA stream's next page (if any); false on abort
+        // Issue the TMA stream's next page into its stage, which the caller
+        // has seen free, and advance the stream.
+        auto issue_page = [&]() {
+            const int id = __shfl_sync(0xffffffffu, tc_pid, tc_i);
+            const int stage = ln * kStagesPerLane + pst.idx;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(full_bar(stage), kStageTxBytes);
+                tma_load_4d(sbase + SmemLayout::kData + stage * kTileBytes, &tmap_k, full_bar(stage), 0, 0, 0, id,
+                            policy);
+                tma_load_2d(sbase + SmemLayout::kScale + stage * kScaleBytes, &tmap_s, full_bar(stage), 0, id,
+                            policy);
             }
-            if (!go) break;
-            cur = c2;
-            ti = ti2;
-            uc = uc2;
-            j0 = j02;
-            n = n2;
-            raw = raw2;
-            have = have2;
-        }
-        if (lane == 0) {
-            // Do not leave while copies into this CTA's smem may be in flight:
-            // every armed stage of this lane completes (bounded) before the CTA exits.
-            for (int i = 0; i < kStagesPerLane; ++i) {
-                // stages before st.idx were armed in phase ph, the others in ph^1 (if ever)
-                const uint32_t par = (i < st.idx) ? st.ph : (st.ph ^ 1u);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(full_bar(pw * kStagesPerLane + i), par) &&
-                       globaltimer_ns() - t0 < 2000000ull) {
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp >= kMmaWarp0) {
-        // ------------------------------------------------------ MMA warps --
-        // MMA warp i issues its lane's pages: the page's scales into a TMEM
-        // scale buffer (tcgen05.cp), then 4 block-scaled MMAs (K = 32 each)
-        // into the lane's accumulator, then one commit.  The tcgen05 operations
-        // of one thread run in issue order, so the MMAs see the copied scales
-        // without a commit/wait in between.
-        const int issuer = warp - kMmaWarp0;
-        {
-            // this warp's copy of the unit scale of A (e8m0 127 everywhere)
-            const uint32_t tmem_sfa = tmem_base + kTmemSfaCol + 4u * issuer;
-            if (elect_one()) tc_cp_32x128b_warpx4(tmem_sfa, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
             __syncwarp();
-            const uint64_t bdesc0 = smem_desc(sbase + SmemLayout::kData, 16, 1024, 2);
-            const uint64_t sdesc0 = smem_desc(sbase + SmemLayout::kScale, 16, 128, 0);
-            const uint32_t d_tmem = tmem_base + issuer * 128u;
-            Ring st, sf, dr;
-            int64_t qcount = 0, uc = 0;
-            uint32_t a_tmem = tmem_base + kTmemACol;
-            TileInfo ti;
-            ti.tile = -1;
-            bool ok = true, holding_q = false;
-            for (UnitCursor c = cursor_begin(p, u_begin, u_end); c.left > 0 && ok; cursor_next(p, c)) {
-                if (c.tile != ti.tile) {
-                    ti = tile_info<kDecode>(p, c.tile);
-                    if (ti.nrows > 0) {
-                        // the previous query tile's buffer is free once its MMAs retire
-                        if (holding_q && elect_one()) tc_commit(qempty_bar(static_cast<int>((qcount - 1) & 1)));
-                        __syncwarp();
-                        const int64_t qi = qcount++;
-                        a_tmem = tmem_base + kTmemACol + static_cast<uint32_t>(qi & 1) * 32u;
-                        holding_q = true;
-                        if (!__all_sync(0xffffffffu, wait_bounded(qfull_bar(static_cast<int>(qi & 1)),
-                                                                  static_cast<uint32_t>((qi >> 1) & 1), abort_flag,
-                                                                  kSiteMmaQFull)))
-                            break;
-                        tc_fence_after();
-                    }
-                }
-                if (ti.nrows <= 0) continue;
-                const bool mine = (uc & 1) == issuer;
-                ++uc;
-                if (!mine) continue;
-                const int j0 = c.chunk * kChunk;
-                const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
-                const int jc = j1 < ti.live_end ? j1 : ti.live_end;
-                for (int j = j0; j < jc; ++j) {
-                    const int stage = issuer * kStagesPerLane + st.idx;
-                    const int sfb = issuer * kSfbPerLane + sf.idx;
-                    if (!__all_sync(0xffffffffu,
-                                    wait_bounded(full_bar(stage), st.ph, abort_flag, kSiteMmaFull) &&
-                                        wait_bounded(sfempty_bar(sfb), sf.ph ^ 1u, abort_flag, kSiteMmaScaleEmpty) &&
-                                        wait_bounded(dempty_bar(issuer), dr.ph ^ 1u, abort_flag, kSiteMmaDEmpty))) {
+            ring_next<kStagesPerLane>(pst);
+            if (++tc_i == tc_n) {
+                tc_cur = nx_cur;
+                tc_ti = nx_ti;
+                tc_turn = nx_turn;
+                tc_j0 = nx_j0;
+                tc_n = nx_n;
+                tc_have = nx_have;
+                tc_i = 0;
+                tc_pid = checked_id(nx_raw, tc_n);
+                if (tc_have) prefetch_next();
+            }
+        };
+        // Wait (bounded) for the next page's stage, then issue it; false on abort.
+        auto issue_next_page = [&]() -> bool {
+            if (!tc_have) return true;
+            if (!__all_sync(0xffffffffu, wait_bounded(empty_bar(ln * kStagesPerLane + pst.idx), pst.ph ^ 1u,
+                                                      abort_flag, kSiteProducerEmpty)))
+                return false;
+            issue_page();
+            return true;
+        };
+
+        // this warp's copy of the unit scale of A (e8m0 127 everywhere)
+        const uint32_t tmem_sfa = tmem_base + kTmemSfaCol + 4u * ln;
+        if (elect_one()) tc_cp_32x128b_warpx4(tmem_sfa, smem_desc(sbase + SmemLayout::kSfa, 16, 128, 0));
+        __syncwarp();
+        const uint64_t bdesc0 = smem_desc(sbase + SmemLayout::kData, 16, 1024, 2);
+        const uint64_t sdesc0 = smem_desc(sbase + SmemLayout::kScale, 16, 128, 0);
+        const uint32_t d_tmem = tmem_base + ln * 128u;
+        bool ok = true;
+        for (int i = 0; i < kLookahead && ok; ++i) ok = issue_next_page();
+        Ring st, sf, dr;
+        int64_t qcount = 0;
+        LaneTurn uc;
+        uint32_t a_tmem = tmem_base + kTmemACol;
+        TileInfo ti;
+        ti.tile = -1;
+        bool holding_q = false;
+        for (UnitCursor c = cursor_begin(p, u_begin, u_end); c.left > 0 && ok; cursor_next(p, c)) {
+            if (c.tile != ti.tile) {
+                ti = tile_info<kDecode>(p, c.tile);
+                if (ti.nrows > 0) {
+                    // the previous query tile's buffer is free once its MMAs retire
+                    if (holding_q && elect_one()) tc_commit(qempty_bar(static_cast<int>((qcount - 1) & 1)));
+                    __syncwarp();
+                    const int64_t qi = qcount++;
+                    a_tmem = tmem_base + kTmemACol + static_cast<uint32_t>(qi & 1) * 32u;
+                    holding_q = true;
+                    if (!__all_sync(0xffffffffu, wait_bounded(qfull_bar(static_cast<int>(qi & 1)),
+                                                              static_cast<uint32_t>((qi >> 1) & 1), abort_flag,
+                                                              kSiteMmaQFull))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (elect_one()) {
-                        const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sfb;
-                        // descriptor start addresses count 16-byte units
-                        tc_cp_32x128b_warpx4(tmem_sfb, sdesc0 + static_cast<uint64_t>(stage * (kScaleBytes >> 4)));
-                        const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
-                        // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
-                        tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
-                        tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k(1), tmem_sfa, tmem_sfb, 1u);
-                        tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k(2), tmem_sfa, tmem_sfb, 1u);
-                        tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k(3), tmem_sfa, tmem_sfb, 1u);
-                        tc_commit(dfull_bar(issuer));
-                    }
-                    __syncwarp();
-                    ring_next<kStagesPerLane>(st);
-                    ring_next<kSfbPerLane>(sf);
-                    ring_next<1>(dr);
                 }
             }
-            // all MMAs retire before TMEM is released
-            if (elect_one()) tc_commit(final_bar(issuer));
-            __syncwarp();
-            const uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(final_bar(issuer), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            if (ti.nrows <= 0) continue;
+            if (!uc.take(ln)) continue;
+            const int j0 = c.chunk * kChunk;
+            const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
+            const int jc = j1 < ti.live_end ? j1 : ti.live_end;
+            for (int j = j0; j < jc; ++j) {
+                const int stage = ln * kStagesPerLane + st.idx;
+                const int sfb = ln * kSfbPerLane + sf.idx;
+                // The page's bytes, a free accumulator and, when the TMA stream
+                // has a page left, a free stage for it (released when the MMAs
+                // of the page before this one completed): one probe round trip
+                // when all are ready, bounded waits otherwise.
+                const bool tma_next = tc_have;
+                const uint32_t e_bar = empty_bar(ln * kStagesPerLane + pst.idx);
+                const uint32_t e_par = pst.ph ^ 1u;
+                const bool ready = tma_next ? mbar_try_wait3(full_bar(stage), st.ph, dempty_bar(ln), dr.ph ^ 1u,
+                                                             e_bar, e_par)
+                                            : mbar_try_wait2(full_bar(stage), st.ph, dempty_bar(ln), dr.ph ^ 1u);
+                if (!__all_sync(0xffffffffu, ready) &&
+                    !__all_sync(0xffffffffu,
+                                wait_bounded(full_bar(stage), st.ph, abort_flag, kSiteMmaFull) &&
+                                    wait_bounded(dempty_bar(ln), dr.ph ^ 1u, abort_flag, kSiteMmaDEmpty) &&
+                                    (!tma_next || wait_bounded(e_bar, e_par, abort_flag, kSiteProducerEmpty)))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (elect_one()) {
+                    const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sfb;
+                    // descriptor start addresses count 16-byte units
+                    tc_cp_32x128b_warpx4(tmem_sfb, sdesc0 + static_cast<uint64_t>(stage * (kScaleBytes >> 4)));
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
+                    // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
+                    tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
+                    tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k(1), tmem_sfa, tmem_sfb, 1u);
+                    tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k(2), tmem_sfa, tmem_sfb, 1u);
+                    tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k(3), tmem_sfa, tmem_sfb, 1u);
+                    tc_commit(dfull_bar(ln));
+                }
+                __syncwarp();
+                ring_next<kStagesPerLane>(st);
+                ring_next<kSfbPerLane>(sf);
+                ring_next<1>(dr);
+                if (tma_next) issue_page();
             }
+        }
+        // Do not leave while copies into this CTA's smem may be in flight:
+        // every armed stage of this lane completes (bounded) before the CTA
+        // exits; then all MMAs retire before TMEM is released.
+        if (lane == 0) {
+            for (int i = 0; i < kStagesPerLane; ++i) {
+                // stages before pst.idx were armed in phase ph, the others in ph^1 (if ever)
+                const uint32_t par = (i < pst.idx) ? pst.ph : (pst.ph ^ 1u);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(full_bar(ln * kStagesPerLane + i), par) && globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+        if (elect_one()) tc_commit(final_bar(ln));
+        __syncwarp();
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(final_bar(ln), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
         }
         __syncwarp();
     } else {
@@ -572,8 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *stg = reinterpret_cast<float *>(smem + SmemLayout::kOut) + (set * 128 + m) * kChunk;
         const float sm_scale = p.sm_scale;
         Ring dr;
-        int st_idx = 0, sf_idx = 0;
-        int64_t qcount = 0, uc = 0;
+        int st_idx = 0;
+        int64_t qcount = 0;
+        LaneTurn uc;
         TileInfo ti;
         ti.tile = -1;
 
@@ -611,9 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            const bool mine = (uc & 1) == set;
-            ++uc;
-            if (!mine) continue;
+            if (!uc.take(set)) continue;
             const int j0 = c.chunk * kChunk;
             const int j1 = j0 + kChunk < p.num_out_pages ? j0 + kChunk : p.num_out_pages;
             const bool has_row = ri < ti.nrows;     // uniform per warp
@@ -628,45 +685,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // the page's MMAs have completed, so its smem stage can be
+                    // refilled at once
+                    if (quad == 0 && lane == 0) mbar_arrive(empty_bar(set * kStagesPerLane + st_idx));
+                    if (++st_idx == kStagesPerLane) st_idx = 0;
                     if (has_row) {
-                        uint32_t v[128];
+                        // the accumulator is read in two 64-column halves (15
+                        // warps per CTA leave 128 registers per thread)
+                        uint32_t v[64];
                         if (!kLogits) {
                             float mx;
                             if (lim >= kPage) {
-                                mx = tmem_ld_max_32x32b_x128(d_taddr, v);
+                                // a rolled loop: the two loads reuse one set of
+                                // destination registers
+                                mx = -INFINITY;
+#pragma unroll 1
+                                for (int hh = 0; hh < 2; ++hh)
+                                    mx = fmaxf(mx, tmem_ld_max_32x32b_x64(d_taddr + 64u * hh, v));
                             } else {
-                                tmem_ld_32x32b_x128(d_taddr, v);
                                 mx = -INFINITY;
 #pragma unroll
-                                for (int n = 0; n < 128; ++n)
-                                    if (token_of_col(n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
+                                for (int hh = 0; hh < 2; ++hh) {
+                                    tmem_ld_32x32b_x64(d_taddr + 64u * hh, v);
+#pragma unroll
+                                    for (int n = 0; n < 64; ++n)
+                                        if (token_of_col(64 * hh + n) < lim) mx = fmaxf(mx, __uint_as_float(v[n]));
+                                }
                             }
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(dempty_bar(set));
                             stg[j - j0] = mx * sm_scale;
                         } else {
-                            tmem_ld_32x32b_x128(d_taddr, v);
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(dempty_bar(set));
                             float *dst = row_out + static_cast<int64_t>(j) * kPage;
                             const int valid = p.max_seq_len - j * kPage;   // columns that exist
-                            const bool vec = (p.out_row_stride & 3) == 0 && valid >= kPage;
+                            const bool vec = (p.out_row_stride & 1) == 0 && valid >= kPage;
 #pragma unroll
-                            for (int g = 0; g < 32; ++g) {
-                                float4 o;
-                                o.x = (4 * g + 0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
-                                o.y = (4 * g + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
-                                o.z = (4 * g + 2 < lim) ? __uint_as_float(v[g + 64]) * sm_scale : -INFINITY;
-                                o.w = (4 * g + 3 < lim) ? __uint_as_float(v[g + 96]) * sm_scale : -INFINITY;
-                                if (vec) {
-                                    __stcs(reinterpret_cast<float4 *>(dst + 4 * g), o);
-                                } else {
-                                    if (4 * g + 0 < valid) dst[4 * g + 0] = o.x;
-                                    if (4 * g + 1 < valid) dst[4 * g + 1] = o.y;
-                                    if (4 * g + 2 < valid) dst[4 * g + 2] = o.z;
-                                    if (4 * g + 3 < valid) dst[4 * g + 3] = o.w;
+                            for (int hh = 0; hh < 2; ++hh) {
+                                tmem_ld_32x32b_x64(d_taddr + 64u * hh, v);
+                                if (hh == 1) {
+                                    tc_fence_before();
+                                    __syncwarp();
+                                    if (lane == 0) mbar_arrive(dempty_bar(set));
+                                }
+                                // column 64hh + g holds token 4g + 2hh, column
+                                // 64hh + 32 + g token 4g + 2hh + 1
+#pragma unroll
+                                for (int g = 0; g < 32; ++g) {
+                                    const int t0 = 4 * g + 2 * hh;
+                                    float2 o;
+                                    o.x = (t0 < lim) ? __uint_as_float(v[g]) * sm_scale : -INFINITY;
+                                    o.y = (t0 + 1 < lim) ? __uint_as_float(v[g + 32]) * sm_scale : -INFINITY;
+                                    if (vec) {
+                                        __stcs(reinterpret_cast<float2 *>(dst + t0), o);
+                                    } else {
+                                        if (t0 < valid) dst[t0] = o.x;
+                                        if (t0 + 1 < valid) dst[t0 + 1] = o.y;
+                                    }
                                 }
                             }
                         }
@@ -675,14 +750,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(dempty_bar(set));
                     }
-                    // the page's MMAs have retired, so its smem stage and
-                    // scale buffer can be refilled
-                    if (quad == 0 && lane == 0) {
-                        mbar_arrive(empty_bar(set * kStagesPerLane + st_idx));
-                        mbar_arrive(sfempty_bar(set * kSfbPerLane + sf_idx));
-                    }
-                    if (++st_idx == kStagesPerLane) st_idx = 0;
-                    if (++sf_idx == kSfbPerLane) sf_idx = 0;
                     ring_next<1>(dr);
                 } else if (has_row) {
                     // no row of the tile sees this page: nothing was computed
@@ -717,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp0) {
+    if (warp == kLaneWarp0) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }

@@ -71,6 +71,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Probe two mbarrier phases with both probes in flight together (one
+// round trip instead of two); true when both phases have completed.
+__device__ __forceinline__ bool mbar_try_wait2(uint32_t bar0, uint32_t parity0, uint32_t bar1, uint32_t parity1)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p0, p1;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p1, [%3], %4;\n\t"
+        "and.pred p0, p0, p1;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\t}"
+        : "=r"(ok)
+        : "r"(bar0), "r"(parity0), "r"(bar1), "r"(parity1)
+        : "memory");
+    return ok != 0;
+}
+
+// Three phases at once, as above.
+__device__ __forceinline__ bool mbar_try_wait3(uint32_t bar0, uint32_t parity0, uint32_t bar1, uint32_t parity1,
+                                               uint32_t bar2, uint32_t parity2)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, p2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p1, [%3], %4;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p2, [%5], %6;\n\t"
+        "and.pred p0, p0, p1;\n\t"
+        "and.pred p0, p0, p2;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\t}"
+        : "=r"(ok)
+        : "r"(bar0), "r"(parity0), "r"(bar1), "r"(parity1), "r"(bar2), "r"(parity2)
+        : "memory");
+    return ok != 0;
+}
+
 // Proxy fence: generic-proxy smem writes become visible to the async proxy
 // (TMA engine, tensor core operand reads, tcgen05.cp).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -294,6 +330,56 @@ __device__ __forceinline__ void tmem_ld_32x32b_x128(uint32_t taddr, uint32_t (&v
           "=r"(v[110]), "=r"(v[111]), "=r"(v[112]), "=r"(v[113]), "=r"(v[114]), "=r"(v[115]),
           "=r"(v[116]), "=r"(v[117]), "=r"(v[118]), "=r"(v[119]), "=r"(v[120]), "=r"(v[121]),
           "=r"(v[122]), "=r"(v[123]), "=r"(v[124]), "=r"(v[125]), "=r"(v[126]), "=r"(v[127])
+        : "r"(taddr)
+        : "memory");
+}
+
+// 64-column forms of the two loads above (half the destination registers).
+__device__ __forceinline__ float tmem_ld_max_32x32b_x64(uint32_t taddr, uint32_t (&v)[64])
+{
+    float mx;
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x64.max.f32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, "
+        "%64, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]),
+          "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]),
+          "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]),
+          "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]),
+          "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63]),
+          "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+    return mx;
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&v)[64])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+        "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, "
+        "[%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]),
+          "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]),
+          "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]), "=r"(v[49]),
+          "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]), "=r"(v[56]),
+          "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
         : "r"(taddr)
         : "memory");
 }

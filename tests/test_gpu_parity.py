@@ -110,6 +110,15 @@ def test_prefill_ragged_batch():
     _check(w)
 
 
+@pytest.mark.parametrize("rows", [8, 24, 40, 300])
+def test_prefill_mid_sizes(rows):
+    """One request, rows/2 row-pair tiles x 32 pages: from fewer units than
+    SMs (every CTA a single unit, most lanes idle) to several units per CTA."""
+    w = W.make_workload(f"mid{rows}", seed=28, q_lens=[rows], seq_lens=[4096], prefix_lens=[4096 - rows],
+                        pool_pages=40)
+    _check(w)
+
+
 def test_prefill_e4m3_q_wide_scales_split_views():
     w = W.make_workload("e4m3", seed=22, q_lens=[9, 16], seq_lens=[700, 2000], pool_pages=40, q_e4m3=True,
                         scale_lo=100, scale_hi=150, layout="split", k_data_page_stride=8192 + 64,
