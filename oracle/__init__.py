@@ -90,6 +90,14 @@ def _load():
         lib.orc_write_index_k.argtypes = [
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+        lib.orc_score_fp8.restype = ctypes.c_int
+        lib.orc_score_fp8.argtypes = [
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int64,
+            c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.orc_live_pairs.restype = ctypes.c_int64
         lib.orc_live_pairs.argtypes = [
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -194,6 +202,43 @@ def score(*, decode: bool, q: np.ndarray, q_is_e4m3: bool, k_data: np.ndarray,
     st = lib.orc_score(
         1 if decode else 0, _ptr(q), 1 if q_is_e4m3 else 0, 1 if unquantized else 0,
         _ptr(k_data), _ptr(k_scale), int(k_data_page_stride), int(k_scale_page_stride),
+        _ptr(bt), int(block_table_stride), _ptr(cu), _ptr(sl), _ptr(pl),
+        num_seqs, int(max_seq_len), float(sm_scale), int(num_pool_pages),
+        rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,
+        _ptr(sc), _ptr(lg), int(num_threads))
+    if st != 0:
+        raise ValueError(f"oracle rejected the inputs (status {st})")
+    return sc, lg
+
+
+def score_fp8(*, decode: bool, q: np.ndarray, q_is_e4m3: bool, k_fp8: np.ndarray, k_page_stride: int,
+              block_table: np.ndarray, block_table_stride: int, seq_lens, max_seq_len: int,
+              sm_scale: float, cu_seqlens_q=None, prefix_lens=None, rows=None,
+              want_scores: bool = True, want_logits: bool = False, num_pool_pages: int = 0,
+              num_threads: int = 0):
+    """The scorer over an fp8 index cache (the format the MXFP4 cache
+    replaces): page p's token i holds 128 e4m3 bytes at
+    ``k_fp8[p * k_page_stride + i * 128 :]``, no scale.  Otherwise as
+    ``score``."""
+    lib = _load()
+    q = np.ascontiguousarray(q)
+    assert q.dtype == (np.uint8 if q_is_e4m3 else np.uint16)
+    k = _u8(k_fp8).reshape(-1)
+    bt = _i32(block_table).reshape(-1)
+    sl = _i32(seq_lens)
+    cu = _i32(cu_seqlens_q)
+    pl = _i32(prefix_lens)
+    num_seqs = int(sl.shape[0])
+    if rows is None:
+        n_total = num_seqs if decode else int(cu[-1])
+        rows = np.arange(n_total, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    P = (max_seq_len + PAGE - 1) // PAGE
+    sc = np.empty((n, HEADS, P), dtype=np.float64) if want_scores else None
+    lg = np.empty((n, HEADS, max_seq_len), dtype=np.float64) if want_logits else None
+    st = lib.orc_score_fp8(
+        1 if decode else 0, _ptr(q), 1 if q_is_e4m3 else 0, 0, _ptr(k), int(k_page_stride),
         _ptr(bt), int(block_table_stride), _ptr(cu), _ptr(sl), _ptr(pl),
         num_seqs, int(max_seq_len), float(sm_scale), int(num_pool_pages),
         rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n,

@@ -171,6 +171,16 @@ static double orc_k_value(const uint8_t *k_data, const uint8_t *k_scale,
     return orc_e2m1_value(code) * orc_e8m0_value(sbyte);
 }
 
+/* fp8 index cache (the format the MXFP4 cache replaces; aiter #7061, summary:
+ * 128 B per token for fp8 against 68 B for MXFP4, and "Format": MXFP4 values
+ * dequantised to e4m3 are exact for scale bytes 119..133).  READING: a page
+ * of 128 tokens x 128 e4m3 bytes, token i at byte i*128, element d at byte d,
+ * no scale; pages `sd` bytes apart. */
+static double orc_k_value_fp8(const uint8_t *k, int64_t sd, int64_t p, int i, int d)
+{
+    return orc_e4m3_value(k[p * sd + (int64_t)i * ORC_DIM + d]);
+}
+
 /* Query value of (row, head, d).  mode 0: the e4m3 value the scorer uses
  * (bf16 rounded to e4m3, or the stored e4m3 byte).  mode 1: the unrounded
  * bf16 value, used only for the cosine context figure. */
@@ -223,20 +233,20 @@ int64_t orc_live_limit(int decode, const int32_t *cu, const int32_t *seq_lens,
  * Returns 0, or -1 if a row is not in any request, -2 if a live token maps
  * to a page id outside [0, num_pool_pages), -3 on a bad argument.
  */
-int orc_score(int decode, const void *q, int q_is_e4m3, int unquantized,
-              const uint8_t *k_data, const uint8_t *k_scale,
-              int64_t k_data_page_stride, int64_t k_scale_page_stride,
-              const int32_t *block_table, int64_t block_table_stride,
-              const int32_t *cu_seqlens_q, const int32_t *seq_lens,
-              const int32_t *prefix_lens, int num_seqs, int max_seq_len,
-              double sm_scale, int64_t num_pool_pages,
-              const int64_t *rows, int64_t n_rows,
-              double *scores, double *logits, int num_threads)
+static int orc_score_impl(int decode, const void *q, int q_is_e4m3, int unquantized, int k_fp8,
+                          const uint8_t *k_data, const uint8_t *k_scale,
+                          int64_t k_data_page_stride, int64_t k_scale_page_stride,
+                          const int32_t *block_table, int64_t block_table_stride,
+                          const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                          const int32_t *prefix_lens, int num_seqs, int max_seq_len,
+                          double sm_scale, int64_t num_pool_pages,
+                          const int64_t *rows, int64_t n_rows,
+                          double *scores, double *logits, int num_threads)
 {
     const int64_t P = ((int64_t)max_seq_len + ORC_PAGE - 1) / ORC_PAGE;
     int status = 0;
 
-    if (max_seq_len < 0 || num_seqs < 0 || n_rows < 0 || !q || !k_data || !k_scale
+    if (max_seq_len < 0 || num_seqs < 0 || n_rows < 0 || !q || !k_data || (!k_fp8 && !k_scale)
         || !block_table || !seq_lens || (!decode && (!cu_seqlens_q || !prefix_lens)))
         return -3;
 #ifdef _OPENMP
@@ -283,8 +293,9 @@ int orc_score(int decode, const void *q, int q_is_e4m3, int unquantized,
                 break;
             }
             for (int d = 0; d < ORC_DIM; ++d)
-                kv[d] = orc_k_value(k_data, k_scale, k_data_page_stride,
-                                    k_scale_page_stride, p, i, d);
+                kv[d] = k_fp8 ? orc_k_value_fp8(k_data, k_data_page_stride, p, i, d)
+                              : orc_k_value(k_data, k_scale, k_data_page_stride,
+                                            k_scale_page_stride, p, i, d);
             for (int h = 0; h < ORC_HEADS; ++h) {
                 double dot = 0.0, val;
                 for (int d = 0; d < ORC_DIM; ++d)
@@ -301,6 +312,39 @@ int orc_score(int decode, const void *q, int q_is_e4m3, int unquantized,
         }
     }
     return status;
+}
+
+/* MXFP4 index cache: the scorer as specified. */
+int orc_score(int decode, const void *q, int q_is_e4m3, int unquantized,
+              const uint8_t *k_data, const uint8_t *k_scale,
+              int64_t k_data_page_stride, int64_t k_scale_page_stride,
+              const int32_t *block_table, int64_t block_table_stride,
+              const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+              const int32_t *prefix_lens, int num_seqs, int max_seq_len,
+              double sm_scale, int64_t num_pool_pages,
+              const int64_t *rows, int64_t n_rows,
+              double *scores, double *logits, int num_threads)
+{
+    return orc_score_impl(decode, q, q_is_e4m3, unquantized, 0, k_data, k_scale, k_data_page_stride,
+                          k_scale_page_stride, block_table, block_table_stride, cu_seqlens_q, seq_lens,
+                          prefix_lens, num_seqs, max_seq_len, sm_scale, num_pool_pages, rows, n_rows,
+                          scores, logits, num_threads);
+}
+
+/* fp8 index cache: the same scorer with K read as plain e4m3 bytes. */
+int orc_score_fp8(int decode, const void *q, int q_is_e4m3, int unquantized,
+                  const uint8_t *k_fp8, int64_t k_page_stride,
+                  const int32_t *block_table, int64_t block_table_stride,
+                  const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                  const int32_t *prefix_lens, int num_seqs, int max_seq_len,
+                  double sm_scale, int64_t num_pool_pages,
+                  const int64_t *rows, int64_t n_rows,
+                  double *scores, double *logits, int num_threads)
+{
+    return orc_score_impl(decode, q, q_is_e4m3, unquantized, 1, k_fp8, NULL, k_page_stride, 0,
+                          block_table, block_table_stride, cu_seqlens_q, seq_lens, prefix_lens,
+                          num_seqs, max_seq_len, sm_scale, num_pool_pages, rows, n_rows, scores,
+                          logits, num_threads);
 }
 
 /* Number of live (row, token) pairs over the listed rows: the causal mask

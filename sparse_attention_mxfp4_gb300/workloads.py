@@ -37,6 +37,7 @@ SCALE_BYTES = PAGE * DIM // 32    # 512: 128 tokens x 4 e8m0 bytes
 PAGE_BYTES = DATA_BYTES + SCALE_BYTES  # 8704
 
 SM_SCALE = float(np.float32(1.0 / math.sqrt(DIM)))
+FP8_PAGE_BYTES = PAGE * DIM       # 16384: 128 tokens x 128 e4m3 bytes (fp8 index cache)
 
 
 @dataclasses.dataclass
@@ -60,6 +61,8 @@ class Workload:
     max_seq_len: int
     sm_scale: float = SM_SCALE
     description: str = ""
+    cache: str = "mxfp4"            # "mxfp4", or "fp8": pages_fp8 holds the cache
+    pages_fp8: Optional[torch.Tensor] = None   # [U, 128, 128] uint8 e4m3 bytes
 
     @property
     def num_seqs(self) -> int:
@@ -118,11 +121,33 @@ def _garbage_tails(g, bt, seq_lens, page_index, pages_data, pages_scale):
         pages_scale[u, PAGE - tail:] = sc
 
 
+def _fp8_pages(g, n_pages):
+    """fp8 index-cache pages: N(0, 1) keys cast to float8_e4m3fn by torch
+    (input synthesis; |x| < 448 for these draws)."""
+    x = torch.randn((n_pages, PAGE, DIM), generator=g, dtype=torch.float32)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _fp8_garbage_tails(g, bt, seq_lens, page_index, pages_fp8):
+    """Random bytes past each request's end inside its last page, the e4m3
+    NaN codes 0x7F and 0xFF included."""
+    for b in range(bt.shape[0]):
+        s = int(seq_lens[b])
+        if s % PAGE == 0 or s == 0:
+            continue
+        u = page_index[int(bt[b, s // PAGE])]
+        tail = PAGE - s % PAGE
+        t = torch.randint(0, 256, (tail, DIM), generator=g, dtype=torch.uint8)
+        t[0, 0] = 0x7F
+        t[-1, -1] = 0xFF
+        pages_fp8[u, PAGE - tail:] = t
+
+
 def make_workload(name, *, seed, q_lens, seq_lens, prefix_lens=None, decode=False,
                   pool_pages, q_e4m3=False, scale_lo=122, scale_hi=127,
                   layout="single", k_data_page_stride=None, k_scale_page_stride=None,
                   page_id_range=None, forced_page_ids=(), bt_width=None,
-                  description="") -> Workload:
+                  description="", cache="mxfp4") -> Workload:
     """Generic seeded workload.
 
     ``q_lens`` (prefill) / one row per request (decode), ``seq_lens`` and
@@ -159,7 +184,16 @@ def make_workload(name, *, seed, q_lens, seq_lens, prefix_lens=None, decode=Fals
     pages_data, pages_scale = _page_contents(g, n_used, scale_lo, scale_hi)
     page_index = {int(p): u for u, p in enumerate(ids)}
     _garbage_tails(g, bt, seq_lens, page_index, pages_data, pages_scale)
-    if layout == "single":
+    pages_fp8 = None
+    if cache == "fp8":
+        # drawn after everything else, so the MXFP4 fields match the same
+        # seed's MXFP4 workload
+        pages_fp8 = _fp8_pages(g, n_used)
+        _fp8_garbage_tails(g, bt, seq_lens, page_index, pages_fp8)
+        layout = "fp8"
+        sd = k_data_page_stride or FP8_PAGE_BYTES
+        ss = 0
+    elif layout == "single":
         sd = ss = k_data_page_stride or PAGE_BYTES
     else:
         sd = k_data_page_stride or DATA_BYTES
@@ -180,11 +214,14 @@ def make_workload(name, *, seed, q_lens, seq_lens, prefix_lens=None, decode=Fals
                     num_pool_pages=pool_pages, layout=layout, k_data_page_stride=sd,
                     k_scale_page_stride=ss, block_table=bt, seq_lens=seq_lens_t,
                     cu_seqlens_q=cu, prefix_lens=pl, max_query_len=max_q,
-                    max_seq_len=max_seq_len, description=description)
+                    max_seq_len=max_seq_len, description=description, cache=cache, pages_fp8=pages_fp8)
 
 
 # ---------------------------------------------------------------- configs --
 CONFIG_NAMES = ("prefill-tiny", "decode", "prefill-long", "mtp", "chunked")
+# the same workloads over an fp8 index cache (128 B per token), the format the
+# MXFP4 cache replaces
+FP8_CONFIG_NAMES = ("decode-fp8", "prefill-long-fp8")
 
 # 2^32 lies inside page 493447 of an 8704 B-page pool (it starts at byte
 # 4,294,962,688), so forcing that page in exercises the 64-bit page rebase.
@@ -192,7 +229,16 @@ STRADDLE_2_32_PAGE = 493447
 
 
 def make_config(name: str, seed: Optional[int] = None) -> Workload:
-    """The five measured configurations (H=64, D=128, 128-token pages)."""
+    """The five measured configurations (H=64, D=128, 128-token pages), and
+    the decode and prefill-long shapes over an fp8 index cache."""
+    if name == "decode-fp8":
+        return make_workload(name, seed=5 if seed is None else seed, q_lens=None, seq_lens=[131072] * 64,
+                             decode=True, pool_pages=70000, cache="fp8",
+                             description="B=64 x 1 row, seq 131072, fp8 cache (16384 B pages) in a 70000-page pool")
+    if name == "prefill-long-fp8":
+        return make_workload(name, seed=6 if seed is None else seed, q_lens=[4096], seq_lens=[131072],
+                             prefix_lens=[126976], pool_pages=2048, cache="fp8",
+                             description="B=1, 4096 rows, prefix 126976, seq 131072, fp8 cache, 2048-page pool")
     idx = CONFIG_NAMES.index(name)
     seed = idx if seed is None else seed
     if name == "prefill-tiny":
@@ -263,6 +309,8 @@ def _fill_pool(data_buf, scale_buf, w, ids, pages_data, pages_scale):
 
 def pool_nbytes(w: Workload):
     """Bytes of the pool buffers: (data_buffer, scale_buffer or 0 when single)."""
+    if w.cache == "fp8":
+        return (w.num_pool_pages - 1) * w.k_data_page_stride + FP8_PAGE_BYTES, 0
     if w.layout == "single":
         return (w.num_pool_pages - 1) * w.k_data_page_stride + PAGE_BYTES, 0
     return ((w.num_pool_pages - 1) * w.k_data_page_stride + DATA_BYTES,
@@ -285,6 +333,12 @@ def build_pool(w: Workload, device="cpu", fill_seed: Optional[int] = 1234,
             t = t.pin_memory()
         return t
     ids = w.page_ids.to(device)
+    if w.cache == "fp8":
+        buf = alloc(nd)
+        d_idx = (ids.view(-1, 1) * w.k_data_page_stride
+                 + torch.arange(FP8_PAGE_BYTES, device=device)).view(-1)
+        buf.index_copy_(0, d_idx, w.pages_fp8.to(device).reshape(-1))
+        return [buf], (buf, 0), (buf, 0)
     pd = w.pages_data.to(device)
     ps = w.pages_scale.to(device)
     if w.layout == "single":
@@ -316,6 +370,9 @@ def compact_host(w: Workload):
     for i in range(flat.shape[0]):
         v = int(flat[i])
         flat[i] = index[v] if v >= 0 else -1
+    if w.cache == "fp8":
+        kd = w.pages_fp8.numpy().reshape(-1)
+        return kd, None, FP8_PAGE_BYTES, 0, bt.numpy(), len(ids)
     kd = w.pages_data.numpy().reshape(-1)
     ks = w.pages_scale.numpy().reshape(-1)
     return kd, ks, DATA_BYTES, SCALE_BYTES, bt.numpy(), len(ids)

@@ -30,6 +30,14 @@ def oracle_run(w: W.Workload, rows=None, logits=False, scores=True, real_pool=Fa
         npool = w.num_pool_pages
     else:
         kd, ks, sd, ss, bt, npool = W.compact_host(w)
+    if w.cache == "fp8":
+        return oracle.score_fp8(
+            decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, k_fp8=kd, k_page_stride=sd,
+            block_table=bt, block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
+            cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
+            prefix_lens=None if w.decode else w.prefix_lens.numpy(),
+            max_seq_len=w.max_seq_len, sm_scale=w.sm_scale, rows=rows,
+            want_scores=scores, want_logits=logits, num_pool_pages=npool, num_threads=num_threads)
     return oracle.score(
         decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, k_data=kd, k_scale=ks,
         k_data_page_stride=sd, k_scale_page_stride=ss, block_table=bt,
@@ -73,9 +81,21 @@ def compare(got, ref, rtol=RTOL, atol=ATOL, what="scores", extra=None):
             "max_rel_err": rel, "fp32_exact_fraction": exact}
 
 
+def e4m3_values_numpy(codes):
+    """e4m3 (fn) values from the bit fields: bias 7, subnormal step 2^-9,
+    S.1111.111 NaN."""
+    c = np.asarray(codes).astype(np.int64)
+    s, e, m = (c >> 7) & 1, (c >> 3) & 15, c & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag)
+
+
 def dequant_numpy(w: W.Workload):
     """Independent dequantisation in numpy from the bit fields of each code
     (used to pin the oracle; shares nothing with the oracle's C code)."""
+    if w.cache == "fp8":
+        return e4m3_values_numpy(w.pages_fp8.numpy())       # [U, 128, 128]
     data = w.pages_data.numpy()
     scale = w.pages_scale.numpy().astype(np.float64)
     lo = data & 15
