@@ -187,7 +187,7 @@ def workload_work(w):
     pages_read = int(((L_last + W.PAGE - 1) // W.PAGE).sum())
     q_bytes = w.q.numel() * w.q.element_size()
     out_bytes = w.total_rows * W.HEADS * w.num_out_pages * 4
-    k_bytes = pages_read * W.PAGE_BYTES
+    k_bytes = pages_read * (W.FP8_PAGE_BYTES if w.cache == "fp8" else W.PAGE_BYTES)
     bt_bytes = pages_read * 4
     flops = live_pairs * W.HEADS * W.DIM * 2
     return {"k_bytes": k_bytes, "q_bytes": q_bytes, "out_bytes": out_bytes, "bt_bytes": bt_bytes,
@@ -271,13 +271,16 @@ def cpu_baseline_decode(w):
     kd, ks, sd, ss, bt, n = W.compact_host(w)
     cores = os.cpu_count() or 1
     rows = np.arange(w.total_rows)
+    common = dict(decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, block_table=bt,
+                  block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
+                  cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
+                  prefix_lens=None if w.decode else w.prefix_lens.numpy(), max_seq_len=w.max_seq_len,
+                  sm_scale=w.sm_scale, rows=rows, num_pool_pages=n, num_threads=cores)
     t0 = time.perf_counter()
-    oracle.score(decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, k_data=kd, k_scale=ks,
-                 k_data_page_stride=sd, k_scale_page_stride=ss, block_table=bt,
-                 block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
-                 cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
-                 prefix_lens=None if w.decode else w.prefix_lens.numpy(), max_seq_len=w.max_seq_len,
-                 sm_scale=w.sm_scale, rows=rows, num_pool_pages=n, num_threads=cores)
+    if w.cache == "fp8":
+        oracle.score_fp8(k_fp8=kd, k_page_stride=sd, **common)
+    else:
+        oracle.score(k_data=kd, k_scale=ks, k_data_page_stride=sd, k_scale_page_stride=ss, **common)
     dt = time.perf_counter() - t0
     return {"value": dt * 1e6, "unit": "us/call", "cores": cores, "kind": "oracle",
             "sample": f"full call: all {len(rows)} query rows of the {w.name} workload, fp64, "
@@ -299,11 +302,12 @@ def secondary_configs(names, peaks, stream):
         steps = 200 if name == "prefill-tiny" else (5 if name == "chunked" else 20)
         ms = time_calls(case, out, steps, 3, stream)
         tf = work["flops"] / (ms * 1e-3) / 1e12
-        res[name] = {"us_per_call": round(ms * 1e3, 3), "steps": steps,
+        res[name] = {"us_per_call": round(ms * 1e3, 3), "steps": steps, "cache": w.cache,
                      "mma_tflops": round(tf, 1),
                      "frac_of_fp8_dense_peak": round(tf / fp8_peak, 4),
                      "frac_of_fp4_dense_peak": round(tf / fp4_peak, 4),
                      "hbm_gbs_algorithmic": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_hbm_peak": round(work["bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
                      "flops_per_call": work["flops"], "bytes_per_call": work["bytes"]}
         del case, out
         torch.cuda.empty_cache()
@@ -461,7 +465,7 @@ def run_ours(args):
         if ws == 1 and not args.no_secondary:
             del case, out
             torch.cuda.empty_cache()
-            names = [n for n in W.CONFIG_NAMES if n != w.name]
+            names = [n for n in W.CONFIG_NAMES + W.FP8_CONFIG_NAMES if n != w.name]
             line["secondary"] = secondary_configs(names, peaks, stream)
             line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
     if ws > 1:
@@ -545,7 +549,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="decode",
-                    choices=("decode", "prefill-tiny", "prefill-long", "mtp", "chunked"))
+                    choices=("decode", "prefill-tiny", "prefill-long", "mtp", "chunked", "decode-fp8",
+                             "prefill-long-fp8"))
     ap.add_argument("--no-secondary", action="store_true", help="skip the other configurations")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     args = ap.parse_args()

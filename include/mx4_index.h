@@ -158,6 +158,45 @@ mx4_status mx4_index_logits_decode(const void *q, int q_is_e4m3, const uint8_t *
                                    int64_t block_table_stride, int64_t num_pool_pages);
 
 /*
+ * The same scorer over an fp8 index cache, the format the MXFP4 cache
+ * replaces ([P1] summary: 128 B per token for fp8 against 68 B for MXFP4;
+ * [P1] "Kernels": the fp8 and MXFP4 scorers share tiling, Q staging, causal
+ * mask, folds and stores and differ only in the K side).  READING of the
+ * fp8 page: 128 tokens x 128 e4m3 bytes, token i at byte i*128 of the page,
+ * element d at byte d, no scale; logit = sm_scale * sum_d Q8 * e4m3(K).
+ *
+ *   k_fp8          page p at k_fp8 + p * k_page_stride; 16-byte aligned,
+ *                  k_page_stride >= 16384 and a multiple of 16.
+ * Every other argument, the outputs, ownership, streams and errors are as
+ * for the MXFP4 calls above (k_scale and its stride do not exist here).
+ */
+mx4_status mx4_index_score_prefill_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8,
+                                       int64_t k_page_stride, const int32_t *block_table,
+                                       const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                       const int32_t *prefix_lens, int max_query_len, int max_seq_len,
+                                       float sm_scale, float *out, void *stream, int num_seqs,
+                                       int64_t block_table_stride, int64_t num_pool_pages);
+
+mx4_status mx4_index_score_decode_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8,
+                                      int64_t k_page_stride, const int32_t *block_table,
+                                      const int32_t *seq_lens, int max_seq_len, float sm_scale, float *out,
+                                      void *stream, int num_seqs, int64_t block_table_stride,
+                                      int64_t num_pool_pages);
+
+mx4_status mx4_index_logits_prefill_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8,
+                                        int64_t k_page_stride, const int32_t *block_table,
+                                        const int32_t *cu_seqlens_q, const int32_t *seq_lens,
+                                        const int32_t *prefix_lens, int max_query_len, int max_seq_len,
+                                        float sm_scale, float *logits, void *stream, int num_seqs,
+                                        int64_t block_table_stride, int64_t num_pool_pages);
+
+mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8,
+                                       int64_t k_page_stride, const int32_t *block_table,
+                                       const int32_t *seq_lens, int max_seq_len, float sm_scale,
+                                       float *logits, void *stream, int num_seqs,
+                                       int64_t block_table_stride, int64_t num_pool_pages);
+
+/*
  * The query-preparation step on its own: n bf16 values (raw bits) rounded to
  * e4m3 bytes, nearest even, saturating to +-448, signed zero kept ([P1]
  * "Kernels": a bf16 query is rounded to e4m3 in-kernel; the scorers above do

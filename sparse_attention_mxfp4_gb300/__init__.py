@@ -40,6 +40,10 @@ EXPORTED_SYMBOLS = (
     "mx4_index_score_decode",
     "mx4_index_logits_prefill",
     "mx4_index_logits_decode",
+    "mx4_index_score_prefill_fp8",
+    "mx4_index_score_decode_fp8",
+    "mx4_index_logits_prefill_fp8",
+    "mx4_index_logits_decode_fp8",
     "mx4_quantize_q_e4m3",
     "mx4_index_k_write",
     "mx4_index_get_device_status",
@@ -76,6 +80,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                            ("mx4_index_logits_prefill", prefill_args),
                            ("mx4_index_score_decode", decode_args),
                            ("mx4_index_logits_decode", decode_args)):
+            f = getattr(lib, name)
+            f.restype = i32
+            f.argtypes = args
+        prefill_fp8_args = [vp, i32, vp, i64, vp, vp, vp, vp, i32, i32, f32, vp, vp, i32, i64, i64]
+        decode_fp8_args = [vp, i32, vp, i64, vp, vp, i32, f32, vp, vp, i32, i64, i64]
+        for name, args in (("mx4_index_score_prefill_fp8", prefill_fp8_args),
+                           ("mx4_index_logits_prefill_fp8", prefill_fp8_args),
+                           ("mx4_index_score_decode_fp8", decode_fp8_args),
+                           ("mx4_index_logits_decode_fp8", decode_fp8_args)):
             f = getattr(lib, name)
             f.restype = i32
             f.argtypes = args
@@ -189,6 +202,52 @@ def mx4_index_logits_prefill(*args, **kwargs):
 
 def mx4_index_logits_decode(*args, **kwargs):
     return mx4_index_score_decode(*args, logits=True, **kwargs)
+
+
+def _bt_stride(block_table):
+    return int(block_table.stride(0)) if block_table.dim() == 2 else int(block_table.shape[-1])
+
+
+def mx4_index_score_prefill_fp8(q, k_fp8, k_page_stride, block_table, cu_seqlens_q, seq_lens, prefix_lens,
+                                max_query_len, max_seq_len, sm_scale, out=None, *, num_pool_pages,
+                                stream=None, logits=False):
+    """Prefill block scores (or logits) over an fp8 index cache: ``k_fp8`` is
+    a uint8 tensor whose first byte is page 0 (128 tokens x 128 e4m3 bytes)."""
+    lib = load_library()
+    e4 = _q_info(q)
+    P = (max_seq_len + PAGE - 1) // PAGE
+    out = _out(out, (q.shape[0], HEADS, max_seq_len if logits else P), q)
+    fn = "mx4_index_logits_prefill_fp8" if logits else "mx4_index_score_prefill_fp8"
+    st = getattr(lib, fn)(
+        _ptr(q), e4, _ptr(k_fp8), int(k_page_stride), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens),
+        _ptr(prefix_lens), int(max_query_len), int(max_seq_len), float(sm_scale), _ptr(out), _stream(stream),
+        int(seq_lens.shape[0]), _bt_stride(block_table), int(num_pool_pages))
+    _check(fn, st)
+    return out
+
+
+def mx4_index_score_decode_fp8(q, k_fp8, k_page_stride, block_table, seq_lens, max_seq_len, sm_scale,
+                               out=None, *, num_pool_pages, stream=None, logits=False):
+    """Decode block scores (or logits) over an fp8 index cache."""
+    lib = load_library()
+    e4 = _q_info(q)
+    P = (max_seq_len + PAGE - 1) // PAGE
+    out = _out(out, (q.shape[0], HEADS, max_seq_len if logits else P), q)
+    fn = "mx4_index_logits_decode_fp8" if logits else "mx4_index_score_decode_fp8"
+    st = getattr(lib, fn)(
+        _ptr(q), e4, _ptr(k_fp8), int(k_page_stride), _ptr(block_table), _ptr(seq_lens), int(max_seq_len),
+        float(sm_scale), _ptr(out), _stream(stream), int(seq_lens.shape[0]), _bt_stride(block_table),
+        int(num_pool_pages))
+    _check(fn, st)
+    return out
+
+
+def mx4_index_logits_prefill_fp8(*args, **kwargs):
+    return mx4_index_score_prefill_fp8(*args, logits=True, **kwargs)
+
+
+def mx4_index_logits_decode_fp8(*args, **kwargs):
+    return mx4_index_score_decode_fp8(*args, logits=True, **kwargs)
 
 
 def mx4_quantize_q_e4m3(q_bf16, out=None, *, stream=None):

@@ -42,20 +42,20 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     int sm_count = 0;
-    bool smem_attr_set[4] = {false, false, false, false};
+    bool smem_attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 
-template <bool kDecode, bool kLogits>
+template <bool kDecode, bool kLogits, bool kFp8>
 constexpr int kernel_index()
 {
-    return (kDecode ? 1 : 0) + (kLogits ? 2 : 0);
+    return (kDecode ? 1 : 0) + (kLogits ? 2 : 0) + (kFp8 ? 4 : 0);
 }
 
 // Per-device one-time setup: SM count and the dynamic smem opt-in.
-template <bool kDecode, bool kLogits>
+template <bool kDecode, bool kLogits, bool kFp8>
 mx4_status device_setup(int *sm_count)
 {
     int dev = 0;
@@ -68,9 +68,10 @@ mx4_status device_setup(int *sm_count)
             return MX4_ERR_CUDA;
         st.sm_count = n;
     }
-    constexpr int ki = kernel_index<kDecode, kLogits>();
+    constexpr int ki = kernel_index<kDecode, kLogits, kFp8>();
     if (!st.smem_attr_set[ki]) {
-        if (cudaFuncSetAttribute(mx4::mx4_score_kernel<kDecode, kLogits>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(mx4::mx4_score_kernel<kDecode, kLogits, kFp8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SmemLayout::kAlloc)) != cudaSuccess)
             return MX4_ERR_CUDA;
         st.smem_attr_set[ki] = true;
@@ -96,6 +97,23 @@ bool encode_kdata_map(CUtensorMap *m, const uint8_t *k_data, int64_t stride, int
     const cuuint32_t box[4] = {128, 32, 4, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t *>(k_data), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp8 page view, the same 4-D shape over bytes: dim0: the 128 e4m3 bytes of
+// one token, dim1: n0 (stride 512 B), dim2: n1 (stride 128 B), dim3: page.
+// The box lands token 4*n0 + n1 in smem row n0 + 32*n1 (128 B rows,
+// 128-byte swizzled), the same row order as the MXFP4 view.
+bool encode_kfp8_map(CUtensorMap *m, const uint8_t *k, int64_t stride, int64_t pages)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {128, 32, 4, static_cast<cuuint64_t>(pages)};
+    const cuuint64_t strides[3] = {512, 128, static_cast<cuuint64_t>(stride)};
+    const cuuint32_t box[4] = {128, 32, 4, 1};
+    const cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(k), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -132,6 +150,7 @@ struct Args {
     int num_seqs;
     int64_t bt_stride;
     int64_t num_pool_pages;
+    bool fp8 = false;   // k_data is an fp8 cache (k_scale, ss unused)
 };
 
 // True when the call has no output cell (no request, no query row or no
@@ -147,23 +166,30 @@ mx4_status validate(const Args &a, bool decode)
     if (a.num_seqs < 0 || a.max_seq_len < 0 || (!decode && a.max_query_len < 0)) return MX4_ERR_INVALID_ARG;
     if (!(std::isfinite(a.sm_scale) && a.sm_scale > 0.0f)) return MX4_ERR_INVALID_ARG;
     if (empty_call(a, decode)) return MX4_OK;
-    if (!a.q || !a.k_data || !a.k_scale || !a.block_table || !a.seq_lens || !a.out) return MX4_ERR_INVALID_ARG;
+    if (!a.q || !a.k_data || (!a.fp8 && !a.k_scale) || !a.block_table || !a.seq_lens || !a.out)
+        return MX4_ERR_INVALID_ARG;
     if (!decode && (!a.cu_seqlens_q || !a.prefix_lens)) return MX4_ERR_INVALID_ARG;
-    if (a.sd < mx4::kDataBytes || a.ss < mx4::kScaleBytes) return MX4_ERR_INVALID_ARG;   // narrow views
+    if (a.fp8 ? a.sd < static_cast<int64_t>(mx4::kFp8PageBytes)
+              : (a.sd < mx4::kDataBytes || a.ss < mx4::kScaleBytes))
+        return MX4_ERR_INVALID_ARG;   // narrow views
     if (a.num_pool_pages < 1) return MX4_ERR_INVALID_ARG;
     if (a.num_pool_pages > INT32_MAX) return MX4_ERR_UNSUPPORTED;
     const int64_t P = (static_cast<int64_t>(a.max_seq_len) + mx4::kPage - 1) / mx4::kPage;
     if (a.bt_stride < P || a.bt_stride < 0) return MX4_ERR_INVALID_ARG;                  // narrow table
     if (a.sd >= (int64_t(1) << 40) || a.ss >= (int64_t(1) << 40)) return MX4_ERR_UNSUPPORTED;
-    if (!aligned(a.k_data, 32) || (a.sd % 32) != 0) return MX4_ERR_MISALIGNED;
-    if (!aligned(a.k_scale, 16) || (a.ss % 16) != 0) return MX4_ERR_MISALIGNED;
+    if (a.fp8) {
+        if (!aligned(a.k_data, 16) || (a.sd % 16) != 0) return MX4_ERR_MISALIGNED;
+    } else {
+        if (!aligned(a.k_data, 32) || (a.sd % 32) != 0) return MX4_ERR_MISALIGNED;
+        if (!aligned(a.k_scale, 16) || (a.ss % 16) != 0) return MX4_ERR_MISALIGNED;
+    }
     if (!aligned(a.q, 16) || !aligned(a.out, 16)) return MX4_ERR_MISALIGNED;
     if (!aligned(a.block_table, 4) || !aligned(a.seq_lens, 4)) return MX4_ERR_MISALIGNED;
     if (!decode && (!aligned(a.cu_seqlens_q, 4) || !aligned(a.prefix_lens, 4))) return MX4_ERR_MISALIGNED;
     return MX4_OK;
 }
 
-template <bool kDecode, bool kLogits>
+template <bool kDecode, bool kLogits, bool kFp8 = false>
 mx4_status launch(const Args &a)
 {
     mx4_status st = validate(a, kDecode);
@@ -176,13 +202,18 @@ mx4_status launch(const Args &a)
     const int64_t num_units = static_cast<int64_t>(a.num_seqs) * tiles_per_seq * chunks_per_tile;
 
     int sm_count = 0;
-    st = device_setup<kDecode, kLogits>(&sm_count);
+    st = device_setup<kDecode, kLogits, kFp8>(&sm_count);
     if (st != MX4_OK) return st;
 
     alignas(64) CUtensorMap tmap_k;
     alignas(64) CUtensorMap tmap_s;
-    if (!encode_kdata_map(&tmap_k, a.k_data, a.sd, a.num_pool_pages)) return MX4_ERR_CUDA;
-    if (!encode_kscale_map(&tmap_s, a.k_scale, a.ss, a.num_pool_pages)) return MX4_ERR_CUDA;
+    if (kFp8) {
+        if (!encode_kfp8_map(&tmap_k, a.k_data, a.sd, a.num_pool_pages)) return MX4_ERR_CUDA;
+        tmap_s = tmap_k;   // unused by the fp8 kernel
+    } else {
+        if (!encode_kdata_map(&tmap_k, a.k_data, a.sd, a.num_pool_pages)) return MX4_ERR_CUDA;
+        if (!encode_kscale_map(&tmap_s, a.k_scale, a.ss, a.num_pool_pages)) return MX4_ERR_CUDA;
+    }
 
     ScoreParams p{};
     p.q = a.q;
@@ -207,7 +238,7 @@ mx4_status launch(const Args &a)
     // units); each CTA takes a contiguous, equal share of the units.
     const int64_t grid = num_units < sm_count ? num_units : sm_count;
     cudaGetLastError();   // clear a stale error so the check below is ours
-    mx4::mx4_score_kernel<kDecode, kLogits>
+    mx4::mx4_score_kernel<kDecode, kLogits, kFp8>
         <<<static_cast<unsigned>(grid), mx4::kThreads, SmemLayout::kAlloc, a.stream>>>(tmap_k, tmap_s, p);
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
@@ -268,6 +299,60 @@ mx4_status mx4_index_logits_decode(const void *q, int q_is_e4m3, const uint8_t *
                  sm_scale,    logits,    static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
                  num_pool_pages};
     return launch<true, true>(a);
+}
+
+mx4_status mx4_index_score_prefill_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8, int64_t k_page_stride,
+                                       const int32_t *block_table, const int32_t *cu_seqlens_q,
+                                       const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
+                                       int max_seq_len, float sm_scale, float *out, void *stream, int num_seqs,
+                                       int64_t block_table_stride, int64_t num_pool_pages)
+{
+    Args a{q,           q_is_e4m3,    k_fp8,    nullptr,     k_page_stride, 0,
+           block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len, max_seq_len,
+           sm_scale,    out,          static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+           num_pool_pages};
+    a.fp8 = true;
+    return launch<false, false, true>(a);
+}
+
+mx4_status mx4_index_score_decode_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8, int64_t k_page_stride,
+                                      const int32_t *block_table, const int32_t *seq_lens, int max_seq_len,
+                                      float sm_scale, float *out, void *stream, int num_seqs,
+                                      int64_t block_table_stride, int64_t num_pool_pages)
+{
+    Args a{q,           q_is_e4m3, k_fp8,    nullptr, k_page_stride, 0,
+           block_table, nullptr,   seq_lens, nullptr, 1,             max_seq_len,
+           sm_scale,    out,       static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+           num_pool_pages};
+    a.fp8 = true;
+    return launch<true, false, true>(a);
+}
+
+mx4_status mx4_index_logits_prefill_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8, int64_t k_page_stride,
+                                        const int32_t *block_table, const int32_t *cu_seqlens_q,
+                                        const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
+                                        int max_seq_len, float sm_scale, float *logits, void *stream, int num_seqs,
+                                        int64_t block_table_stride, int64_t num_pool_pages)
+{
+    Args a{q,           q_is_e4m3,    k_fp8,    nullptr,     k_page_stride, 0,
+           block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len, max_seq_len,
+           sm_scale,    logits,       static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+           num_pool_pages};
+    a.fp8 = true;
+    return launch<false, true, true>(a);
+}
+
+mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8_t *k_fp8, int64_t k_page_stride,
+                                       const int32_t *block_table, const int32_t *seq_lens, int max_seq_len,
+                                       float sm_scale, float *logits, void *stream, int num_seqs,
+                                       int64_t block_table_stride, int64_t num_pool_pages)
+{
+    Args a{q,           q_is_e4m3, k_fp8,    nullptr, k_page_stride, 0,
+           block_table, nullptr,   seq_lens, nullptr, 1,             max_seq_len,
+           sm_scale,    logits,    static_cast<cudaStream_t>(stream), num_seqs, block_table_stride,
+           num_pool_pages};
+    a.fp8 = true;
+    return launch<true, true, true>(a);
 }
 
 mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t n, void *stream)

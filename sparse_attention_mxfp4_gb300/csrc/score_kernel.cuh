@@ -88,19 +88,26 @@ constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4 * kMmaWarps;
 // Transaction bytes of one page: the 4-bit TMA load counts the packed
 // global bytes (8192), not the 16 KB it writes in the padded smem form.
 constexpr uint32_t kStageTxBytes = kDataBytes + kScaleBytes;
+// fp8 index cache: one 16 KB page of 128 tokens x 128 e4m3 bytes, no scales.
+constexpr uint32_t kFp8PageBytes = 128 * 128;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s per wait
 
 static_assert(kTmemSfbCol + 4 * kSfbBufs <= kTmemCols, "TMEM budget");
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling:
-// A = E4M3 (0, bits 7..9), B = E2M1 (5, bits 10..12), both K-major,
-// N >> 3 in bits 17..22, scale type UE8M0 (bit 23), M >> 4 in bits 24..28,
-// B scale-factor id in bits 4..5, A scale-factor id in bits 29..30 (the id
-// picks byte k of each 32-bit scale word for the k-th 32-element block).
-constexpr uint32_t kIdescBase = (0u << 7) | (5u << 10) | ((128u >> 3) << 17) | (1u << 23) |
-                                ((128u >> 4) << 24);
-
-__device__ __forceinline__ uint32_t idesc_for_k(uint32_t k) { return kIdescBase | (k << 4) | (k << 29); }
+// A = E4M3 (0, bits 7..9), B = E2M1 (5, bits 10..12) for the MXFP4 cache or
+// E4M3 (0) for the fp8 cache, both K-major, N >> 3 in bits 17..22, scale type
+// UE8M0 (bit 23), M >> 4 in bits 24..28, B scale-factor id in bits 4..5, A
+// scale-factor id in bits 29..30 (the id picks byte k of each 32-bit scale
+// word for the k-th 32-element block).  The fp8 cache runs with unit scales
+// on both sides.
+template <bool kFp8>
+__device__ __forceinline__ uint32_t idesc_for_k(uint32_t k)
+{
+    constexpr uint32_t kBase = (0u << 7) | ((kFp8 ? 0u : 5u) << 10) | ((128u >> 3) << 17) | (1u << 23) |
+                               ((128u >> 4) << 24);
+    return kBase | (k << 4) | (k << 29);
+}
 
 // Device status word of this module (MX4_DEV_* bits), ORed by the kernels
 // and read back and cleared by the host.
@@ -335,7 +342,9 @@ struct LaneTurn {
 // MMA column n holds token 4*(n%32) + n/32.
 __device__ __forceinline__ int token_of_col(int n) { return ((n & 31) << 2) | (n >> 5); }
 
-template <bool kDecode, bool kLogits>
+// kFp8: the cache holds 128 e4m3 bytes per token (tmap_k is a UINT8 view of
+// the same 4-D shape, tmap_s is unused); otherwise MXFP4 codes and scales.
+template <bool kDecode, bool kLogits, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     mx4_score_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_s,
                      const __grid_constant__ ScoreParams p)
@@ -385,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == kLaneWarp0 && lane == 0) {
         prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_s);
+        if (!kFp8) prefetch_tmap(&tmap_s);
     }
     if (warp == kLaneWarp0) {
         tmem_alloc(sbase + SmemLayout::kTmemSlot, kTmemCols);
@@ -486,11 +495,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int id = __shfl_sync(0xffffffffu, tc_pid, tc_i);
             const int stage = ln * kStagesPerLane + pst.idx;
             if (elect_one()) {
-                mbar_arrive_expect_tx(full_bar(stage), kStageTxBytes);
+                mbar_arrive_expect_tx(full_bar(stage), kFp8 ? kFp8PageBytes : kStageTxBytes);
                 tma_load_4d(sbase + SmemLayout::kData + stage * kTileBytes, &tmap_k, full_bar(stage), 0, 0, 0, id,
                             policy);
-                tma_load_2d(sbase + SmemLayout::kScale + stage * kScaleBytes, &tmap_s, full_bar(stage), 0, id,
-                            policy);
+                if (!kFp8)
+                    tma_load_2d(sbase + SmemLayout::kScale + stage * kScaleBytes, &tmap_s, full_bar(stage), 0, id,
+                                policy);
             }
             __syncwarp();
             ring_next<kStagesPerLane>(pst);
@@ -579,15 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (elect_one()) {
-                    const uint32_t tmem_sfb = tmem_base + kTmemSfbCol + 4u * sfb;
-                    // descriptor start addresses count 16-byte units
-                    tc_cp_32x128b_warpx4(tmem_sfb, sdesc0 + static_cast<uint64_t>(stage * (kScaleBytes >> 4)));
+                    // fp8 pages carry no scales: B uses the unit scales of A
+                    uint32_t tmem_sfb = tmem_sfa;
+                    if (!kFp8) {
+                        tmem_sfb = tmem_base + kTmemSfbCol + 4u * sfb;
+                        // descriptor start addresses count 16-byte units
+                        tc_cp_32x128b_warpx4(tmem_sfb, sdesc0 + static_cast<uint64_t>(stage * (kScaleBytes >> 4)));
+                    }
                     const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (kTileBytes >> 4));
                     // K block k: +32 bytes of B (2 units of 16 B), +8 TMEM columns of A
-                    tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k(0), tmem_sfa, tmem_sfb, 0u);
-                    tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k(1), tmem_sfa, tmem_sfb, 1u);
-                    tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k(2), tmem_sfa, tmem_sfb, 1u);
-                    tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k(3), tmem_sfa, tmem_sfb, 1u);
+                    tc_mma_mx_ts(d_tmem, a_tmem, bdesc, idesc_for_k<kFp8>(0), tmem_sfa, tmem_sfb, 0u);
+                    tc_mma_mx_ts(d_tmem, a_tmem + 8u, bdesc + 2, idesc_for_k<kFp8>(1), tmem_sfa, tmem_sfb, 1u);
+                    tc_mma_mx_ts(d_tmem, a_tmem + 16u, bdesc + 4, idesc_for_k<kFp8>(2), tmem_sfa, tmem_sfb, 1u);
+                    tc_mma_mx_ts(d_tmem, a_tmem + 24u, bdesc + 6, idesc_for_k<kFp8>(3), tmem_sfa, tmem_sfb, 1u);
                     tc_commit(dfull_bar(ln));
                 }
                 __syncwarp();

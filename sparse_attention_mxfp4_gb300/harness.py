@@ -10,7 +10,8 @@ import dataclasses
 
 import torch
 
-from . import mx4_index_score_decode, mx4_index_score_prefill
+from . import (mx4_index_score_decode, mx4_index_score_decode_fp8, mx4_index_score_prefill,
+               mx4_index_score_prefill_fp8)
 from . import workloads as W
 
 
@@ -36,6 +37,15 @@ class DeviceCase:
 
     def run(self, out=None, logits=False, stream=None):
         w = self.w
+        if w.cache == "fp8":
+            if w.decode:
+                return mx4_index_score_decode_fp8(
+                    self.q, self.k_data, w.k_data_page_stride, self.block_table, self.seq_lens, w.max_seq_len,
+                    w.sm_scale, out, num_pool_pages=w.num_pool_pages, stream=stream, logits=logits)
+            return mx4_index_score_prefill_fp8(
+                self.q, self.k_data, w.k_data_page_stride, self.block_table, self.cu_seqlens_q, self.seq_lens,
+                self.prefix_lens, w.max_query_len, w.max_seq_len, w.sm_scale, out,
+                num_pool_pages=w.num_pool_pages, stream=stream, logits=logits)
         if w.decode:
             return mx4_index_score_decode(
                 self.q, self.k_data, self.k_scale, w.k_data_page_stride, w.k_scale_page_stride,
@@ -63,7 +73,7 @@ def to_device(w: W.Workload, device="cuda", fill_seed=None) -> DeviceCase:
     if fill_seed is not None:
         bufs = [b.to(device) for b in bufs]
         dbuf = bufs[0]
-        sbuf = bufs[-1] if w.layout != "single" else bufs[0]
+        sbuf = bufs[-1] if w.layout == "split" else bufs[0]
     q = w.q.to(device)
     bt = w.block_table.to(device)
     sl = w.seq_lens.to(device)

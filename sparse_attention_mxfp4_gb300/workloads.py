@@ -19,6 +19,10 @@ of the same page, "Format", uses bytes 100..150):
   garbage, scale bytes 0 and 255 included.
 * Block-table entries past a request's last page are filled with -1.
 * sm_scale = fp32(1/sqrt(128)).
+* fp8 index cache (cache="fp8"): keys N(0, 1) cast to float8_e4m3fn by torch;
+  garbage tails are random bytes with the e4m3 NaN codes planted.
+* Index-K writes: bf16 keys N(0, 1), or a wide-range mix (see _keys), into
+  slots from seeded block tables or seeded distinct pool slots.
 """
 from __future__ import annotations
 

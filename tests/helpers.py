@@ -214,3 +214,40 @@ def logits_accum_allowance(w: W.Workload, rows=None):
         val = np.abs(qv[r] @ k.T)
         out[ri, :, :n] = w.sm_scale * (GAMMA_128 * absum + _U * val)
     return out
+
+
+def e4m3_code_exact(v):
+    """The e4m3 byte whose value is exactly v (exhaustive search over the 256
+    codes, sign of zero kept), or -1 where no byte has that value."""
+    vals = e4m3_values_numpy(np.arange(256))
+    v = np.asarray(v, dtype=np.float64)
+    out = np.full(v.shape, -1, dtype=np.int64)
+    o = out.reshape(-1)
+    for i, x in enumerate(v.reshape(-1)):
+        hit = [c for c in np.nonzero(vals == x)[0] if np.signbit(vals[c]) == np.signbit(x)]
+        if hit:
+            o[i] = hit[0]
+    return out
+
+
+def mxfp4_as_fp8(w: W.Workload) -> W.Workload:
+    """The MXFP4 workload's keys re-stored as an fp8 cache (every value must be
+    an e4m3 value: scale bytes 119..133)."""
+    import dataclasses
+    vals = dequant_numpy(w)                       # [U, 128, 128]
+    uniq, inv = np.unique(vals.reshape(-1), return_inverse=True)
+    # np.unique merges -0.0 and +0.0; map zeros by their own sign below
+    uc = e4m3_code_exact(uniq)
+    assert (uc >= 0).all(), "a value outside e4m3"
+    codes = uc[inv].reshape(vals.shape)
+    codes = np.where(vals == 0, np.where(np.signbit(vals), 0x80, 0x00), codes).astype(np.uint8)
+    return dataclasses.replace(w, cache="fp8", layout="fp8", pages_fp8=torch.from_numpy(codes),
+                               k_data_page_stride=W.FP8_PAGE_BYTES, k_scale_page_stride=0)
+
+
+def clamp_garbage_scales(w: W.Workload, lo=119, hi=133) -> W.Workload:
+    """Scale bytes outside [lo, hi] (only in garbage tails) set to 127."""
+    import dataclasses
+    ps = w.pages_scale.clone()
+    ps[(ps < lo) | (ps > hi)] = 127
+    return dataclasses.replace(w, pages_scale=ps)

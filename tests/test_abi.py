@@ -134,6 +134,25 @@ def test_writer_rejections(lib, kw, status):
                                  a["pages"], None) == status
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sd=16384 - 16), mx4.MX4_ERR_INVALID_ARG),             # narrow fp8 page
+    (dict(k=A + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(sd=16384 + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(pages=0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(B=0, k=None), mx4.MX4_OK),                             # nothing to do
+])
+def test_fp8_rejections(lib, kw, status):
+    a = dict(q=A, k=A, sd=16384, bt=A, cu=A, sl=A, pl=A, mq=4, ms=512, out=A, B=1, bts=4, pages=8)
+    a.update(kw)
+    got = lib.mx4_index_score_prefill_fp8(a["q"], 0, a["k"], a["sd"], a["bt"], a["cu"], a["sl"], a["pl"], a["mq"],
+                                          a["ms"], 0.088, a["out"], None, a["B"], a["bts"], a["pages"])
+    assert got == status
+    got_d = lib.mx4_index_score_decode_fp8(a["q"], 0, a["k"], a["sd"], a["bt"], a["sl"], a["ms"], 0.088, a["out"],
+                                           None, a["B"], a["bts"], a["pages"])
+    assert got_d == status
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import importlib
     missing = str(tmp_path / "nope.so")

@@ -15,36 +15,8 @@ import torch
 
 import oracle
 from sparse_attention_mxfp4_gb300 import workloads as W
-from helpers import dequant_numpy, e4m3_values_numpy, oracle_run, scores_numpy
-
-
-def _e4m3_code_exact(v):
-    """The e4m3 byte whose value is exactly v (exhaustive search), or None."""
-    codes = np.arange(256)
-    vals = e4m3_values_numpy(codes)
-    out = np.full(v.shape, -1, dtype=np.int64)
-    flat = v.reshape(-1)
-    o = out.reshape(-1)
-    for i, x in enumerate(flat):
-        hit = np.nonzero(vals == x)[0]
-        if len(hit):
-            # +0 and -0 both match 0.0; keep the sign of x
-            hit = [c for c in hit if np.signbit(vals[c]) == np.signbit(x)] or list(hit)
-            o[i] = hit[0]
-    return out
-
-
-def _mxfp4_as_fp8(w):
-    """The MXFP4 workload's live keys re-stored as an fp8 cache."""
-    vals = dequant_numpy(w)                       # [U, 128, 128]
-    codes = np.zeros(vals.shape, dtype=np.uint8)
-    flat_v = vals.reshape(-1)
-    uniq, inv = np.unique(flat_v, return_inverse=True)
-    uc = _e4m3_code_exact(uniq)
-    assert (uc >= 0).all(), "a value outside e4m3"
-    codes = uc[inv].reshape(vals.shape).astype(np.uint8)
-    return dataclasses.replace(w, cache="fp8", layout="fp8", pages_fp8=torch.from_numpy(codes),
-                               k_data_page_stride=W.FP8_PAGE_BYTES, k_scale_page_stride=0)
+from helpers import (clamp_garbage_scales, e4m3_code_exact as _e4m3_code_exact, e4m3_values_numpy,
+                     mxfp4_as_fp8, oracle_run, scores_numpy)
 
 
 def test_mxfp4_window_values_are_exact_e4m3():
@@ -67,10 +39,8 @@ def test_fp8_cache_scores_like_mxfp4_within_the_window(decode):
                             pool_pages=24, scale_lo=119, scale_hi=133)
     # the garbage tails (bytes 0 and 255) are not e4m3-exact: clear them to a
     # representable byte; they are past every live limit
-    ps = w.pages_scale.clone()
-    ps[(ps < 119) | (ps > 133)] = 127
-    w = dataclasses.replace(w, pages_scale=ps)
-    f = _mxfp4_as_fp8(w)
+    w = clamp_garbage_scales(w)
+    f = mxfp4_as_fp8(w)
     a, la = oracle_run(w, logits=True)
     b, lb = oracle_run(f, logits=True)
     np.testing.assert_array_equal(a, b)
