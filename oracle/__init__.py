@@ -98,6 +98,11 @@ def _load():
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
             ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int64,
             c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.orc_topk.restype = ctypes.c_int
+        lib.orc_topk.argtypes = [
+            ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
         lib.orc_live_pairs.restype = ctypes.c_int64
         lib.orc_live_pairs.argtypes = [
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -299,3 +304,33 @@ def write_index_k(*, k_bits: np.ndarray, slot_mapping, k_data: np.ndarray, k_sca
     return int(_load().orc_write_index_k(_ptr(k), n, int(k.shape[1]), _ptr(sm), _ptr(k_data),
                                          _ptr(k_scale), int(k_data_page_stride),
                                          int(k_scale_page_stride), int(num_pool_pages)))
+
+
+# ------------------------------------------------------------------- top-k --
+def topk(*, decode: bool, scores: np.ndarray, block_table: np.ndarray, block_table_stride: int, seq_lens,
+         max_seq_len: int, topk: int, local: int = 1, kv_groups: int = 1, cu_seqlens_q=None,
+         prefix_lens=None, rows=None):
+    """Top-k page selection after the scorer (the readings are stated in
+    ``mx4_oracle.c``).  ``scores``: float32 [rows_total, 64, P] block scores.
+    Returns (sel int32 [n_rows, kv_groups, topk] physical ids, -1 padded, in
+    ascending page order; count int32 [n_rows, kv_groups])."""
+    lib = _load()
+    sc = np.ascontiguousarray(scores, dtype=np.float32)
+    bt = _i32(block_table).reshape(-1)
+    sl = _i32(seq_lens)
+    cu = _i32(cu_seqlens_q)
+    pl = _i32(prefix_lens)
+    num_seqs = int(sl.shape[0])
+    if rows is None:
+        n_total = num_seqs if decode else int(cu[-1])
+        rows = np.arange(n_total, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    sel = np.empty((n, kv_groups, topk), dtype=np.int32)
+    cnt = np.empty((n, kv_groups), dtype=np.int32)
+    st = lib.orc_topk(1 if decode else 0, _ptr(sc), int(max_seq_len), _ptr(bt), int(block_table_stride),
+                      _ptr(cu), _ptr(sl), _ptr(pl), num_seqs, int(topk), int(local), int(kv_groups),
+                      rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(sel), _ptr(cnt))
+    if st != 0:
+        raise ValueError(f"oracle rejected the inputs (status {st})")
+    return sel, cnt

@@ -44,6 +44,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -484,4 +485,100 @@ int64_t orc_write_index_k(const uint16_t *k, int64_t num_tokens, int64_t k_row_s
         }
     }
     return bad;
+}
+
+/* ---------------------------------------------------- top-k page selection -- */
+/*
+ * The step after the scorer: each query row reads at most `topk` pages of its
+ * request, chosen from the block scores (ATOM #2770 "MiniMax-M3.1 MXFP4 sparse
+ * KV cache and index cache", "How it works": the index scores feed the
+ * selection and the emit of a page-level block table, one page a block for
+ * 128-token pages; the local block and the tail page are always selected; a
+ * row reads at most topk pages).  READINGS where the pages are silent:
+ *   - the 64 index heads form kv_groups contiguous groups; a page's value for
+ *     a group is the max of its block scores over the group's heads;
+ *   - live pages of a row are j < ceil(L/128) with L the scorer's live limit;
+ *     the last min(local, live) of them are always selected;
+ *   - the other topk - forced slots go to the live pages with the largest
+ *     values, ties to the lower page index;
+ *   - the emit lists the selected pages' physical ids (block_table) in
+ *     ascending page order, then -1 up to topk; count = number selected.
+ * Values are the fp32 block scores as given; every comparison is exact.
+ */
+static int orc_cmp_desc_value_asc_index(const void *pa, const void *pb)
+{
+    const double *a = (const double *)pa, *b = (const double *)pb;
+    if (a[0] > b[0]) return -1;
+    if (a[0] < b[0]) return 1;
+    return (a[1] < b[1]) ? -1 : (a[1] > b[1]);
+}
+
+/*
+ * scores [n_rows_total, 64, P] fp32 (P = ceil(max_seq_len/128)); rows as for
+ * orc_score.  sel [n_rows, kv_groups, topk] int32, count [n_rows, kv_groups].
+ * Returns 0, or -1 for a row outside every request, -3 for bad arguments.
+ */
+int orc_topk(int decode, const float *scores, int max_seq_len,
+             const int32_t *block_table, int64_t block_table_stride,
+             const int32_t *cu_seqlens_q, const int32_t *seq_lens, const int32_t *prefix_lens,
+             int num_seqs, int topk, int local, int kv_groups,
+             const int64_t *rows, int64_t n_rows, int32_t *sel, int32_t *count)
+{
+    const int64_t P = ((int64_t)max_seq_len + ORC_PAGE - 1) / ORC_PAGE;
+    int status = 0;
+    if (topk < 1 || local < 0 || local > topk || kv_groups < 1 || ORC_HEADS % kv_groups != 0 || !scores
+        || !sel || !count || !block_table || !seq_lens || (!decode && (!cu_seqlens_q || !prefix_lens)))
+        return -3;
+    const int hg = ORC_HEADS / kv_groups;
+    double *cand = (double *)malloc(sizeof(double) * 2 * (size_t)(P > 0 ? P : 1));
+    char *pick = (char *)malloc((size_t)(P > 0 ? P : 1));
+    if (!cand || !pick) {
+        free(cand);
+        free(pick);
+        return -3;
+    }
+    for (int64_t ri = 0; ri < n_rows; ++ri) {
+        int64_t r = rows[ri];
+        int b = decode ? (int)r : orc_request_of_row(cu_seqlens_q, num_seqs, r);
+        for (int g = 0; g < kv_groups; ++g) {
+            int32_t *out = sel + (ri * kv_groups + g) * (int64_t)topk;
+            int64_t L, nl, forced, n_c = 0, n_sel = 0;
+            for (int i = 0; i < topk; ++i)
+                out[i] = -1;
+            count[ri * kv_groups + g] = 0;
+            if (b < 0 || b >= num_seqs) {
+                status = -1;
+                continue;
+            }
+            L = orc_live_limit(decode, cu_seqlens_q, seq_lens, prefix_lens, b, r);
+            if (L > max_seq_len)
+                L = max_seq_len;
+            nl = L > 0 ? (L + ORC_PAGE - 1) / ORC_PAGE : 0;
+            forced = local < nl ? local : nl;
+            for (int64_t j = 0; j < nl; ++j)
+                pick[j] = (j >= nl - forced);
+            /* candidates: the live pages before the forced tail */
+            for (int64_t j = 0; j < nl - forced; ++j) {
+                double v = -INFINITY;
+                for (int h = g * hg; h < (g + 1) * hg; ++h) {
+                    double s = scores[(r * ORC_HEADS + h) * P + j];
+                    if (s > v)
+                        v = s;
+                }
+                cand[2 * n_c] = v;
+                cand[2 * n_c + 1] = (double)j;
+                ++n_c;
+            }
+            qsort(cand, (size_t)n_c, 2 * sizeof(double), orc_cmp_desc_value_asc_index);
+            for (int64_t i = 0; i < n_c && i < topk - forced; ++i)
+                pick[(int64_t)cand[2 * i + 1]] = 1;
+            for (int64_t j = 0; j < nl; ++j)
+                if (pick[j])
+                    out[n_sel++] = block_table[(int64_t)b * block_table_stride + j];
+            count[ri * kv_groups + g] = (int32_t)n_sel;
+        }
+    }
+    free(cand);
+    free(pick);
+    return status;
 }
