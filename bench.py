@@ -366,6 +366,60 @@ def secondary_writer(peaks, stream, steps=20):
     return res
 
 
+def secondary_topk(peaks, stream, topk=16, steps=50):
+    """Top-k page selection (topk pages, the last page forced, one head
+    group) on the block scores of the decode and prefill-long workloads,
+    timed as one replay of a graph of `steps` calls.  Algorithmic bytes: the
+    scores read (rows x 64 x P x 4) plus the selection written."""
+    import torch
+    import sparse_attention_mxfp4_gb300 as mx4
+    from sparse_attention_mxfp4_gb300 import harness
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    res = {}
+    for name in ("decode", "prefill-long"):
+        w = W.make_config(name)
+        case = harness.to_device(w)
+        with torch.cuda.stream(stream):
+            scores = case.run(stream=stream)
+            torch.cuda.synchronize()
+            sel = torch.empty((w.total_rows, 1, topk), dtype=torch.int32, device="cuda")
+            cnt = torch.empty((w.total_rows, 1), dtype=torch.int32, device="cuda")
+
+            def call():
+                if w.decode:
+                    mx4.mx4_index_topk_decode(scores, case.block_table, case.seq_lens, w.max_seq_len, topk,
+                                              sel=sel, count=cnt, stream=stream)
+                else:
+                    mx4.mx4_index_topk_prefill(scores, case.block_table, case.cu_seqlens_q, case.seq_lens,
+                                               case.prefix_lens, w.max_query_len, w.max_seq_len, topk, sel=sel,
+                                               count=cnt, stream=stream)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(steps):
+                    call()
+            g.replay()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / steps * 1e3
+        nbytes = scores.numel() * 4 + sel.numel() * 4 + cnt.numel() * 4
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us_per_call": round(us, 3), "steps": steps, "topk": topk, "local_pages": 1, "kv_groups": 1,
+                     "bytes_per_call": nbytes, "hbm_gbs_algorithmic": round(gbs, 1),
+                     "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                     "l2": "scores larger than L2" if scores.numel() * 4 > 129e6 else "scores fit in L2 (warm)"}
+        del case, scores, sel, cnt, g
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -468,6 +522,7 @@ def run_ours(args):
             names = [n for n in W.CONFIG_NAMES + W.FP8_CONFIG_NAMES if n != w.name]
             line["secondary"] = secondary_configs(names, peaks, stream)
             line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
+            line["secondary"]["topk"] = secondary_topk(peaks, stream)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()

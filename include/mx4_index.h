@@ -197,6 +197,40 @@ mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8
                                        int64_t block_table_stride, int64_t num_pool_pages);
 
 /*
+ * Top-k page selection, the step after the scorer ([P2] "How it works": the
+ * index scores feed the selection and the emit of a page-level block table,
+ * one page a block for 128-token pages, with the local and tail blocks always
+ * selected; a row reads at most topk pages).  READINGS where the sources are
+ * silent: the 64 index heads form kv_groups contiguous groups (64/kv_groups
+ * heads each); a page's value for a group is the max of its block scores over
+ * those heads; a row's live pages are j < ceil(L/128) with the scorer's live
+ * limit L; the last min(local_pages, live) live pages are always selected and
+ * the other topk - forced slots go to the largest values, ties to the lower
+ * page index.
+ *
+ *   scores      fp32 [total_rows, 64, ceil(max_seq_len/128)], the scorer's
+ *               block scores (device, 4-byte aligned).
+ *   sel         int32 [total_rows, kv_groups, topk]: physical page ids of the
+ *               selected pages in ascending page order, then -1.
+ *   count       int32 [total_rows, kv_groups]: pages selected.
+ *   topk >= 1, 0 <= local_pages <= topk, kv_groups divides 64,
+ *   ceil(max_seq_len/128) <= 16384 (MX4_ERR_UNSUPPORTED beyond).
+ * The request arguments (block_table, cu_seqlens_q, seq_lens, prefix_lens,
+ * max_query_len, num_seqs, block_table_stride) are those of the scorer call
+ * that produced `scores`.  Every row that exists is written; a call with no
+ * row returns MX4_OK at once.  Comparisons are exact (fp32 values, -0 equal
+ * to +0), so the selection is deterministic.
+ */
+mx4_status mx4_index_topk_prefill(const float *scores, const int32_t *block_table, const int32_t *cu_seqlens_q,
+                                  const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
+                                  int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
+                                  int32_t *count, void *stream, int num_seqs, int64_t block_table_stride);
+
+mx4_status mx4_index_topk_decode(const float *scores, const int32_t *block_table, const int32_t *seq_lens,
+                                 int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
+                                 int32_t *count, void *stream, int num_seqs, int64_t block_table_stride);
+
+/*
  * The query-preparation step on its own: n bf16 values (raw bits) rounded to
  * e4m3 bytes, nearest even, saturating to +-448, signed zero kept ([P1]
  * "Kernels": a bf16 query is rounded to e4m3 in-kernel; the scorers above do

@@ -44,6 +44,8 @@ EXPORTED_SYMBOLS = (
     "mx4_index_score_decode_fp8",
     "mx4_index_logits_prefill_fp8",
     "mx4_index_logits_decode_fp8",
+    "mx4_index_topk_prefill",
+    "mx4_index_topk_decode",
     "mx4_quantize_q_e4m3",
     "mx4_index_k_write",
     "mx4_index_get_device_status",
@@ -92,6 +94,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             f = getattr(lib, name)
             f.restype = i32
             f.argtypes = args
+        lib.mx4_index_topk_prefill.restype = i32
+        lib.mx4_index_topk_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, i64]
+        lib.mx4_index_topk_decode.restype = i32
+        lib.mx4_index_topk_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, i64]
         lib.mx4_quantize_q_e4m3.restype = i32
         lib.mx4_quantize_q_e4m3.argtypes = [vp, vp, i64, vp]
         lib.mx4_index_k_write.restype = i32
@@ -248,6 +254,53 @@ def mx4_index_logits_prefill_fp8(*args, **kwargs):
 
 def mx4_index_logits_decode_fp8(*args, **kwargs):
     return mx4_index_score_decode_fp8(*args, logits=True, **kwargs)
+
+
+def _topk_out(sel, count, rows, groups, topk, like):
+    import torch
+    if sel is None:
+        sel = torch.empty((rows, groups, topk), dtype=torch.int32, device=like.device)
+    if count is None:
+        count = torch.empty((rows, groups), dtype=torch.int32, device=like.device)
+    if sel.dtype != torch.int32 or tuple(sel.shape) != (rows, groups, topk) or not sel.is_contiguous():
+        raise ValueError(f"sel must be a contiguous int32 tensor of shape {(rows, groups, topk)}")
+    if count.dtype != torch.int32 or tuple(count.shape) != (rows, groups) or not count.is_contiguous():
+        raise ValueError(f"count must be a contiguous int32 tensor of shape {(rows, groups)}")
+    return sel, count
+
+
+def mx4_index_topk_prefill(scores, block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len, max_seq_len,
+                           topk, *, local_pages=1, kv_groups=1, sel=None, count=None, stream=None):
+    """Top-k page selection over prefill block scores ``scores`` [rows, 64, P]
+    (the scorer's output).  Returns (sel int32 [rows, kv_groups, topk],
+    count int32 [rows, kv_groups])."""
+    import torch
+    lib = load_library()
+    if scores.dtype != torch.float32 or scores.dim() != 3 or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous float32 [rows, 64, P] tensor")
+    sel, count = _topk_out(sel, count, scores.shape[0], kv_groups, topk, scores)
+    fn = "mx4_index_topk_prefill"
+    _check(fn, lib.mx4_index_topk_prefill(
+        _ptr(scores), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(prefix_lens), int(max_query_len),
+        int(max_seq_len), int(topk), int(local_pages), int(kv_groups), _ptr(sel), _ptr(count), _stream(stream),
+        int(seq_lens.shape[0]), _bt_stride(block_table)))
+    return sel, count
+
+
+def mx4_index_topk_decode(scores, block_table, seq_lens, max_seq_len, topk, *, local_pages=1, kv_groups=1,
+                          sel=None, count=None, stream=None):
+    """Top-k page selection over decode block scores (one row per request)."""
+    import torch
+    lib = load_library()
+    if scores.dtype != torch.float32 or scores.dim() != 3 or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous float32 [rows, 64, P] tensor")
+    sel, count = _topk_out(sel, count, scores.shape[0], kv_groups, topk, scores)
+    fn = "mx4_index_topk_decode"
+    _check(fn, lib.mx4_index_topk_decode(
+        _ptr(scores), _ptr(block_table), _ptr(seq_lens), int(max_seq_len), int(topk), int(local_pages),
+        int(kv_groups), _ptr(sel), _ptr(count), _stream(stream), int(seq_lens.shape[0]),
+        _bt_stride(block_table)))
+    return sel, count
 
 
 def mx4_quantize_q_e4m3(q_bf16, out=None, *, stream=None):

@@ -13,6 +13,7 @@
 
 #include "score_kernel.cuh"
 #include "writer_kernel.cuh"
+#include "topk_kernel.cuh"
 
 namespace {
 
@@ -42,6 +43,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
     int sm_count = 0;
+    bool topk_attr_set[2] = {false, false};
     bool smem_attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 
@@ -243,6 +245,73 @@ mx4_status launch(const Args &a)
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 
+template <bool kDecode>
+mx4_status topk_launch(const float *scores, const int32_t *block_table, const int32_t *cu_seqlens_q,
+                       const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len, int max_seq_len,
+                       int topk, int local_pages, int kv_groups, int32_t *sel, int32_t *count, void *stream,
+                       int num_seqs, int64_t block_table_stride)
+{
+    if (num_seqs < 0 || max_seq_len < 0 || (!kDecode && max_query_len < 0)) return MX4_ERR_INVALID_ARG;
+    if (topk < 1 || local_pages < 0 || local_pages > topk) return MX4_ERR_INVALID_ARG;
+    if (kv_groups < 1 || kv_groups > 64 || 64 % kv_groups != 0) return MX4_ERR_INVALID_ARG;
+    if (num_seqs == 0 || (!kDecode && max_query_len == 0)) return MX4_OK;       // no row exists
+    if (!scores || !block_table || !seq_lens || !sel || !count) return MX4_ERR_INVALID_ARG;
+    if (!kDecode && (!cu_seqlens_q || !prefix_lens)) return MX4_ERR_INVALID_ARG;
+    const int64_t P = (static_cast<int64_t>(max_seq_len) + mx4::kPage - 1) / mx4::kPage;
+    if (P > mx4::kTopkMaxPages) return MX4_ERR_UNSUPPORTED;
+    if (block_table_stride < P) return MX4_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || !aligned(sel, 4) || !aligned(count, 4) || !aligned(block_table, 4) ||
+        !aligned(seq_lens, 4))
+        return MX4_ERR_MISALIGNED;
+    if (!kDecode && (!aligned(cu_seqlens_q, 4) || !aligned(prefix_lens, 4))) return MX4_ERR_MISALIGNED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX4_ERR_CUDA;
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState &st = g_dev[dev];
+        if (st.sm_count == 0) {
+            int n = 0;
+            if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+                return MX4_ERR_CUDA;
+            st.sm_count = n;
+        }
+        if (!st.topk_attr_set[kDecode ? 1 : 0]) {
+            if (cudaFuncSetAttribute(mx4::mx4_topk_kernel<kDecode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     mx4::kTopkMaxPages * 4) != cudaSuccess)
+                return MX4_ERR_CUDA;
+            st.topk_attr_set[kDecode ? 1 : 0] = true;
+        }
+        sms = st.sm_count;
+    }
+    mx4::TopkParams p{};
+    p.scores = scores;
+    p.block_table = block_table;
+    p.cu_seqlens_q = cu_seqlens_q;
+    p.seq_lens = seq_lens;
+    p.prefix_lens = prefix_lens;
+    p.sel = sel;
+    p.count = count;
+    p.bt_stride = block_table_stride;
+    p.num_seqs = num_seqs;
+    p.rows_per_seq = kDecode ? 1 : max_query_len;
+    p.max_seq_len = max_seq_len;
+    p.num_pages = static_cast<int>(P);
+    p.topk = topk;
+    p.local = local_pages;
+    p.groups = kv_groups;
+    p.vec = aligned(scores, 16) && (P % 4) == 0;
+    p.num_items = static_cast<int64_t>(num_seqs) * p.rows_per_seq * kv_groups;
+    // one CTA per (row, group) item, at most 8 resident per SM, grid-stride
+    const int64_t grid = p.num_items < 8LL * sms ? p.num_items : 8LL * sms;
+    const size_t smem = static_cast<size_t>(P > 0 ? P : 1) * 4;
+    cudaGetLastError();
+    mx4::mx4_topk_kernel<kDecode><<<static_cast<unsigned>(grid), mx4::kTopkThreads, smem,
+                                    static_cast<cudaStream_t>(stream)>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -353,6 +422,23 @@ mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8
            num_pool_pages};
     a.fp8 = true;
     return launch<true, true, true>(a);
+}
+
+mx4_status mx4_index_topk_prefill(const float *scores, const int32_t *block_table, const int32_t *cu_seqlens_q,
+                                  const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
+                                  int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
+                                  int32_t *count, void *stream, int num_seqs, int64_t block_table_stride)
+{
+    return topk_launch<false>(scores, block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len, max_seq_len,
+                              topk, local_pages, kv_groups, sel, count, stream, num_seqs, block_table_stride);
+}
+
+mx4_status mx4_index_topk_decode(const float *scores, const int32_t *block_table, const int32_t *seq_lens,
+                                 int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
+                                 int32_t *count, void *stream, int num_seqs, int64_t block_table_stride)
+{
+    return topk_launch<true>(scores, block_table, nullptr, seq_lens, nullptr, 1, max_seq_len, topk, local_pages,
+                             kv_groups, sel, count, stream, num_seqs, block_table_stride);
 }
 
 mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t n, void *stream)

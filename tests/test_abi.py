@@ -153,6 +153,26 @@ def test_fp8_rejections(lib, kw, status):
     assert got_d == status
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(local=5, k=4), mx4.MX4_ERR_INVALID_ARG),
+    (dict(local=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(groups=3), mx4.MX4_ERR_INVALID_ARG),
+    (dict(groups=128), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sc=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(sel=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(ms=16384 * 128 + 1, bts=16385), mx4.MX4_ERR_UNSUPPORTED),
+    (dict(bts=3), mx4.MX4_ERR_INVALID_ARG),                     # narrow block table
+    (dict(sc=A + 2), mx4.MX4_ERR_MISALIGNED),
+    (dict(B=0, sc=None), mx4.MX4_OK),                            # no row
+])
+def test_topk_rejections(lib, kw, status):
+    a = dict(sc=A, bt=A, sl=A, ms=512, k=4, local=1, groups=1, sel=A, cnt=A, B=1, bts=4)
+    a.update(kw)
+    assert lib.mx4_index_topk_decode(a["sc"], a["bt"], a["sl"], a["ms"], a["k"], a["local"], a["groups"],
+                                     a["sel"], a["cnt"], None, a["B"], a["bts"]) == status
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     import importlib
     missing = str(tmp_path / "nope.so")
