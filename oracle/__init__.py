@@ -103,6 +103,13 @@ def _load():
             ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+        lib.orc_pa_decode.restype = ctypes.c_int
+        lib.orc_pa_decode.argtypes = [
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_double, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_int]
         lib.orc_live_pairs.restype = ctypes.c_int64
         lib.orc_live_pairs.argtypes = [
             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -334,3 +341,30 @@ def topk(*, decode: bool, scores: np.ndarray, block_table: np.ndarray, block_tab
     if st != 0:
         raise ValueError(f"oracle rejected the inputs (status {st})")
     return sel, cnt
+
+
+# ------------------------------------------------ sparse paged attention --
+def pa_decode(*, q: np.ndarray, k_data, k_scale, kd_ps: int, kd_hs: int, ks_ps: int, ks_hs: int,
+              v_data, v_scale, vd_ps: int, vd_hs: int, vs_ps: int, vs_hs: int, block_table: np.ndarray,
+              context_lens, softmax_scale: float, num_pool_pages: int = 0, num_threads: int = 0) -> np.ndarray:
+    """Decode attention over each row's selected MXFP4 K/V pages, fp64 (the
+    definition and readings are in ``mx4_oracle.c``).  ``q``: e4m3 bytes
+    [rows, kv_heads, groups, 128]; ``block_table``: int32 [rows, kv_heads,
+    width]; ``context_lens``: int32 [rows, kv_heads].  Returns float64
+    [rows, kv_heads, groups, 128]."""
+    lib = _load()
+    q = _u8(q)
+    assert q.ndim == 4 and q.shape[3] == DIM
+    n, kvh, g, _ = q.shape
+    bt = _i32(block_table)
+    assert bt.ndim == 3 and bt.shape[:2] == (n, kvh)
+    cl = _i32(context_lens).reshape(-1)
+    out = np.empty((n, kvh, g, DIM), dtype=np.float64)
+    st = lib.orc_pa_decode(_ptr(q), n, kvh, g,
+                           _ptr(_u8(k_data).reshape(-1)), _ptr(_u8(k_scale).reshape(-1)), kd_ps, kd_hs, ks_ps, ks_hs,
+                           _ptr(_u8(v_data).reshape(-1)), _ptr(_u8(v_scale).reshape(-1)), vd_ps, vd_hs, vs_ps, vs_hs,
+                           _ptr(bt), int(bt.shape[2]), _ptr(cl), float(softmax_scale), int(num_pool_pages),
+                           _ptr(out), int(num_threads))
+    if st != 0:
+        raise ValueError(f"oracle rejected the inputs (status {st})")
+    return out

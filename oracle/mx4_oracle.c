@@ -582,3 +582,103 @@ int orc_topk(int decode, const float *scores, int max_seq_len,
     free(pick);
     return status;
 }
+
+/* -------------------------------------- sparse paged-attention decode -- */
+/*
+ * Decode attention over the pages a row selected, with K and V in MXFP4
+ * (aiter pa_decode MXFP4, as described in ATOM #2770 "MiniMax-M3.1 MXFP4
+ * sparse KV cache and index cache", commit "pa_decode MXFP4": K and V are
+ * e2m1 data plus one e8m0 byte per 32 elements along head_dim, read through
+ * data/scale views with their own page and head strides; the fp8 query is
+ * used as stored; invalid tokens get a -inf score; (token, kv head) pairs are
+ * folded into rows that each read at most topk pages).  Definition, per row
+ * r and query head h of the row's group of G heads:
+ *     s[t]   = softmax_scale * sum_d q[r,h,d] * K[t,d]      (t valid)
+ *     out    = sum_t softmax(s)[t] * V[t,:]
+ * READINGS: head_dim 128 for K and V; the row's tokens are those of its
+ * block-table pages in list order, the first context_len of them valid (the
+ * selection lists pages in ascending order with the tail page last);
+ * page p of kv head k holds token i's K codes at k_data + p*kd_ps + k*kd_hs +
+ * i*64 and scales at k_scale + p*ks_ps + k*ks_hs + i*4 (V the same); a row
+ * with no valid token outputs zeros.  fp64 here; the stored output is bf16.
+ */
+int orc_pa_decode(const uint8_t *q, int64_t n_rows, int kv_heads, int groups,
+                  const uint8_t *k_data, const uint8_t *k_scale, int64_t kd_ps, int64_t kd_hs,
+                  int64_t ks_ps, int64_t ks_hs,
+                  const uint8_t *v_data, const uint8_t *v_scale, int64_t vd_ps, int64_t vd_hs,
+                  int64_t vs_ps, int64_t vs_hs,
+                  const int32_t *block_table, int64_t bt_stride, const int32_t *context_lens,
+                  double softmax_scale, int64_t num_pool_pages, double *out, int num_threads)
+{
+    int status = 0;
+    if (n_rows < 0 || kv_heads < 1 || groups < 1 || !q || !k_data || !k_scale || !v_data || !v_scale
+        || !block_table || !context_lens || !out)
+        return -3;
+#ifdef _OPENMP
+    if (num_threads > 0)
+        omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        for (int kh = 0; kh < kv_heads; ++kh) {
+            const int64_t row = r * kv_heads + kh;
+            const int64_t ctx = context_lens[row];
+            double *o = out + row * groups * ORC_DIM;
+            for (int64_t i = 0; i < (int64_t)groups * ORC_DIM; ++i)
+                o[i] = 0.0;
+            if (ctx <= 0)
+                continue;
+            double *s = (double *)malloc(sizeof(double) * (size_t)ctx * (size_t)groups);
+            double kv[ORC_DIM];
+            if (!s) {
+#pragma omp atomic write
+                status = -3;
+                continue;
+            }
+            for (int64_t t = 0; t < ctx; ++t) {
+                int64_t p = block_table[row * bt_stride + t / ORC_PAGE];
+                int i = (int)(t % ORC_PAGE);
+                if (p < 0 || (num_pool_pages > 0 && p >= num_pool_pages)) {
+#pragma omp atomic write
+                    status = -2;
+                    p = 0;
+                }
+                for (int d = 0; d < ORC_DIM; ++d)
+                    kv[d] = orc_k_value(k_data + kh * kd_hs, k_scale + kh * ks_hs, kd_ps, ks_ps, p, i, d);
+                for (int h = 0; h < groups; ++h) {
+                    double dot = 0.0;
+                    for (int d = 0; d < ORC_DIM; ++d)
+                        dot += orc_e4m3_value(q[(row * groups + h) * ORC_DIM + d]) * kv[d];
+                    s[t * groups + h] = softmax_scale * dot;
+                }
+            }
+            for (int h = 0; h < groups; ++h) {
+                double m = -INFINITY, sum = 0.0;
+                for (int64_t t = 0; t < ctx; ++t)
+                    if (s[t * groups + h] > m)
+                        m = s[t * groups + h];
+                for (int64_t t = 0; t < ctx; ++t) {
+                    s[t * groups + h] = exp(s[t * groups + h] - m);
+                    sum += s[t * groups + h];
+                }
+                for (int64_t t = 0; t < ctx; ++t)
+                    s[t * groups + h] /= sum;
+            }
+            for (int64_t t = 0; t < ctx; ++t) {
+                int64_t p = block_table[row * bt_stride + t / ORC_PAGE];
+                int i = (int)(t % ORC_PAGE);
+                if (p < 0 || (num_pool_pages > 0 && p >= num_pool_pages))
+                    p = 0;
+                for (int d = 0; d < ORC_DIM; ++d)
+                    kv[d] = orc_k_value(v_data + kh * vd_hs, v_scale + kh * vs_hs, vd_ps, vs_ps, p, i, d);
+                for (int h = 0; h < groups; ++h)
+                    for (int d = 0; d < ORC_DIM; ++d)
+                        o[h * ORC_DIM + d] += s[t * groups + h] * kv[d];
+            }
+            free(s);
+        }
+    }
+    return status;
+}

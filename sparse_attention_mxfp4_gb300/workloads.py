@@ -535,3 +535,109 @@ def make_write_config(name: str, seed: Optional[int] = None) -> WriteCase:
                                description="32768 keys at positions 100000..132767 of one request, "
                                            "1200-page pool")
     raise KeyError(name)
+
+
+# ----------------------------------------------- sparse paged attention --
+@dataclasses.dataclass
+class AttnCase:
+    """Decode attention over each row's selected pages.
+
+    K and V pools are [pool_pages, kv_heads, 8704] uint8: one MXFP4 page per
+    (page, kv head), codes at byte 0 and scales at byte 8192 of each page
+    (ATOM #2770 "How it works", item "Pool").  ``block_table`` [rows,
+    kv_heads, width] lists each row's pages in order (-1 padded);
+    ``context_lens`` [rows, kv_heads] counts its valid tokens (a prefix of the
+    list); ``q`` is e4m3 bytes [rows, kv_heads, groups, 128]."""
+    name: str
+    q: torch.Tensor
+    k_pool: torch.Tensor
+    v_pool: torch.Tensor
+    block_table: torch.Tensor
+    context_lens: torch.Tensor
+    softmax_scale: float = SM_SCALE
+    description: str = ""
+
+    @property
+    def rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def kv_heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def groups(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
+    def num_pool_pages(self) -> int:
+        return int(self.k_pool.shape[0])
+
+    def views(self, pool):
+        """(data, scale, data page stride, data head stride, scale page
+        stride, scale head stride) of a [pages, kv_heads, 8704] pool (flat
+        uint8 views starting at page 0 of each)."""
+        flat = pool.reshape(-1)
+        ps = self.kv_heads * PAGE_BYTES
+        return flat, flat[DATA_BYTES:], ps, PAGE_BYTES, ps, PAGE_BYTES
+
+
+def make_attn_case(name, *, seed, rows, kv_heads=1, groups=16, width=16, pool_pages=None, ctx=None,
+                   scale_lo=122, scale_hi=127, description="") -> AttnCase:
+    """Seeded attention case: each (row, kv head) selects ``width`` distinct
+    pool pages (a seeded draw); ``ctx`` gives each row's valid tokens (default:
+    a seeded length in ((width-1)*128, width*128], so the last page is partial
+    most of the time); bytes past a row's context in its last page are garbage
+    (e8m0 0 and 255 included).  Q: N(0, 1) cast to float8_e4m3fn by torch."""
+    g = _gen(seed)
+    pool_pages = pool_pages or max(2 * width * rows * kv_heads, 64)
+    q = torch.randn((rows, kv_heads, groups, DIM), generator=g).clamp_(-448, 448)
+    q = q.to(torch.float8_e4m3fn).view(torch.uint8)
+    pools = []
+    for _ in range(2):
+        data = torch.randint(0, 256, (pool_pages, kv_heads, DATA_BYTES), generator=g, dtype=torch.uint8)
+        scale = torch.randint(scale_lo, scale_hi + 1, (pool_pages, kv_heads, SCALE_BYTES), generator=g,
+                              dtype=torch.uint8)
+        pools.append(torch.cat([data, scale], dim=2).contiguous())
+    bt = torch.full((rows, kv_heads, width), -1, dtype=torch.int32)
+    cl = torch.zeros((rows, kv_heads), dtype=torch.int32)
+    # distinct pages across the whole case (a page belongs to one row)
+    assert pool_pages >= rows * kv_heads * width
+    ids = torch.randperm(pool_pages, generator=g)[: rows * kv_heads * width].to(torch.int32)
+    for r in range(rows):
+        for h in range(kv_heads):
+            if ctx is None:
+                c = int(torch.randint((width - 1) * PAGE + 1, width * PAGE + 1, (1,), generator=g))
+            else:
+                c = int(ctx[r] if hasattr(ctx, "__len__") else ctx)
+            npg = (c + PAGE - 1) // PAGE
+            k0 = (r * kv_heads + h) * width
+            bt[r, h, :npg] = ids[k0:k0 + npg]
+            cl[r, h] = c
+            if c % PAGE:
+                # garbage past the context inside the last page, K and V
+                p = int(bt[r, h, npg - 1])
+                i0 = c % PAGE
+                for pool in pools:
+                    pool[p, h, i0 * 64:DATA_BYTES] = torch.randint(0, 256, (DATA_BYTES - i0 * 64,), generator=g,
+                                                                   dtype=torch.uint8)
+                    sc = torch.randint(0, 256, (SCALE_BYTES - i0 * 4,), generator=g, dtype=torch.uint8)
+                    sc[0] = 0
+                    sc[-1] = 255
+                    pool[p, h, DATA_BYTES + i0 * 4:] = sc
+    return AttnCase(name=name, q=q, k_pool=pools[0], v_pool=pools[1], block_table=bt, context_lens=cl,
+                    description=description)
+
+
+ATTN_CONFIG_NAMES = ("pa-decode",)
+
+
+def make_attn_config(name: str, seed: Optional[int] = None) -> AttnCase:
+    """Sparse decode attention of the decode workload's shape: 64 requests,
+    one KV head with 16 query heads, 16 selected pages (2,048 tokens) each."""
+    if name == "pa-decode":
+        return make_attn_case(name, seed=20 if seed is None else seed, rows=64, kv_heads=1, groups=16, width=16,
+                              pool_pages=8192,
+                              description="64 rows x 1 KV head x 16 query heads, 16 selected pages of an "
+                                          "8192-page pool (K+V pools 143 MB), context 1921..2048 tokens")
+    raise KeyError(name)
