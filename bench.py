@@ -420,6 +420,49 @@ def secondary_topk(peaks, stream, topk=16, steps=50):
     return res
 
 
+def secondary_attn(peaks, stream, steps=50):
+    """Sparse paged-attention decode on the pa-decode workload (64 rows x 16
+    query heads over 16 selected MXFP4 pages of K and V), timed as one replay
+    of a graph of `steps` calls.  Algorithmic bytes: the listed K and V pages
+    (8704 B each per KV head) + Q + the bf16 output."""
+    import torch
+    import sparse_attention_mxfp4_gb300 as mx4
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    c = W.make_attn_config("pa-decode")
+    q, kp, vp = c.q.cuda(), c.k_pool.cuda(), c.v_pool.cuda()
+    bt, cl = c.block_table.cuda(), c.context_lens.cuda()
+    out = torch.empty((c.rows, c.kv_heads, c.groups, W.DIM), dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            mx4.mx4_sparse_pa_decode(q, kp, vp, bt, cl, c.softmax_scale, out, stream=stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(steps):
+                mx4.mx4_sparse_pa_decode(q, kp, vp, bt, cl, c.softmax_scale, out, stream=stream)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps * 1e3
+    ctx = c.context_lens.to(torch.int64)
+    pages = int(((ctx + 127) // 128).sum())
+    nbytes = pages * 2 * W.PAGE_BYTES + q.numel() + out.numel() * 2
+    flops = int(ctx.sum()) * c.groups * W.DIM * 2 * 2
+    res = {"us_per_call": round(us, 3), "steps": steps, "rows": c.rows, "kv_heads": c.kv_heads,
+           "groups": c.groups, "pages_per_row": int(c.block_table.shape[2]), "bytes_per_call": nbytes,
+           "hbm_gbs_algorithmic": round(nbytes / (us * 1e-6) / 1e9, 1),
+           "frac_of_hbm_peak": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+           "tflops": round(flops / (us * 1e-6) / 1e12, 2), "description": c.description}
+    del q, kp, vp, bt, cl, out, g
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -523,6 +566,7 @@ def run_ours(args):
             line["secondary"] = secondary_configs(names, peaks, stream)
             line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
             line["secondary"]["topk"] = secondary_topk(peaks, stream)
+            line["secondary"]["sparse_pa_decode"] = secondary_attn(peaks, stream)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()

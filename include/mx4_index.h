@@ -80,7 +80,8 @@ typedef enum {
  * producer waiting for a free smem stage, 1 = MMA waiting for the query tile,
  * 2 = MMA waiting for a page's bytes, 3 = MMA waiting for a free
  * accumulator, 4 = epilogue waiting for a free query buffer, 5 = epilogue
- * waiting for an accumulator.  Diagnostic only. */
+ * waiting for an accumulator; attention: 6 = copy issue, 7 = MMA issue,
+ * 8 = softmax warps.  Diagnostic only. */
 
 /*
  * Block scores for ragged prefill (causal) rows.  [P1] "Kernels":
@@ -229,6 +230,49 @@ mx4_status mx4_index_topk_prefill(const float *scores, const int32_t *block_tabl
 mx4_status mx4_index_topk_decode(const float *scores, const int32_t *block_table, const int32_t *seq_lens,
                                  int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
                                  int32_t *count, void *stream, int num_seqs, int64_t block_table_stride);
+
+/*
+ * Sparse paged-attention decode over MXFP4 K and V: each row (a decode token
+ * and one KV head) attends over the pages its block table lists.  [P2] "How
+ * it works" (sparse attention: (token, kv head) folded into rows, each row
+ * reads at most topk pages) and the pa_decode MXFP4 commit message (K and V
+ * as e2m1 + one e8m0 byte per 32 elements along head_dim through data/scale
+ * views with page and head strides; the e4m3 query used as stored; invalid
+ * tokens get a -inf score and a zero V; V widened to bf16, P bf16):
+ *     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V
+ * over the row's valid tokens: the first context_lens[row] tokens of its
+ * listed pages, in list order (the top-k emit lists pages in ascending order
+ * with the partial tail page last).
+ *
+ *   q              e4m3 bytes [num_rows, kv_heads, groups, 128], 16-byte
+ *                  aligned; groups <= 16.
+ *   K / V views    page p of KV head k: codes at data + p * page_stride +
+ *                  k * head_stride (128 tokens x 64 B), scales at scale +
+ *                  p * page_stride + k * head_stride (128 tokens x 4 B).
+ *                  K codes 32-byte aligned with strides multiple of 32; K
+ *                  scales, V codes and V scales 16-byte aligned with strides
+ *                  multiple of 16; head strides >= 8192 / 512, page strides
+ *                  >= kv_heads * head stride.  A [pages, kv_heads, 8704] pool
+ *                  has data = pool, scale = pool + 8192, page stride
+ *                  kv_heads * 8704, head stride 8704 for both.
+ *   block_table    int32 [num_rows, kv_heads, block_table_width] page ids;
+ *                  entries past ceil(context_len / 128) are never read;
+ *                  block_table_width <= 24 (MX4_ERR_UNSUPPORTED beyond).
+ *   context_lens   int32 [num_rows, kv_heads]; clamped to [0, width*128].
+ *   out            bf16 [num_rows, kv_heads, groups, 128]; a row with no
+ *                  valid token is written with zeros.
+ * A listed page id outside [0, num_pool_pages) reads page 0 and sets
+ * MX4_DEV_BAD_PAGE.  Pointers are caller-owned device memory; no allocation;
+ * num_rows == 0 returns MX4_OK at once.
+ */
+mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads, int groups,
+                                const uint8_t *k_data, const uint8_t *k_scale, int64_t k_data_page_stride,
+                                int64_t k_data_head_stride, int64_t k_scale_page_stride,
+                                int64_t k_scale_head_stride, const uint8_t *v_data, const uint8_t *v_scale,
+                                int64_t v_data_page_stride, int64_t v_data_head_stride,
+                                int64_t v_scale_page_stride, int64_t v_scale_head_stride,
+                                const int32_t *block_table, int block_table_width, const int32_t *context_lens,
+                                float softmax_scale, void *out, int64_t num_pool_pages, void *stream);
 
 /*
  * The query-preparation step on its own: n bf16 values (raw bits) rounded to

@@ -46,6 +46,7 @@ EXPORTED_SYMBOLS = (
     "mx4_index_logits_decode_fp8",
     "mx4_index_topk_prefill",
     "mx4_index_topk_decode",
+    "mx4_sparse_pa_decode",
     "mx4_quantize_q_e4m3",
     "mx4_index_k_write",
     "mx4_index_get_device_status",
@@ -98,6 +99,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.mx4_index_topk_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, i64]
         lib.mx4_index_topk_decode.restype = i32
         lib.mx4_index_topk_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, i64]
+        lib.mx4_sparse_pa_decode.restype = i32
+        lib.mx4_sparse_pa_decode.argtypes = [vp, i64, i32, i32, vp, vp, i64, i64, i64, i64, vp, vp, i64, i64, i64,
+                                             i64, vp, i32, vp, f32, vp, i64, vp]
         lib.mx4_quantize_q_e4m3.restype = i32
         lib.mx4_quantize_q_e4m3.argtypes = [vp, vp, i64, vp]
         lib.mx4_index_k_write.restype = i32
@@ -301,6 +305,41 @@ def mx4_index_topk_decode(scores, block_table, seq_lens, max_seq_len, topk, *, l
         int(kv_groups), _ptr(sel), _ptr(count), _stream(stream), int(seq_lens.shape[0]),
         _bt_stride(block_table)))
     return sel, count
+
+
+def mx4_sparse_pa_decode(q, k_pool, v_pool, block_table, context_lens, softmax_scale, out=None, *,
+                         stream=None):
+    """Sparse paged-attention decode over MXFP4 K/V pools [pages, kv_heads,
+    8704] (codes at byte 0, scales at byte 8192 of each page).  ``q``: e4m3
+    bytes [rows, kv_heads, groups, 128]; ``block_table``: int32 [rows,
+    kv_heads, width]; ``context_lens``: int32 [rows, kv_heads].  Returns bf16
+    [rows, kv_heads, groups, 128]."""
+    import torch
+    lib = load_library()
+    if q.dtype not in (torch.uint8, torch.float8_e4m3fn) or q.dim() != 4 or q.shape[3] != DIM \
+            or not q.is_contiguous():
+        raise ValueError("q must be a contiguous e4m3 [rows, kv_heads, groups, 128] tensor")
+    rows, kvh, groups, _ = q.shape
+    for pool in (k_pool, v_pool):
+        if pool.dtype != torch.uint8 or pool.dim() != 3 or pool.shape[1] != kvh or pool.shape[2] != 8704 \
+                or not pool.is_contiguous():
+            raise ValueError("pools must be contiguous uint8 [pages, kv_heads, 8704] tensors")
+    if v_pool.shape[0] != k_pool.shape[0]:
+        raise ValueError("k_pool and v_pool must hold the same number of pages")
+    if block_table.dtype != torch.int32 or block_table.dim() != 3 or not block_table.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 [rows, kv_heads, width] tensor")
+    if context_lens.dtype != torch.int32 or not context_lens.is_contiguous():
+        raise ValueError("context_lens must be a contiguous int32 [rows, kv_heads] tensor")
+    if out is None:
+        out = torch.empty((rows, kvh, groups, DIM), dtype=torch.bfloat16, device=q.device)
+    ps = kvh * 8704
+    kd = k_pool.data_ptr()
+    vd = v_pool.data_ptr()
+    _check("mx4_sparse_pa_decode", lib.mx4_sparse_pa_decode(
+        _ptr(q), rows, kvh, groups, kd, kd + 8192, ps, 8704, ps, 8704, vd, vd + 8192, ps, 8704, ps, 8704,
+        _ptr(block_table), int(block_table.shape[2]), _ptr(context_lens), float(softmax_scale), _ptr(out),
+        int(k_pool.shape[0]), _stream(stream)))
+    return out
 
 
 def mx4_quantize_q_e4m3(q_bf16, out=None, *, stream=None):

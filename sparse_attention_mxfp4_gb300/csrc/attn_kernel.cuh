@@ -1,0 +1,505 @@
+// attn_kernel.cuh -- sparse paged-attention decode over MXFP4 K and V.
+//
+// Each row (a decode token and one KV head) attends over the pages it
+// selected (ATOM #2770 "MiniMax-M3.1 MXFP4 sparse KV cache and index cache",
+// commit "pa_decode MXFP4": K and V are e2m1 data plus one e8m0 byte per 32
+// elements along head_dim; the e4m3 query is used as stored; QK is a mixed
+// fp4 x fp8 block-scaled product; V is widened to bf16 exactly and P stays
+// bf16; invalid tokens get a -inf score and a zero V, so tail garbage cannot
+// leak):
+//     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V.
+//
+// One CTA per row (320 threads), two passes over the row's pages:
+//   warp 4   producer: per page, the K codes (4-D token-permuting TMA view
+//            plus a KV-head dimension, the scorer's smem form) and K scales,
+//            then the V codes and scales as two plain bulk copies (natural
+//            token order: V is not an MMA operand in MXFP4 form).
+//   warp 5   MMA: QK per page with tcgen05.mma kind::mxf8f6f4 block_scale,
+//            A = the K page (M = 128 tokens, e2m1, its e8m0 scales copied to a
+//            per-page TMEM slot), B = the Q tile (N = 16 heads, e4m3, unit
+//            scales), D = the page's 16 score columns in TMEM (all pages kept).
+//            Then PV per page with kind::f16: A = V^T (M = 128 head dims,
+//            K = 128 tokens, bf16), B = P^T (N = 16 heads, bf16), D = the
+//            output accumulator (16 columns), accumulated over pages.
+//   warps 0-3 softmax: thread m reads TMEM lane m (token 4(m%32)+m/32 of each
+//            page), takes the per-head max over valid tokens (shuffles across
+//            lanes, shared memory across warps), then per page writes P^T
+//            (bf16, natural token order), widens tokens 0..63 of the page's V
+//            into V^T (bf16) for the PV MMA, and sums the bf16 P; finally
+//            out = acc / sum, stored as bf16.
+//   warps 6-9 widen tokens 64..127 of each page's V.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "score_kernel.cuh"
+
+namespace mx4 {
+
+constexpr int kAttnThreads = 320;       // warps 0-3 softmax, 4 copies, 5 MMA, 6-9 V widening
+constexpr int kAttnWidenWarps = 8;      // warps 0-3 and 6-9 share the V widening
+constexpr int kAttnMaxPages = 24;       // pages a row may list: every page's scores stay in TMEM
+constexpr int kAttnN = 16;              // query heads per KV head (fewer are zero-padded)
+constexpr int kAttnKStages = 4;
+constexpr int kAttnVStages = 3;
+constexpr uint32_t kAttnSCol = 0;                                    // page j: 16 columns at 16 j
+constexpr uint32_t kAttnOutCol = kAttnMaxPages * kAttnN;              // 384
+constexpr uint32_t kAttnSfaCol = kAttnOutCol + kAttnN;                // 400: 4 per page
+constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnMaxPages;     // 496
+static_assert(kAttnSfbCol + 4 <= 512, "attention TMEM budget");
+
+enum AttnSite : uint32_t { kSiteAttnProducer = 6, kSiteAttnMma = 7, kSiteAttnEpi = 8 };
+
+struct AttnParams {
+    const uint8_t *q;                 // e4m3 [rows, kv_heads, groups, 128]
+    const uint8_t *v_data;
+    const uint8_t *v_scale;
+    int64_t vd_ps, vd_hs, vs_ps, vs_hs;
+    const int32_t *block_table;       // [rows, kv_heads, width]
+    const int32_t *context_lens;      // [rows, kv_heads]
+    __nv_bfloat16 *out;               // [rows, kv_heads, groups, 128]
+    int64_t num_pool_pages;
+    int kv_heads;
+    int groups;
+    int width;
+    float softmax_scale;
+};
+
+struct AttnSmem {
+    static constexpr uint32_t kK = 0;                                    // K pages, 16 KB each
+    static constexpr uint32_t kKs = kK + kAttnKStages * kTileBytes;      // K scales
+    static constexpr uint32_t kV = kKs + kAttnKStages * kScaleBytes;     // V codes, natural order
+    static constexpr uint32_t kVs = kV + kAttnVStages * kDataBytes;      // V scales
+    static constexpr uint32_t kVt = ((kVs + kAttnVStages * kScaleBytes) + 1023) & ~1023u;   // 2 x 32 KB
+    static constexpr uint32_t kPt = kVt + 2 * 32768;                     // 2 x 4 KB
+    static constexpr uint32_t kQ = kPt + 2 * 4096;                       // 16 x 128 B
+    static constexpr uint32_t kUnit = kQ + 2048;                         // 512 B of 0x7F
+    static constexpr uint32_t kRed = kUnit + 512;                        // 4 warps x 16 floats
+    static constexpr uint32_t kLut = kRed + 4 * 16 * 4;                  // 256 x bf16x2: code pair -> values
+    static constexpr uint32_t kBars = kLut + 256 * 4;
+    // kfull[4] kempty[4] vfull[3] vempty[3] qready qk_done pvready[2] pvfree[2] pv_done
+    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 2 + 4 + 1;
+    static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
+    static constexpr uint32_t kAbort = kTmemSlot + 4;
+    static constexpr uint32_t kPid = kAbort + 4;                         // page ids of the row
+    static constexpr uint32_t kEnd = kPid + 4 * kAttnMaxPages;
+    static constexpr uint32_t kAlloc = kEnd + 1024;
+};
+static_assert(AttnSmem::kAlloc <= 227 * 1024, "attention shared memory budget");
+
+// Instruction descriptors.  QK (kind::mxf8f6f4): A = E2M1 (5, bits 7..9),
+// B = E4M3 (0, bits 10..12), N = 16, M = 128, UE8M0 scales (bit 23), scale
+// ids of K block k in bits 4..5 (B) and 29..30 (A).  PV (kind::f16): F32
+// accumulator (1, bits 4..5), A = B = BF16 (1), both K-major, N = 16, M = 128.
+__device__ __forceinline__ uint32_t attn_idesc_qk(uint32_t k)
+{
+    constexpr uint32_t kBase = (5u << 7) | (0u << 10) | ((16u >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
+    return kBase | (k << 4) | (k << 29);
+}
+constexpr uint32_t kAttnIdescPv = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+
+// Byte offset of element (row, k) of a K-major bf16 operand tile with
+// 128-byte swizzling: 64 elements (128 B) per row and atom, 8-row atoms of
+// 1 KB, `rows` rows per K-atom (K-atoms of 64 elements follow each other).
+__device__ __forceinline__ uint32_t sw128_bf16_offset(int row, int k, int rows)
+{
+    const int ka = k >> 6, kk = k & 63;
+    const uint32_t chunk = static_cast<uint32_t>(kk >> 3) ^ static_cast<uint32_t>(row & 7);
+    return static_cast<uint32_t>(ka) * rows * 128u + static_cast<uint32_t>(row >> 3) * 1024u +
+           static_cast<uint32_t>(row & 7) * 128u + chunk * 16u + static_cast<uint32_t>(kk & 7) * 2u;
+}
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// e2m1 code -> value (format definition: magnitudes 0, 0.5, 1, 1.5, 2, 3,
+// 4, 6, bit 3 the sign); twice the magnitudes are the bytes of one constant.
+__device__ __forceinline__ float e2m1_value(uint32_t code)
+{
+    const uint32_t twice = static_cast<uint32_t>((0x0C08060403020100ull >> (8u * (code & 7u))) & 0xFFu);
+    const float m = static_cast<float>(twice) * 0.5f;
+    return (code & 8u) ? -m : m;
+}
+
+// Widen tokens 16 wi .. 16 wi + 15 of a V page (natural layout in smem: 64
+// code bytes and 4 scale bytes per token) into the bf16 V^T operand tile.
+// Lane l takes the token pair t0 = 16 wi + 2 (l % 8), t0 + 1 and head dims
+// 32 (l / 8) .. +32 (one scale group): per head dim the two tokens' codes form
+// one byte that indexes `lut` (both unscaled values as bf16), one packed bf16
+// multiply applies the two tokens' scales (2^(b-127) is bf16 bits b << 7,
+// exact), tokens at or past `valid` are zeroed, and the pair lands in one
+// 4-byte store (adjacent K positions of one V^T row).
+__device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc, uint8_t *vt,
+                                           const __nv_bfloat162 *lut, int wi, int lane, int valid)
+{
+    const int t0 = 16 * wi + 2 * (lane & 7);
+    const int qd = lane >> 3;
+    const uint4 a = *reinterpret_cast<const uint4 *>(vc + t0 * 64 + qd * 16);
+    const uint4 c = *reinterpret_cast<const uint4 *>(vc + (t0 + 1) * 64 + qd * 16);
+    const uint32_t sbits = (static_cast<uint32_t>(vsc[t0 * 4 + qd]) << 7) |
+                           (static_cast<uint32_t>(vsc[(t0 + 1) * 4 + qd]) << 23);
+    const __nv_bfloat162 sc = *reinterpret_cast<const __nv_bfloat162 *>(&sbits);
+    const uint32_t keep = (t0 < valid ? 0x0000FFFFu : 0u) | (t0 + 1 < valid ? 0xFFFF0000u : 0u);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
+    const uint32_t cch = static_cast<uint32_t>((t0 & 63) >> 3);    // the pair's 16-byte chunk in a row
+    uint8_t *base = vt + (t0 >> 6) * 16384 + (t0 & 7) * 2;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        // byte i of lo: codes of head dim 2i of both tokens; of hi: dim 2i+1
+        const uint32_t lo = (wa[w] & 0x0F0F0F0Fu) | ((wc[w] & 0x0F0F0F0Fu) << 4);
+        const uint32_t hi = ((wa[w] >> 4) & 0x0F0F0F0Fu) | (wc[w] & 0xF0F0F0F0u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t idx = (((e & 1) ? hi : lo) >> (8 * (e >> 1))) & 0xFFu;
+            const __nv_bfloat162 v = __hmul2(lut[idx], sc);
+            const uint32_t bits = *reinterpret_cast<const uint32_t *>(&v) & keep;
+            const int d = 32 * qd + 8 * w + e;                 // d % 8 == e
+            *reinterpret_cast<uint32_t *>(base + (d >> 3) * 1024 + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4)) =
+                bits;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    mx4_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_ks,
+                    const __grid_constant__ AttnParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x;                       // row * kv_heads + kv head
+    const int kvh = static_cast<int>(item % p.kv_heads);
+
+    auto bar = [&](int i) { return sbase + AttnSmem::kBars + 8u * i; };
+    auto kfull = [&](int i) { return bar(i); };
+    auto kempty = [&](int i) { return bar(kAttnKStages + i); };
+    auto vfull = [&](int i) { return bar(2 * kAttnKStages + i); };
+    auto vempty = [&](int i) { return bar(2 * kAttnKStages + kAttnVStages + i); };
+    const uint32_t qready = bar(2 * kAttnKStages + 2 * kAttnVStages);
+    const uint32_t qk_done = qready + 8;
+    auto pvready = [&](int i) { return bar(2 * kAttnKStages + 2 * kAttnVStages + 2 + i); };
+    auto pvfree = [&](int i) { return bar(2 * kAttnKStages + 2 * kAttnVStages + 4 + i); };
+    const uint32_t pv_done = bar(2 * kAttnKStages + 2 * kAttnVStages + 6);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
+    int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
+
+    int ctx = p.context_lens[item];
+    if (ctx > p.width * kPage) ctx = p.width * kPage;
+    if (ctx < 0) ctx = 0;
+    const int npages = (ctx + kPage - 1) / kPage;
+
+    if (threadIdx.x == 0) {
+        // arrivals: TMA / commits count 1; the 4 softmax warps arrive on
+        // qready, the 8 widening warps on vempty and pvready
+        for (int i = 0; i < kAttnKStages; ++i) {
+            mbar_init(kfull(i), 1);
+            mbar_init(kempty(i), 1);
+        }
+        for (int i = 0; i < kAttnVStages; ++i) {
+            mbar_init(vfull(i), 1);
+            mbar_init(vempty(i), kAttnWidenWarps);
+        }
+        mbar_init(qready, 4);
+        mbar_init(qk_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(pvready(i), kAttnWidenWarps);
+            mbar_init(pvfree(i), 1);
+        }
+        mbar_init(pv_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < kAttnMaxPages) {
+        int32_t id = 0;
+        if (threadIdx.x < npages) {
+            const int64_t raw = p.block_table[item * p.width + threadIdx.x];
+            if (raw < 0 || raw >= p.num_pool_pages)
+                atomicOr(&g_mx4_device_status, 0x1u);
+            else
+                id = static_cast<int32_t>(raw);
+        }
+        pids[threadIdx.x] = id;
+    }
+    if (threadIdx.x < 256) {
+        // code pair (low nibble: token t, high nibble: token t+1) -> their
+        // unscaled e2m1 values as bf16 (exact)
+        const __nv_bfloat162 v = __floats2bfloat162_rn(e2m1_value(threadIdx.x & 15u), e2m1_value(threadIdx.x >> 4));
+        reinterpret_cast<__nv_bfloat162 *>(smem + AttnSmem::kLut)[threadIdx.x] = v;
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_ks);
+    }
+    if (warp == 5) {
+        tmem_alloc(sbase + AttnSmem::kTmemSlot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<uint32_t *>(smem + AttnSmem::kTmemSlot);
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer --
+        const uint64_t policy = l2_policy_evict_first();
+        bool ok = true;
+        for (int j = 0; j < npages && ok; ++j) {
+            const int s = j % kAttnKStages, u = j / kAttnKStages;
+            if (!__all_sync(0xffffffffu, wait_bounded(kempty(s), (u & 1) ^ 1u, abort_flag, kSiteAttnProducer))) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
+                mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
+                tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh, pids[j], policy);
+                tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, kvh, pids[j], policy);
+            }
+            __syncwarp();
+        }
+        for (int j = 0; j < npages && ok; ++j) {
+            const int s = j % kAttnVStages, u = j / kAttnVStages;
+            if (!__all_sync(0xffffffffu, wait_bounded(vempty(s), (u & 1) ^ 1u, abort_flag, kSiteAttnProducer))) {
+                ok = false;
+                break;
+            }
+            if (elect_one()) {
+                const int64_t pg = pids[j];
+                mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
+                bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + kvh * p.vd_hs, kDataBytes,
+                          vfull(s), policy);
+                bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + kvh * p.vs_hs,
+                          kScaleBytes, vfull(s), policy);
+            }
+            __syncwarp();
+        }
+        // no copy may be in flight when the CTA exits
+        if (lane == 0) {
+            const int nk = npages < kAttnKStages ? npages : kAttnKStages;
+            for (int i = 0; i < nk; ++i) {
+                const int j = npages - 1 - i;          // the last use of each stage
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(kfull(j % kAttnKStages), (j / kAttnKStages) & 1) &&
+                       globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+            const int nv = npages < kAttnVStages ? npages : kAttnVStages;
+            for (int i = 0; i < nv; ++i) {
+                const int j = npages - 1 - i;
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(vfull(j % kAttnVStages), (j / kAttnVStages) & 1) &&
+                       globaltimer_ns() - t0 < 2000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA --
+        bool ok = __all_sync(0xffffffffu, wait_bounded(qready, 0, abort_flag, kSiteAttnMma));
+        const uint32_t sfb = tmem_base + kAttnSfbCol;
+        const uint64_t qdesc = smem_desc(sbase + AttnSmem::kQ, 16, 1024, 2);
+        if (ok) {
+            tc_fence_after();
+            if (elect_one()) tc_cp_32x128b_warpx4(sfb, smem_desc(sbase + AttnSmem::kUnit, 16, 128, 0));
+            __syncwarp();
+        }
+        for (int j = 0; j < npages && ok; ++j) {
+            const int s = j % kAttnKStages, u = j / kAttnKStages;
+            if (!__all_sync(0xffffffffu, wait_bounded(kfull(s), u & 1, abort_flag, kSiteAttnMma))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t sfa = tmem_base + kAttnSfaCol + 4u * j;
+                tc_cp_32x128b_warpx4(sfa, smem_desc(sbase + AttnSmem::kKs + s * kScaleBytes, 16, 128, 0));
+                const uint64_t kdesc = smem_desc(sbase + AttnSmem::kK + s * kTileBytes, 16, 1024, 2);
+                const uint32_t d = tmem_base + kAttnSCol + kAttnN * j;
+#pragma unroll
+                for (uint32_t k = 0; k < 4; ++k)
+                    tc_mma_mx_ss(d, kdesc + 2 * k, qdesc + 2 * k, attn_idesc_qk(k), sfa, sfb, k > 0 ? 1u : 0u);
+                tc_commit(kempty(s));
+            }
+            __syncwarp();
+        }
+        if (elect_one()) tc_commit(qk_done);
+        __syncwarp();
+        for (int j = 0; j < npages && ok; ++j) {
+            const int b = j & 1, u = j >> 1;
+            if (!__all_sync(0xffffffffu, wait_bounded(pvready(b), u & 1, abort_flag, kSiteAttnMma))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (elect_one()) {
+                const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
+                const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    // K step of 16 tokens: 32 B inside a 128-byte atom row, next K-atom after 4 steps
+                    const uint64_t a = smem_desc(vt + (ks >> 2) * 16384u + (ks & 3) * 32u, 16, 1024, 2);
+                    const uint64_t bd = smem_desc(pt + (ks >> 2) * 2048u + (ks & 3) * 32u, 16, 1024, 2);
+                    tc_mma_f16_ss(tmem_base + kAttnOutCol, a, bd, kAttnIdescPv, (j > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(pvfree(b));
+            }
+            __syncwarp();
+        }
+        if (elect_one()) tc_commit(pv_done);
+        __syncwarp();
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(pv_done, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+        __syncwarp();
+    } else if (warp >= 6) {
+        // ---------------------------------------------------------- V widening --
+        // warps 6-9 widen tokens 64..127 of each page (warps 0-3 take 0..63)
+        for (int j = 0; j < npages; ++j) {
+            const int b = j & 1, u = j >> 1;
+            const int vs = j % kAttnVStages;
+            if (!__all_sync(0xffffffffu,
+                            (u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi)) &&
+                                wait_bounded(vfull(vs), (j / kAttnVStages) & 1, abort_flag, kSiteAttnEpi)))
+                break;
+            attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
+                       smem + AttnSmem::kVt + b * 32768, reinterpret_cast<const __nv_bfloat162 *>(smem + AttnSmem::kLut),
+                       warp - 2, lane, ctx - j * kPage);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(pvready(b));
+                mbar_arrive(vempty(vs));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------- softmax --
+        const int m = threadIdx.x;                       // TMEM lane
+        const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+        const int tok_m = token_of_col(m);               // token of lane m within each page
+        const int G = p.groups;
+        {
+            // Q tile (16 rows x 128 B, SW128) and the unit scale block
+            const int h = m >> 3, c = m & 7;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (h < G) v = *reinterpret_cast<const uint4 *>(p.q + ((item * G + h) << 7) + c * 16);
+            *reinterpret_cast<uint4 *>(smem + AttnSmem::kQ + (h >> 3) * 1024 + (h & 7) * 128 + ((c ^ (h & 7)) << 4)) = v;
+            reinterpret_cast<uint32_t *>(smem + AttnSmem::kUnit)[m] = 0x7F7F7F7Fu;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qready);
+        }
+        float M[kAttnN], S[kAttnN];
+#pragma unroll
+        for (int h = 0; h < kAttnN; ++h) {
+            M[h] = -INFINITY;
+            S[h] = 0.0f;
+        }
+        bool ok = __all_sync(0xffffffffu, wait_bounded(qk_done, 0, abort_flag, kSiteAttnEpi));
+        if (ok) {
+            tc_fence_after();
+            // pass A: per-head max over valid tokens
+            for (int j = 0; j < npages; ++j) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
+                if (j * kPage + tok_m < ctx) {
+#pragma unroll
+                    for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __uint_as_float(v[h]) * p.softmax_scale);
+                }
+            }
+        }
+        // (the named-barrier syncs below run on every path, so the four
+        // warps always pass the same number of them)
+        float *red = reinterpret_cast<float *>(smem + AttnSmem::kRed);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], o));
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) red[warp * kAttnN + h] = M[h];
+        }
+        epi_bar_sync();
+#pragma unroll
+        for (int h = 0; h < kAttnN; ++h)
+            M[h] = fmaxf(fmaxf(red[h], red[kAttnN + h]), fmaxf(red[2 * kAttnN + h], red[3 * kAttnN + h]));
+        epi_bar_sync();
+        // pass B: per page P^T and V^T for the PV MMA
+        constexpr float kLog2e = 1.4426950408889634f;
+        for (int j = 0; j < npages && ok; ++j) {
+            const int b = j & 1, u = j >> 1;
+            const int vs = j % kAttnVStages;
+            if (!__all_sync(0xffffffffu,
+                            (u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi)) &&
+                                wait_bounded(vfull(vs), (j / kAttnVStages) & 1, abort_flag, kSiteAttnEpi))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // P^T[h][t] for this lane's token, natural order
+            {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
+                const bool valid = j * kPage + tok_m < ctx;
+                uint8_t *pt = smem + AttnSmem::kPt + b * 4096;
+#pragma unroll
+                for (int h = 0; h < kAttnN; ++h) {
+                    float pr = 0.0f;
+                    if (valid && h < G)
+                        pr = exp2f((__uint_as_float(v[h]) * p.softmax_scale - M[h]) * kLog2e);
+                    const __nv_bfloat16 pb = __float2bfloat16_rn(pr);
+                    S[h] += __bfloat162float(pb);
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + sw128_bf16_offset(h, tok_m, kAttnN)) = pb;
+                }
+            }
+            attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
+                       smem + AttnSmem::kVt + b * 32768, reinterpret_cast<const __nv_bfloat162 *>(smem + AttnSmem::kLut),
+                       warp, lane, ctx - j * kPage);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(pvready(b));
+                mbar_arrive(vempty(vs));
+            }
+        }
+        // the normaliser: sum of the bf16 weights over all lanes
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) S[h] += __shfl_xor_sync(0xffffffffu, S[h], o);
+        if (lane == 0) {
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) red[warp * kAttnN + h] = S[h];
+        }
+        epi_bar_sync();
+#pragma unroll
+        for (int h = 0; h < kAttnN; ++h) S[h] = (red[h] + red[kAttnN + h]) + (red[2 * kAttnN + h] + red[3 * kAttnN + h]);
+        // output: lane m holds head dim m of every head
+        if (ok && npages > 0)
+            ok = __all_sync(0xffffffffu, wait_bounded(pv_done, 0, abort_flag, kSiteAttnEpi));
+        uint32_t acc[16];
+        if (ok && npages > 0) {
+            tc_fence_after();
+            tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnOutCol, acc);
+        } else {
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) acc[h] = 0u;
+        }
+        __nv_bfloat16 *o = p.out + (item * G) * kDim;
+#pragma unroll
+        for (int h = 0; h < kAttnN; ++h)
+            if (h < G) o[h * kDim + m] = __float2bfloat16_rn(S[h] > 0.0f ? __uint_as_float(acc[h]) / S[h] : 0.0f);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+}  // namespace mx4

@@ -14,6 +14,7 @@
 #include "score_kernel.cuh"
 #include "writer_kernel.cuh"
 #include "topk_kernel.cuh"
+#include "attn_kernel.cuh"
 
 namespace {
 
@@ -44,6 +45,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     int sm_count = 0;
     bool topk_attr_set[2] = {false, false};
+    bool attn_attr_set = false;
     bool smem_attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 
@@ -312,6 +314,34 @@ mx4_status topk_launch(const float *scores, const int32_t *block_table, const in
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 
+// Attention K views: the scorer's 4-D token-permuting view of a page's codes
+// with a KV-head dimension (5-D), and the scale words per (head, page) (3-D).
+bool encode_attn_k_map(CUtensorMap *m, const uint8_t *k_data, int64_t ps, int64_t hs, int heads, int64_t pages)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[5] = {128, 32, 4, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(pages)};
+    const cuuint64_t strides[4] = {256, 64, static_cast<cuuint64_t>(hs), static_cast<cuuint64_t>(ps)};
+    const cuuint32_t box[5] = {128, 32, 4, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 5, const_cast<uint8_t *>(k_data), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_attn_ks_map(CUtensorMap *m, const uint8_t *k_scale, int64_t ps, int64_t hs, int heads, int64_t pages)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(pages)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hs), static_cast<cuuint64_t>(ps)};
+    const cuuint32_t box[3] = {128, 1, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t *>(k_scale), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -439,6 +469,81 @@ mx4_status mx4_index_topk_decode(const float *scores, const int32_t *block_table
 {
     return topk_launch<true>(scores, block_table, nullptr, seq_lens, nullptr, 1, max_seq_len, topk, local_pages,
                              kv_groups, sel, count, stream, num_seqs, block_table_stride);
+}
+
+mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads, int groups,
+                                const uint8_t *k_data, const uint8_t *k_scale, int64_t k_data_page_stride,
+                                int64_t k_data_head_stride, int64_t k_scale_page_stride,
+                                int64_t k_scale_head_stride, const uint8_t *v_data, const uint8_t *v_scale,
+                                int64_t v_data_page_stride, int64_t v_data_head_stride,
+                                int64_t v_scale_page_stride, int64_t v_scale_head_stride,
+                                const int32_t *block_table, int block_table_width, const int32_t *context_lens,
+                                float softmax_scale, void *out, int64_t num_pool_pages, void *stream)
+{
+    if (num_rows < 0 || kv_heads < 1 || groups < 1 || block_table_width < 0) return MX4_ERR_INVALID_ARG;
+    if (!(std::isfinite(softmax_scale) && softmax_scale > 0.0f)) return MX4_ERR_INVALID_ARG;
+    if (num_rows == 0) return MX4_OK;
+    if (groups > mx4::kAttnN || block_table_width > mx4::kAttnMaxPages) return MX4_ERR_UNSUPPORTED;
+    if (!q || !k_data || !k_scale || !v_data || !v_scale || !block_table || !context_lens || !out)
+        return MX4_ERR_INVALID_ARG;
+    if (num_pool_pages < 1) return MX4_ERR_INVALID_ARG;
+    if (num_pool_pages > INT32_MAX || num_rows * kv_heads > INT32_MAX) return MX4_ERR_UNSUPPORTED;
+    // views: a page of one head holds 8192 code bytes and 512 scale bytes
+    const int64_t strides[8] = {k_data_page_stride, k_data_head_stride, k_scale_page_stride, k_scale_head_stride,
+                                v_data_page_stride, v_data_head_stride, v_scale_page_stride, v_scale_head_stride};
+    for (int64_t st : strides)
+        if (st < 0 || st >= (int64_t(1) << 40)) return MX4_ERR_INVALID_ARG;
+    if (k_data_head_stride < mx4::kDataBytes || k_scale_head_stride < mx4::kScaleBytes ||
+        v_data_head_stride < mx4::kDataBytes || v_scale_head_stride < mx4::kScaleBytes ||
+        k_data_page_stride < k_data_head_stride * kv_heads || k_scale_page_stride < k_scale_head_stride * kv_heads ||
+        v_data_page_stride < v_data_head_stride * kv_heads || v_scale_page_stride < v_scale_head_stride * kv_heads)
+        return MX4_ERR_INVALID_ARG;                                    // narrow views
+    if (!aligned(k_data, 32) || k_data_page_stride % 32 || k_data_head_stride % 32) return MX4_ERR_MISALIGNED;
+    if (!aligned(k_scale, 16) || k_scale_page_stride % 16 || k_scale_head_stride % 16) return MX4_ERR_MISALIGNED;
+    if (!aligned(v_data, 16) || v_data_page_stride % 16 || v_data_head_stride % 16) return MX4_ERR_MISALIGNED;
+    if (!aligned(v_scale, 16) || v_scale_page_stride % 16 || v_scale_head_stride % 16) return MX4_ERR_MISALIGNED;
+    if (!aligned(q, 16) || !aligned(out, 2) || !aligned(block_table, 4) || !aligned(context_lens, 4))
+        return MX4_ERR_MISALIGNED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX4_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState &st = g_dev[dev];
+        if (!st.attn_attr_set) {
+            if (cudaFuncSetAttribute(mx4::mx4_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(mx4::AttnSmem::kAlloc)) != cudaSuccess)
+                return MX4_ERR_CUDA;
+            st.attn_attr_set = true;
+        }
+    }
+    alignas(64) CUtensorMap tmap_k;
+    alignas(64) CUtensorMap tmap_ks;
+    if (!encode_attn_k_map(&tmap_k, k_data, k_data_page_stride, k_data_head_stride, kv_heads, num_pool_pages))
+        return MX4_ERR_CUDA;
+    if (!encode_attn_ks_map(&tmap_ks, k_scale, k_scale_page_stride, k_scale_head_stride, kv_heads, num_pool_pages))
+        return MX4_ERR_CUDA;
+    mx4::AttnParams p{};
+    p.q = q;
+    p.v_data = v_data;
+    p.v_scale = v_scale;
+    p.vd_ps = v_data_page_stride;
+    p.vd_hs = v_data_head_stride;
+    p.vs_ps = v_scale_page_stride;
+    p.vs_hs = v_scale_head_stride;
+    p.block_table = block_table;
+    p.context_lens = context_lens;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.num_pool_pages = num_pool_pages;
+    p.kv_heads = kv_heads;
+    p.groups = groups;
+    p.width = block_table_width;
+    p.softmax_scale = softmax_scale;
+    // one CTA per (row, KV head)
+    cudaGetLastError();
+    mx4::mx4_attn_kernel<<<static_cast<unsigned>(num_rows * kv_heads), mx4::kAttnThreads, mx4::AttnSmem::kAlloc,
+                           static_cast<cudaStream_t>(stream)>>>(tmap_k, tmap_ks, p);
+    return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 
 mx4_status mx4_quantize_q_e4m3(const uint16_t *q_bf16, uint8_t *q_e4m3, int64_t n, void *stream)

@@ -1,0 +1,104 @@
+"""GPU sparse paged-attention decode (MXFP4 K and V) against the fp64 oracle.
+
+Tolerance, from the arithmetic: the kernel rounds the softmax weights p to
+bf16 (relative 2^-9) both in sum_t p v and in the normaliser, and rounds the
+output to bf16; K, V and Q values are exact.  So
+    |gpu - ref| <= 2^-9 (E_p|v| + |ref|) + 2^-9 |ref|,
+E_p|v| = sum_t p_t |v_t| / sum_t p_t; the test allows twice each term.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_mxfp4_gb300 as mx4
+from sparse_attention_mxfp4_gb300 import workloads as W
+from helpers import e4m3_values_numpy
+from test_oracle_attn import _dequant_pool, _run as oracle_attn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mx4.build()
+    mx4.load_library()
+    mx4.mx4_index_get_device_status()
+    yield
+    assert mx4.mx4_index_get_device_status() == 0
+
+
+def _gpu(c):
+    out = mx4.mx4_sparse_pa_decode(c.q.cuda(), c.k_pool.cuda(), c.v_pool.cuda(), c.block_table.cuda(),
+                                   c.context_lens.cuda(), c.softmax_scale)
+    torch.cuda.synchronize()
+    st = mx4.mx4_index_get_device_status()
+    assert st == 0, f"device status {st:#x}"
+    return out.float().cpu().numpy()
+
+
+def _abs_weighted_v(c):
+    """E_p|v| for every (row, head, group, d), by a numpy softmax."""
+    K, V = _dequant_pool(c.k_pool), _dequant_pool(c.v_pool)
+    q = e4m3_values_numpy(c.q.numpy())
+    out = np.zeros(q.shape)
+    for r in range(c.rows):
+        for h in range(c.kv_heads):
+            n = int(c.context_lens[r, h])
+            if n <= 0:
+                continue
+            ids = [int(x) for x in c.block_table[r, h, : (n + 127) // 128]]
+            k = np.concatenate([K[x, h] for x in ids])[:n]
+            v = np.concatenate([V[x, h] for x in ids])[:n]
+            s = c.softmax_scale * (q[r, h] @ k.T)
+            w = np.exp(s - s.max(axis=1, keepdims=True))
+            out[r, h] = (w / w.sum(axis=1, keepdims=True)) @ np.abs(v)
+    return out
+
+
+def _check(c):
+    got = _gpu(c)
+    ref = oracle_attn(c)
+    lim = 2.0 ** -8 * (_abs_weighted_v(c) + np.abs(ref)) + 2.0 ** -8 * np.abs(ref) + 1e-30
+    err = np.abs(got - ref)
+    bad = err > lim
+    assert not bad.any(), (f"{int(bad.sum())} of {bad.size} outside; worst err {err.max():.3e}, "
+                           f"at ref {ref.reshape(-1)[np.argmax(err)]:.4f}")
+    rel_l2 = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert rel_l2 < 4e-3, rel_l2
+    return rel_l2
+
+
+@pytest.mark.parametrize("rows,kvh,groups,width", [(3, 1, 16, 5), (4, 2, 16, 3), (5, 1, 4, 7), (2, 2, 1, 24)])
+def test_attn_small(rows, kvh, groups, width):
+    c = W.make_attn_case(f"a{rows}{kvh}{groups}{width}", seed=100 + rows, rows=rows, kv_heads=kvh, groups=groups,
+                         width=width)
+    _check(c)
+
+
+def test_attn_wide_scales_and_ragged_contexts():
+    c = W.make_attn_case("wide", seed=110, rows=6, kv_heads=1, groups=16, width=6,
+                         ctx=[1, 127, 128, 129, 640, 768], scale_lo=115, scale_hi=135)
+    _check(c)
+
+
+def test_attn_zero_query_is_mean_of_v():
+    c = W.make_attn_case("mean", seed=111, rows=3, kv_heads=1, groups=16, width=4)
+    c = dataclasses.replace(c, q=torch.zeros_like(c.q))
+    _check(c)
+
+
+def test_attn_empty_rows_are_zero():
+    c = W.make_attn_case("empty", seed=112, rows=3, kv_heads=1, groups=8, width=2, ctx=[0, 5, 0])
+    got = _gpu(c)
+    assert (got[0] == 0).all() and (got[2] == 0).all()
+    _check(c)
+
+
+def test_attn_full_size_config():
+    c = W.make_attn_config("pa-decode")
+    print("rel_l2", _check(c))
