@@ -9,11 +9,12 @@
 // leak):
 //     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V.
 //
-// One CTA per row (320 threads), two passes over the row's pages:
-//   warp 4   producer: per page, the K codes (4-D token-permuting TMA view
-//            plus a KV-head dimension, the scorer's smem form) and K scales,
-//            then the V codes and scales as two plain bulk copies (natural
-//            token order: V is not an MMA operand in MXFP4 form).
+// One CTA per row (512 threads), two passes over the row's pages:
+//   warp 4   K copies: per page, the K codes (4-D token-permuting TMA view
+//            plus a KV-head dimension, the scorer's smem form) and K scales.
+//   warp 10  V copies: the V codes and scales as two plain bulk copies per
+//            page (natural token order: V is not an MMA operand in MXFP4
+//            form), from the start, six pages deep.
 //   warp 5   MMA: QK per page with tcgen05.mma kind::mxf8f6f4 block_scale,
 //            A = the K page (M = 128 tokens, e2m1, its e8m0 scales copied to a
 //            per-page TMEM slot), B = the Q tile (N = 16 heads, e4m3, unit
@@ -24,10 +25,9 @@
 //   warps 0-3 softmax: thread m reads TMEM lane m (token 4(m%32)+m/32 of each
 //            page), takes the per-head max over valid tokens (shuffles across
 //            lanes, shared memory across warps), then per page writes P^T
-//            (bf16, natural token order), widens tokens 0..63 of the page's V
-//            into V^T (bf16) for the PV MMA, and sums the bf16 P; finally
-//            out = acc / sum, stored as bf16.
-//   warps 6-9 widen tokens 64..127 of each page's V.
+//            (bf16, natural token order) for the PV MMA and sums the bf16 P;
+//            finally out = acc / sum, stored as bf16.
+//   warps 6-9, 11-14 widen each page's V into V^T (bf16), 16 tokens each.
 #pragma once
 
 #include <cuda.h>
@@ -39,12 +39,15 @@
 
 namespace mx4 {
 
-constexpr int kAttnThreads = 320;       // warps 0-3 softmax, 4 copies, 5 MMA, 6-9 V widening
-constexpr int kAttnWidenWarps = 8;      // warps 0-3 and 6-9 share the V widening
+// warps 0-3 softmax (P^T), 4 K copies, 5 MMA, 6-9 and 11-14 V widening,
+// 10 V copies, 15 idle (the block is 16 warps so that 4 sit on each SM
+// sub-partition: 128 registers a thread)
+constexpr int kAttnThreads = 512;
+constexpr int kAttnWidenWarps = 8;
 constexpr int kAttnMaxPages = 24;       // pages a row may list: every page's scores stay in TMEM
 constexpr int kAttnN = 16;              // query heads per KV head (fewer are zero-padded)
 constexpr int kAttnKStages = 4;
-constexpr int kAttnVStages = 3;
+constexpr int kAttnVStages = 6;        // V pages load from the start, alongside the K pages
 constexpr uint32_t kAttnSCol = 0;                                    // page j: 16 columns at 16 j
 constexpr uint32_t kAttnOutCol = kAttnMaxPages * kAttnN;              // 384
 constexpr uint32_t kAttnSfaCol = kAttnOutCol + kAttnN;                // 400: 4 per page
@@ -132,7 +135,7 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
 // exact), tokens at or past `valid` are zeroed, and the pair lands in one
 // 4-byte store (adjacent K positions of one V^T row).
 __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc, uint8_t *vt,
-                                           const __nv_bfloat162 *lut, int wi, int lane, int valid)
+                                           const __nv_bfloat162 *__restrict__ lut, int wi, int lane, int valid)
 {
     const int t0 = 16 * wi + 2 * (lane & 7);
     const int qd = lane >> 3;
@@ -144,22 +147,26 @@ __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc
     const uint32_t keep = (t0 < valid ? 0x0000FFFFu : 0u) | (t0 + 1 < valid ? 0xFFFF0000u : 0u);
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
     const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
-    const uint32_t cch = static_cast<uint32_t>((t0 & 63) >> 3);    // the pair's 16-byte chunk in a row
-    uint8_t *base = vt + (t0 >> 6) * 16384 + (t0 & 7) * 2;
+    // all 32 table lookups first (nothing stored yet, so they are not held
+    // back behind stores that might alias them), then scale and store
+    __nv_bfloat162 v[32];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         // byte i of lo: codes of head dim 2i of both tokens; of hi: dim 2i+1
         const uint32_t lo = (wa[w] & 0x0F0F0F0Fu) | ((wc[w] & 0x0F0F0F0Fu) << 4);
         const uint32_t hi = ((wa[w] >> 4) & 0x0F0F0F0Fu) | (wc[w] & 0xF0F0F0F0u);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t idx = (((e & 1) ? hi : lo) >> (8 * (e >> 1))) & 0xFFu;
-            const __nv_bfloat162 v = __hmul2(lut[idx], sc);
-            const uint32_t bits = *reinterpret_cast<const uint32_t *>(&v) & keep;
-            const int d = 32 * qd + 8 * w + e;                 // d % 8 == e
-            *reinterpret_cast<uint32_t *>(base + (d >> 3) * 1024 + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4)) =
-                bits;
-        }
+        for (int e = 0; e < 8; ++e) v[8 * w + e] = lut[(((e & 1) ? hi : lo) >> (8 * (e >> 1))) & 0xFFu];
+    }
+    const uint32_t cch = static_cast<uint32_t>((t0 & 63) >> 3);    // the pair's 16-byte chunk in a row
+    uint8_t *base = vt + (t0 >> 6) * 16384 + (t0 & 7) * 2 + qd * 4096;   // rows 32 qd ..
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int e = i & 7;                                   // head dim 32 qd + i, i % 8 == e
+        const __nv_bfloat162 x = __hmul2(v[i], sc);
+        const uint32_t bits = *reinterpret_cast<const uint32_t *>(&x) & keep;
+        *reinterpret_cast<uint32_t *>(base + (i >> 3) * 1024 + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4)) =
+            bits;
     }
 }
 
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         // arrivals: TMA / commits count 1; the 4 softmax warps arrive on
-        // qready, the 8 widening warps on vempty and pvready
+        // qready and pvready, the 8 widening warps on vempty and pvready
         for (int i = 0; i < kAttnKStages; ++i) {
             mbar_init(kfull(i), 1);
             mbar_init(kempty(i), 1);
@@ -204,10 +211,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(vfull(i), 1);
             mbar_init(vempty(i), kAttnWidenWarps);
         }
+        // pvready: the 4 softmax warps (P^T) and the 8 widening warps (V^T)
         mbar_init(qready, 4);
         mbar_init(qk_done, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(pvready(i), kAttnWidenWarps);
+            mbar_init(pvready(i), 4 + kAttnWidenWarps);
             mbar_init(pvfree(i), 1);
         }
         mbar_init(pv_done, 1);
@@ -244,55 +252,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<uint32_t *>(smem + AttnSmem::kTmemSlot);
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ producer --
+    if (warp == 4 || warp == 10) {
+        // ------------------------------------------------------------ copies --
+        // warp 4: the K pages (TMA); warp 10: the V pages (bulk copies), from
+        // the start so they overlap the QK phase
         const uint64_t policy = l2_policy_evict_first();
-        bool ok = true;
-        for (int j = 0; j < npages && ok; ++j) {
-            const int s = j % kAttnKStages, u = j / kAttnKStages;
-            if (!__all_sync(0xffffffffu, wait_bounded(kempty(s), (u & 1) ^ 1u, abort_flag, kSiteAttnProducer))) {
-                ok = false;
+        const bool is_k = warp == 4;
+        const int nst = is_k ? kAttnKStages : kAttnVStages;
+        int issued = 0;
+        for (int j = 0; j < npages; ++j) {
+            const int s = j % nst, u = j / nst;
+            const uint32_t empty_b = is_k ? kempty(s) : vempty(s);
+            if (!__all_sync(0xffffffffu, wait_bounded(empty_b, (u & 1) ^ 1u, abort_flag, kSiteAttnProducer)))
                 break;
-            }
-            if (elect_one()) {
-                mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
-                tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh, pids[j], policy);
-                tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, kvh, pids[j], policy);
-            }
-            __syncwarp();
-        }
-        for (int j = 0; j < npages && ok; ++j) {
-            const int s = j % kAttnVStages, u = j / kAttnVStages;
-            if (!__all_sync(0xffffffffu, wait_bounded(vempty(s), (u & 1) ^ 1u, abort_flag, kSiteAttnProducer))) {
-                ok = false;
-                break;
-            }
             if (elect_one()) {
                 const int64_t pg = pids[j];
-                mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
-                bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + kvh * p.vd_hs, kDataBytes,
-                          vfull(s), policy);
-                bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + kvh * p.vs_hs,
-                          kScaleBytes, vfull(s), policy);
-            }
-            __syncwarp();
-        }
-        // no copy may be in flight when the CTA exits
-        if (lane == 0) {
-            const int nk = npages < kAttnKStages ? npages : kAttnKStages;
-            for (int i = 0; i < nk; ++i) {
-                const int j = npages - 1 - i;          // the last use of each stage
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(kfull(j % kAttnKStages), (j / kAttnKStages) & 1) &&
-                       globaltimer_ns() - t0 < 2000000ull) {
+                if (is_k) {
+                    mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
+                    tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh,
+                                static_cast<int>(pg), policy);
+                    tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, kvh,
+                                static_cast<int>(pg), policy);
+                } else {
+                    mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
+                    bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + kvh * p.vd_hs,
+                              kDataBytes, vfull(s), policy);
+                    bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + kvh * p.vs_hs,
+                              kScaleBytes, vfull(s), policy);
                 }
             }
-            const int nv = npages < kAttnVStages ? npages : kAttnVStages;
-            for (int i = 0; i < nv; ++i) {
-                const int j = npages - 1 - i;
+            __syncwarp();
+            ++issued;
+        }
+        // no copy may be in flight when the CTA exits: the last use of each
+        // stage this warp armed completes (bounded)
+        if (lane == 0) {
+            const int n = issued < nst ? issued : nst;
+            for (int i = 0; i < n; ++i) {
+                const int j = issued - 1 - i;
+                const uint32_t full_b = is_k ? kfull(j % nst) : vfull(j % nst);
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(vfull(j % kAttnVStages), (j / kAttnVStages) & 1) &&
-                       globaltimer_ns() - t0 < 2000000ull) {
+                while (!mbar_try_wait(full_b, (j / nst) & 1) && globaltimer_ns() - t0 < 2000000ull) {
                 }
             }
         }
@@ -357,7 +357,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
     } else if (warp >= 6) {
         // ---------------------------------------------------------- V widening --
-        // warps 6-9 widen tokens 64..127 of each page (warps 0-3 take 0..63)
+        // warps 6-9 and 11-14 widen 16 tokens of each page each (warp 10 is
+        // the V copy warp above, warp 15 has no role)
+        if (warp == 15) goto done;
         for (int j = 0; j < npages; ++j) {
             const int b = j & 1, u = j >> 1;
             const int vs = j % kAttnVStages;
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
                        smem + AttnSmem::kVt + b * 32768, reinterpret_cast<const __nv_bfloat162 *>(smem + AttnSmem::kLut),
-                       warp - 2, lane, ctx - j * kPage);
+                       warp < 10 ? warp - 6 : warp - 7, lane, ctx - j * kPage);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -431,10 +433,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         constexpr float kLog2e = 1.4426950408889634f;
         for (int j = 0; j < npages && ok; ++j) {
             const int b = j & 1, u = j >> 1;
-            const int vs = j % kAttnVStages;
             if (!__all_sync(0xffffffffu,
-                            (u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi)) &&
-                                wait_bounded(vfull(vs), (j / kAttnVStages) & 1, abort_flag, kSiteAttnEpi))) {
+                            u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi))) {
                 ok = false;
                 break;
             }
@@ -455,15 +455,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     *reinterpret_cast<__nv_bfloat16 *>(pt + sw128_bf16_offset(h, tok_m, kAttnN)) = pb;
                 }
             }
-            attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
-                       smem + AttnSmem::kVt + b * 32768, reinterpret_cast<const __nv_bfloat162 *>(smem + AttnSmem::kLut),
-                       warp, lane, ctx - j * kPage);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(pvready(b));
-                mbar_arrive(vempty(vs));
-            }
+            if (lane == 0) mbar_arrive(pvready(b));
         }
         // the normaliser: sum of the bf16 weights over all lanes
 #pragma unroll
@@ -494,6 +488,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (h < G) o[h * kDim + m] = __float2bfloat16_rn(S[h] > 0.0f ? __uint_as_float(acc[h]) / S[h] : 0.0f);
     }
 
+done:
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {
