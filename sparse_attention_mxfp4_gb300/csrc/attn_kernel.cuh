@@ -126,10 +126,12 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
     return (code & 8u) ? -m : m;
 }
 
-// Widen tokens 16 wi .. 16 wi + 15 of a V page (natural layout in smem: 64
-// code bytes and 4 scale bytes per token) into the bf16 V^T operand tile.
-// Lane l takes the token pair t0 = 16 wi + 2 (l % 8), t0 + 1 and head dims
-// 32 (l / 8) .. +32 (one scale group): per head dim the two tokens' codes form
+// Widen one eighth of a V page (natural layout in smem: 64 code bytes and 4
+// scale bytes per token) into the bf16 V^T operand tile: warp slot wi takes
+// tokens 64 (wi % 2) .. +64 and head dims 32 (wi / 2) .. +32 (one scale
+// group); lane l takes the token pair t0 = 64 (wi % 2) + 2 l, t0 + 1, so the
+// 32 lanes of each store fill one 128-byte V^T row segment (no bank
+// conflicts).  Per head dim the two tokens' codes form
 // one byte that indexes `lut` (both unscaled values as bf16), one packed bf16
 // multiply applies the two tokens' scales (2^(b-127) is bf16 bits b << 7,
 // exact), tokens at or past `valid` are zeroed, and the pair lands in one
@@ -137,8 +139,8 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
 __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc, uint8_t *vt,
                                            const __nv_bfloat162 *__restrict__ lut, int wi, int lane, int valid)
 {
-    const int t0 = 16 * wi + 2 * (lane & 7);
-    const int qd = lane >> 3;
+    const int t0 = 64 * (wi & 1) + 2 * lane;
+    const int qd = wi >> 1;
     const uint4 a = *reinterpret_cast<const uint4 *>(vc + t0 * 64 + qd * 16);
     const uint4 c = *reinterpret_cast<const uint4 *>(vc + (t0 + 1) * 64 + qd * 16);
     const uint32_t sbits = (static_cast<uint32_t>(vsc[t0 * 4 + qd]) << 7) |
