@@ -9,7 +9,9 @@
 // leak):
 //     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V.
 //
-// One CTA per row (512 threads), two passes over the row's pages:
+// One 2-CTA cluster per row, 512 threads a CTA, each CTA taking half of the
+// row's pages (the halves exchange their maxima and rank 1 hands its partial
+// results to rank 0 through distributed shared memory); two passes per CTA:
 //   warp 4   K copies: per page, the K codes (4-D token-permuting TMA view
 //            plus a KV-head dimension, the scorer's smem form) and K scales.
 //   warp 10  V copies: the V codes and scales as two plain bulk copies per
@@ -44,14 +46,16 @@ namespace mx4 {
 // sub-partition: 128 registers a thread)
 constexpr int kAttnThreads = 512;
 constexpr int kAttnWidenWarps = 8;
-constexpr int kAttnMaxPages = 24;       // pages a row may list: every page's scores stay in TMEM
+constexpr int kAttnMaxPages = 24;       // pages a row may list
+constexpr int kAttnSplit = 2;           // CTAs (one cluster) per row: each takes half of the row's pages
+constexpr int kAttnCtaPages = (kAttnMaxPages + kAttnSplit - 1) / kAttnSplit;   // scores kept in TMEM
 constexpr int kAttnN = 16;              // query heads per KV head (fewer are zero-padded)
 constexpr int kAttnKStages = 4;
 constexpr int kAttnVStages = 6;        // V pages load from the start, alongside the K pages
 constexpr uint32_t kAttnSCol = 0;                                    // page j: 16 columns at 16 j
-constexpr uint32_t kAttnOutCol = kAttnMaxPages * kAttnN;              // 384
-constexpr uint32_t kAttnSfaCol = kAttnOutCol + kAttnN;                // 400: 4 per page
-constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnMaxPages;     // 496
+constexpr uint32_t kAttnOutCol = kAttnCtaPages * kAttnN;              // 192
+constexpr uint32_t kAttnSfaCol = kAttnOutCol + kAttnN;                // 208: 4 per page
+constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnCtaPages;     // 256
 static_assert(kAttnSfbCol + 4 <= 512, "attention TMEM budget");
 
 enum AttnSite : uint32_t { kSiteAttnProducer = 6, kSiteAttnMma = 7, kSiteAttnEpi = 8 };
@@ -82,9 +86,12 @@ struct AttnSmem {
     static constexpr uint32_t kUnit = kQ + 2048;                         // 512 B of 0x7F
     static constexpr uint32_t kRed = kUnit + 512;                        // 4 warps x 16 floats
     static constexpr uint32_t kLut = kRed + 4 * 16 * 4;                  // 256 x bf16x2: code pair -> values
-    static constexpr uint32_t kBars = kLut + 256 * 4;
-    // kfull[4] kempty[4] vfull[3] vempty[3] qready qk_done pvready[2] pvfree[2] pv_done
-    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 2 + 4 + 1;
+    static constexpr uint32_t kPeerMax = kLut + 256 * 4;                 // the other CTA's 16 head maxima
+    static constexpr uint32_t kComb = kPeerMax + 16 * 4;                 // rank 1's accumulator (128 x 16)
+    static constexpr uint32_t kCombS = kComb + 128 * 16 * 4;             // rank 1's 16 sums
+    static constexpr uint32_t kBars = kCombS + 16 * 4;
+    // kfull[4] kempty[4] vfull[6] vempty[6] qready qk_done pvready[2] pvfree[2] pv_done max_ready comb_ready
+    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 2 + 4 + 1 + 2;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kPid = kAbort + 4;                         // page ids of the row
@@ -125,6 +132,27 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
     const float m = static_cast<float>(twice) * 0.5f;
     return (code & 8u) ? -m : m;
 }
+
+// Bounded wait on a barrier that the peer CTA arrives on remotely (cluster-
+// scope acquire); on timeout it records the site and aborts like
+// wait_bounded.
+__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                                     uint32_t site)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Widen one eighth of a V page (natural layout in smem: 64 code bytes and 4
 // scale bytes per token) into the bf16 V^T operand tile: warp slot wi takes
@@ -172,7 +200,7 @@ __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc
     }
 }
 
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThreads, 1)
     mx4_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_ks,
                     const __grid_constant__ AttnParams p)
 {
@@ -181,8 +209,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t item = blockIdx.x;                       // row * kv_heads + kv head
+    const int64_t item = blockIdx.x / kAttnSplit;          // row * kv_heads + kv head
     const int kvh = static_cast<int>(item % p.kv_heads);
+    const uint32_t rank = cluster_ctarank();               // this CTA's half of the row's pages
+    const uint32_t peer = rank ^ 1u;
 
     auto bar = [&](int i) { return sbase + AttnSmem::kBars + 8u * i; };
     auto kfull = [&](int i) { return bar(i); };
@@ -194,13 +224,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto pvready = [&](int i) { return bar(2 * kAttnKStages + 2 * kAttnVStages + 2 + i); };
     auto pvfree = [&](int i) { return bar(2 * kAttnKStages + 2 * kAttnVStages + 4 + i); };
     const uint32_t pv_done = bar(2 * kAttnKStages + 2 * kAttnVStages + 6);
+    const uint32_t max_ready = pv_done + 8;                // the peer's maxima have landed (remote arrive)
+    const uint32_t comb_ready = pv_done + 16;              // rank 1's partial results have landed (rank 0)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
     int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
 
     int ctx = p.context_lens[item];
     if (ctx > p.width * kPage) ctx = p.width * kPage;
     if (ctx < 0) ctx = 0;
-    const int npages = (ctx + kPage - 1) / kPage;
+    const int npages_all = (ctx + kPage - 1) / kPage;
+    const int half = (npages_all + 1) / 2;
+    const int pbase = rank == 0 ? 0 : half;                // first page of this CTA
+    const int npages = rank == 0 ? half : npages_all - half;   // pages of this CTA
 
     if (threadIdx.x == 0) {
         // arrivals: TMA / commits count 1; the 4 softmax warps arrive on
@@ -221,12 +256,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(pvfree(i), 1);
         }
         mbar_init(pv_done, 1);
+        mbar_init(max_ready, 1);
+        mbar_init(comb_ready, 4);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (threadIdx.x < kAttnMaxPages) {
         int32_t id = 0;
-        if (threadIdx.x < npages) {
+        if (static_cast<int>(threadIdx.x) >= pbase && static_cast<int>(threadIdx.x) < pbase + npages) {
             const int64_t raw = p.block_table[item * p.width + threadIdx.x];
             if (raw < 0 || raw >= p.num_pool_pages)
                 atomicOr(&g_mx4_device_status, 0x1u);
@@ -251,6 +288,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // the peer's barriers are initialised before anyone arrives on them remotely
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<uint32_t *>(smem + AttnSmem::kTmemSlot);
 
@@ -268,7 +307,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!__all_sync(0xffffffffu, wait_bounded(empty_b, (u & 1) ^ 1u, abort_flag, kSiteAttnProducer)))
                 break;
             if (elect_one()) {
-                const int64_t pg = pids[j];
+                const int64_t pg = pids[pbase + j];
                 if (is_k) {
                     mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
                     tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh,
@@ -371,7 +410,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
                        smem + AttnSmem::kVt + b * 32768, reinterpret_cast<const __nv_bfloat162 *>(smem + AttnSmem::kLut),
-                       warp < 10 ? warp - 6 : warp - 7, lane, ctx - j * kPage);
+                       warp < 10 ? warp - 6 : warp - 7, lane, ctx - (pbase + j) * kPage);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -409,7 +448,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int j = 0; j < npages; ++j) {
                 uint32_t v[16];
                 tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
-                if (j * kPage + tok_m < ctx) {
+                if ((pbase + j) * kPage + tok_m < ctx) {
 #pragma unroll
                     for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __uint_as_float(v[h]) * p.softmax_scale);
                 }
@@ -431,6 +470,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int h = 0; h < kAttnN; ++h)
             M[h] = fmaxf(fmaxf(red[h], red[kAttnN + h]), fmaxf(red[2 * kAttnN + h], red[3 * kAttnN + h]));
         epi_bar_sync();
+        // The row's max over both CTAs: lane 0 of warp 0 stores this CTA's
+        // maxima into the peer's shared memory and arrives on the peer's
+        // barrier (release, cluster scope); every softmax warp then waits for
+        // the peer's maxima (acquire) and takes the larger value per head.
+        if (warp == 0 && lane == 0) {
+            const uint32_t dst = cluster_map(sbase + AttnSmem::kPeerMax, peer);
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) st_cluster_f32(dst + 4u * h, M[h]);
+            mbar_arrive_remote(cluster_map(max_ready, peer));
+        }
+        {
+            const bool got = __all_sync(0xffffffffu, wait_cluster_bounded(max_ready, 0, abort_flag, kSiteAttnEpi));
+            if (got) {
+                const float *pm = reinterpret_cast<const float *>(smem + AttnSmem::kPeerMax);
+#pragma unroll
+                for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], pm[h]);
+            }
+            ok = ok && got;
+        }
         // pass B: per page P^T and V^T for the PV MMA
         constexpr float kLog2e = 1.4426950408889634f;
         for (int j = 0; j < npages && ok; ++j) {
@@ -445,7 +503,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             {
                 uint32_t v[16];
                 tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
-                const bool valid = j * kPage + tok_m < ctx;
+                const bool valid = (pbase + j) * kPage + tok_m < ctx;
                 uint8_t *pt = smem + AttnSmem::kPt + b * 4096;
 #pragma unroll
                 for (int h = 0; h < kAttnN; ++h) {
@@ -484,10 +542,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int h = 0; h < kAttnN; ++h) acc[h] = 0u;
         }
-        __nv_bfloat16 *o = p.out + (item * G) * kDim;
+        if (rank != 0) {
+            // hand this CTA's accumulator column and sums to rank 0
+            const uint32_t dst = cluster_map(sbase + AttnSmem::kComb + m * 64u, 0);
 #pragma unroll
-        for (int h = 0; h < kAttnN; ++h)
-            if (h < G) o[h * kDim + m] = __float2bfloat16_rn(S[h] > 0.0f ? __uint_as_float(acc[h]) / S[h] : 0.0f);
+            for (int h = 0; h < kAttnN; ++h) st_cluster_f32(dst + 4u * h, __uint_as_float(acc[h]));
+            if (threadIdx.x == 0) {
+                const uint32_t ds = cluster_map(sbase + AttnSmem::kCombS, 0);
+#pragma unroll
+                for (int h = 0; h < kAttnN; ++h) st_cluster_f32(ds + 4u * h, S[h]);
+            }
+            fence_cluster();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(cluster_map(comb_ready, 0));
+        } else {
+            // rank 0: add rank 1's partial results, normalise, store bf16
+            float a[kAttnN];
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) a[h] = __uint_as_float(acc[h]);
+            if (__all_sync(0xffffffffu, wait_cluster_bounded(comb_ready, 0, abort_flag, kSiteAttnEpi))) {
+                const float *cm = reinterpret_cast<const float *>(smem + AttnSmem::kComb) + m * kAttnN;
+                const float *cs = reinterpret_cast<const float *>(smem + AttnSmem::kCombS);
+#pragma unroll
+                for (int h = 0; h < kAttnN; ++h) {
+                    a[h] += cm[h];
+                    S[h] += cs[h];
+                }
+            }
+            __nv_bfloat16 *o = p.out + (item * G) * kDim;
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h)
+                if (h < G) o[h * kDim + m] = __float2bfloat16_rn(S[h] > 0.0f ? a[h] / S[h] : 0.0f);
+        }
     }
 
 done:
@@ -497,6 +583,8 @@ done:
         tc_fence_after();
         tmem_dealloc(tmem_base, 512);
     }
+    // neither CTA leaves while the other may still write into its shared memory
+    cluster_sync();
 }
 
 }  // namespace mx4

@@ -539,9 +539,10 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     p.groups = groups;
     p.width = block_table_width;
     p.softmax_scale = softmax_scale;
-    // one CTA per (row, KV head)
+    // one cluster of kAttnSplit CTAs per (row, KV head)
     cudaGetLastError();
-    mx4::mx4_attn_kernel<<<static_cast<unsigned>(num_rows * kv_heads), mx4::kAttnThreads, mx4::AttnSmem::kAlloc,
+    mx4::mx4_attn_kernel<<<static_cast<unsigned>(num_rows * kv_heads * mx4::kAttnSplit), mx4::kAttnThreads,
+                           mx4::AttnSmem::kAlloc,
                            static_cast<cudaStream_t>(stream)>>>(tmap_k, tmap_ks, p);
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
