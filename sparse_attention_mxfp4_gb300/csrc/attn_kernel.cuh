@@ -10,13 +10,15 @@
 //     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V.
 //
 // One 2-CTA cluster per row, 512 threads a CTA, each CTA taking half of the
-// row's pages (the halves exchange their maxima and rank 1 hands its partial
-// results to rank 0 through distributed shared memory); two passes per CTA:
+// row's pages with its own softmax max; at the end each CTA finalises 8 of
+// the 16 heads, reading the peer's partial output, weight sums and maxima
+// from the peer's shared memory (rescaled to the row's max, added,
+// normalised); per CTA:
 //   warp 4   K copies: per page, the K codes (4-D token-permuting TMA view
 //            plus a KV-head dimension, the scorer's smem form) and K scales.
 //   warp 10  V copies: the V codes and scales as two plain bulk copies per
 //            page (natural token order: V is not an MMA operand in MXFP4
-//            form), from the start, six pages deep.
+//            form), from the start, four pages deep.
 //   warp 5   MMA: QK per page with tcgen05.mma kind::mxf8f6f4 block_scale,
 //            A = the K page (M = 128 tokens, e2m1, its e8m0 scales copied to a
 //            per-page TMEM slot), B = the Q tile (N = 16 heads, e4m3, unit
@@ -25,11 +27,13 @@
 //            K = 128 tokens, bf16), B = P^T (N = 16 heads, bf16), D = the
 //            output accumulator (16 columns), accumulated over pages.
 //   warps 0-3 softmax: thread m reads TMEM lane m (token 4(m%32)+m/32 of each
-//            page), takes the per-head max over valid tokens (shuffles across
-//            lanes, shared memory across warps), then per page writes P^T
-//            (bf16, natural token order) for the PV MMA and sums the bf16 P;
-//            finally out = acc / sum, stored as bf16.
-//   warps 6-9, 11-14 widen each page's V into V^T (bf16), 16 tokens each.
+//            page) as each page's QK product completes, takes the per-head
+//            max over valid tokens (shuffles across lanes, shared memory
+//            across warps), then per page writes P^T (bf16, natural token
+//            order) for the PV MMA and sums the bf16 P; finally the combine
+//            above and out = acc / sum, stored as bf16.
+//   warps 6-9, 11-14 widen each page's V into V^T (bf16), one (token pair,
+//            32-dim scale group) cell a thread.
 #pragma once
 
 #include <cuda.h>
@@ -51,7 +55,8 @@ constexpr int kAttnSplit = 2;           // CTAs (one cluster) per row: each take
 constexpr int kAttnCtaPages = (kAttnMaxPages + kAttnSplit - 1) / kAttnSplit;   // scores kept in TMEM
 constexpr int kAttnN = 16;              // query heads per KV head (fewer are zero-padded)
 constexpr int kAttnKStages = 4;
-constexpr int kAttnVStages = 6;        // V pages load from the start, alongside the K pages
+constexpr int kAttnVStages = 4;        // V pages load from the start, alongside the K pages
+constexpr int kAttnPvBufs = 3;         // V^T / P^T operand buffers: widening runs up to 3 pages ahead of PV
 constexpr uint32_t kAttnSCol = 0;                                    // page j: 16 columns at 16 j
 constexpr uint32_t kAttnOutCol = kAttnCtaPages * kAttnN;              // 192
 constexpr uint32_t kAttnSfaCol = kAttnOutCol + kAttnN;                // 208: 4 per page
@@ -80,18 +85,16 @@ struct AttnSmem {
     static constexpr uint32_t kKs = kK + kAttnKStages * kTileBytes;      // K scales
     static constexpr uint32_t kV = kKs + kAttnKStages * kScaleBytes;     // V codes, natural order
     static constexpr uint32_t kVs = kV + kAttnVStages * kDataBytes;      // V scales
-    static constexpr uint32_t kVt = ((kVs + kAttnVStages * kScaleBytes) + 1023) & ~1023u;   // 2 x 32 KB
-    static constexpr uint32_t kPt = kVt + 2 * 32768;                     // 2 x 4 KB
-    static constexpr uint32_t kQ = kPt + 2 * 4096;                       // 16 x 128 B
+    static constexpr uint32_t kVt = ((kVs + kAttnVStages * kScaleBytes) + 1023) & ~1023u;   // 3 x 32 KB
+    static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // 3 x 4 KB
+    static constexpr uint32_t kQ = kPt + kAttnPvBufs * 4096;             // 16 x 128 B
     static constexpr uint32_t kUnit = kQ + 2048;                         // 512 B of 0x7F
     static constexpr uint32_t kRed = kUnit + 512;                        // 4 warps x 16 floats
-    static constexpr uint32_t kLut = kRed + 4 * 16 * 4;                  // 256 x bf16x2: code pair -> values
-    static constexpr uint32_t kPeerMax = kLut + 256 * 4;                 // the other CTA's 16 head maxima
-    static constexpr uint32_t kComb = kPeerMax + 16 * 4;                 // rank 1's accumulator (128 x 16)
-    static constexpr uint32_t kCombS = kComb + 128 * 16 * 4;             // rank 1's 16 sums
-    static constexpr uint32_t kBars = kCombS + 16 * 4;
-    // kfull[4] kempty[4] vfull[6] vempty[6] qready qk_done pvready[2] pvfree[2] pv_done max_ready comb_ready
-    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 2 + 4 + 1 + 2;
+    static constexpr uint32_t kComb = kRed + 4 * 16 * 4;                 // the peer's 8 heads x 128 (staged)
+    static constexpr uint32_t kCombS = kComb + 128 * 8 * 4;              // this CTA's 16 sums, then 16 maxima
+    static constexpr uint32_t kBars = kCombS + 2 * 16 * 4;
+    // kfull[4] kempty[4] vfull[4] vempty[4] qready sready[12] pvready[3] pvfree[3] pv_done comb_ready
+    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 1 + kAttnCtaPages + 2 * kAttnPvBufs + 2;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kPid = kAbort + 4;                         // page ids of the row
@@ -124,25 +127,26 @@ __device__ __forceinline__ uint32_t sw128_bf16_offset(int row, int k, int rows)
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// e2m1 code -> value (format definition: magnitudes 0, 0.5, 1, 1.5, 2, 3,
-// 4, 6, bit 3 the sign); twice the magnitudes are the bytes of one constant.
-__device__ __forceinline__ float e2m1_value(uint32_t code)
+// prmt.b32 in its default mode: result byte i is byte (sel >> 4i) & 7 of
+// {b, a} (a = bytes 0..3), or that byte's sign bit replicated when bit 3 of
+// the selector nibble is set.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
-    const uint32_t twice = static_cast<uint32_t>((0x0C08060403020100ull >> (8u * (code & 7u))) & 0xFFu);
-    const float m = static_cast<float>(twice) * 0.5f;
-    return (code & 8u) ? -m : m;
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
 }
 
-// Bounded wait on a barrier that the peer CTA arrives on remotely (cluster-
-// scope acquire); on timeout it records the site and aborts like
-// wait_bounded.
+// Bounded spin on a barrier that the peer CTA completes remotely (cluster-
+// scope acquire, non-blocking tests); on timeout it records the site and
+// aborts like wait_bounded.
 __device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                                      uint32_t site)
 {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_test_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (mbar_test_wait_cluster(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
@@ -155,48 +159,78 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t pari
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Widen one eighth of a V page (natural layout in smem: 64 code bytes and 4
-// scale bytes per token) into the bf16 V^T operand tile: warp slot wi takes
-// tokens 64 (wi % 2) .. +64 and head dims 32 (wi / 2) .. +32 (one scale
-// group); lane l takes the token pair t0 = 64 (wi % 2) + 2 l, t0 + 1, so the
-// 32 lanes of each store fill one 128-byte V^T row segment (no bank
-// conflicts).  Per head dim the two tokens' codes form
-// one byte that indexes `lut` (both unscaled values as bf16), one packed bf16
-// multiply applies the two tokens' scales (2^(b-127) is bf16 bits b << 7,
-// exact), tokens at or past `valid` are zeroed, and the pair lands in one
-// 4-byte store (adjacent K positions of one V^T row).
-__device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc, uint8_t *vt,
-                                           const __nv_bfloat162 *__restrict__ lut, int wi, int lane, int valid)
+// scale bytes per token) into the bf16 V^T operand tile.  The 256 threads of
+// the 8 widening warps each take one (token pair, 32-dim scale group) cell:
+// lane l of warp slot wi takes group qd = l % 4 and the pair
+// pr = 32 (wi % 2) + (8 qd + l / 4 + 8 (wi / 2)) mod 32 (tokens 2 pr, 2 pr + 1),
+// so that
+//   - the two 16-byte code loads of a warp touch 8 distinct 16-byte bank
+//     groups per quarter-warp (lanes with l & 4 load the odd token first),
+//   - at every store the 32 lanes hold 32 distinct pairs mod 32, whose
+//     4-byte cells of one 128-byte-swizzled V^T row lie in 32 distinct banks.
+// Conversion without a table: an e2m1 code s|E|m (E two bits) placed as
+// bf16 bits (E m) << 6 | s << 15 is the bf16 number 2^-126 times its value
+// (a subnormal for E = 0, exact), so one packed multiply by 2^(b-1) (bf16
+// bits (b + 126) << 7; b = the token's e8m0 byte) gives the scaled value;
+// when some lane has b > 128 that factor overflows bf16, and the warp
+// multiplies by 2^126 and 2^(b-127) instead.  Tokens at or past `valid` get
+// a zero factor.  Each pair lands in one 4-byte store (adjacent K positions
+// of one V^T row).
+__device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc, uint8_t *vt, int wi, int lane,
+                                           int valid)
 {
-    const int t0 = 64 * (wi & 1) + 2 * lane;
-    const int qd = wi >> 1;
-    const uint4 a = *reinterpret_cast<const uint4 *>(vc + t0 * 64 + qd * 16);
-    const uint4 c = *reinterpret_cast<const uint4 *>(vc + (t0 + 1) * 64 + qd * 16);
-    const uint32_t sbits = (static_cast<uint32_t>(vsc[t0 * 4 + qd]) << 7) |
-                           (static_cast<uint32_t>(vsc[(t0 + 1) * 4 + qd]) << 23);
-    const __nv_bfloat162 sc = *reinterpret_cast<const __nv_bfloat162 *>(&sbits);
-    const uint32_t keep = (t0 < valid ? 0x0000FFFFu : 0u) | (t0 + 1 < valid ? 0xFFFF0000u : 0u);
+    const int qd = lane & 3;
+    const int pr = 32 * (wi & 1) + ((8 * qd + (lane >> 2) + 8 * (wi >> 1)) & 31);
+    const int t0 = 2 * pr;
+    const bool odd_first = (lane & 4) != 0;
+    const uint4 f = *reinterpret_cast<const uint4 *>(vc + (t0 + (odd_first ? 1 : 0)) * 64 + qd * 16);
+    const uint4 g = *reinterpret_cast<const uint4 *>(vc + (t0 + (odd_first ? 0 : 1)) * 64 + qd * 16);
+    const uint4 a = odd_first ? g : f;     // token t0
+    const uint4 c = odd_first ? f : g;     // token t0 + 1
+    const uint32_t b0 = t0 < valid ? vsc[t0 * 4 + qd] : 0u;
+    const uint32_t b1 = t0 + 1 < valid ? vsc[(t0 + 1) * 4 + qd] : 0u;
+    const bool one_step = __all_sync(0xffffffffu, b0 <= 128u && b1 <= 128u);
+    uint32_t fbits;
+    if (one_step)
+        fbits = (t0 < valid ? (b0 + 126u) << 7 : 0u) | (t0 + 1 < valid ? (b1 + 126u) << 23 : 0u);
+    else    // 2^(b-127); byte 0 is the subnormal 2^-127 (bits 0x40)
+        fbits = (t0 < valid ? (b0 ? b0 << 7 : 0x40u) : 0u) | (t0 + 1 < valid ? (b1 ? b1 << 23 : 0x400000u) : 0u);
+    const __nv_bfloat162 fac = *reinterpret_cast<const __nv_bfloat162 *>(&fbits);
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
     const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
-    // all 32 table lookups first (nothing stored yet, so they are not held
-    // back behind stores that might alias them), then scale and store
-    __nv_bfloat162 v[32];
+    // v[i]: head dim 32 qd + i of both tokens (t0 in the low half); the
+    // multiply by 0x1040 adds the non-overlapping copies x << 6 and x << 12
+    uint32_t v[32];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        // byte i of lo: codes of head dim 2i of both tokens; of hi: dim 2i+1
-        const uint32_t lo = (wa[w] & 0x0F0F0F0Fu) | ((wc[w] & 0x0F0F0F0Fu) << 4);
-        const uint32_t hi = ((wa[w] >> 4) & 0x0F0F0F0Fu) | (wc[w] & 0xF0F0F0F0u);
+        const uint32_t ae = wa[w] & 0x0F0F0F0Fu, ce = wc[w] & 0x0F0F0F0Fu;                  // even dims
+        const uint32_t ao = (wa[w] >> 4) & 0x0F0F0F0Fu, co = (wc[w] >> 4) & 0x0F0F0F0Fu;    // odd dims
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[8 * w + e] = lut[(((e & 1) ? hi : lo) >> (8 * (e >> 1))) & 0xFFu];
+        for (int j = 0; j < 4; ++j) {
+            // byte j of each token in bytes 0 and 2, zeros in bytes 1 and 3
+            const uint32_t sel = static_cast<uint32_t>(j | ((8 + j) << 4) | ((4 + j) << 8) | ((12 + j) << 12));
+            v[8 * w + 2 * j] = (prmt(ae, ce, sel) * 0x1040u) & 0x81C081C0u;
+            v[8 * w + 2 * j + 1] = (prmt(ao, co, sel) * 0x1040u) & 0x81C081C0u;
+        }
     }
+    // the store address of head dim 32 qd + 8 r + e is row[e] + 1024 r
     const uint32_t cch = static_cast<uint32_t>((t0 & 63) >> 3);    // the pair's 16-byte chunk in a row
     uint8_t *base = vt + (t0 >> 6) * 16384 + (t0 & 7) * 2 + qd * 4096;   // rows 32 qd ..
+    uint8_t *row[8];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int e = i & 7;                                   // head dim 32 qd + i, i % 8 == e
-        const __nv_bfloat162 x = __hmul2(v[i], sc);
-        const uint32_t bits = *reinterpret_cast<const uint32_t *>(&x) & keep;
-        *reinterpret_cast<uint32_t *>(base + (i >> 3) * 1024 + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4)) =
-            bits;
+    for (int e = 0; e < 8; ++e) row[e] = base + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4);
+    if (one_step) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat162 *>(row[i & 7] + (i >> 3) * 1024) =
+                __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i]), fac);
+    } else {
+        const uint32_t k126 = 0x7E807E80u;                             // 2^126 in both halves
+        const __nv_bfloat162 two126 = *reinterpret_cast<const __nv_bfloat162 *>(&k126);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            *reinterpret_cast<__nv_bfloat162 *>(row[i & 7] + (i >> 3) * 1024) =
+                __hmul2(__hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i]), two126), fac);
     }
 }
 
@@ -212,20 +246,19 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     const int64_t item = blockIdx.x / kAttnSplit;          // row * kv_heads + kv head
     const int kvh = static_cast<int>(item % p.kv_heads);
     const uint32_t rank = cluster_ctarank();               // this CTA's half of the row's pages
-    const uint32_t peer = rank ^ 1u;
 
     auto bar = [&](int i) { return sbase + AttnSmem::kBars + 8u * i; };
     auto kfull = [&](int i) { return bar(i); };
     auto kempty = [&](int i) { return bar(kAttnKStages + i); };
     auto vfull = [&](int i) { return bar(2 * kAttnKStages + i); };
     auto vempty = [&](int i) { return bar(2 * kAttnKStages + kAttnVStages + i); };
-    const uint32_t qready = bar(2 * kAttnKStages + 2 * kAttnVStages);
-    const uint32_t qk_done = qready + 8;
-    auto pvready = [&](int i) { return bar(2 * kAttnKStages + 2 * kAttnVStages + 2 + i); };
-    auto pvfree = [&](int i) { return bar(2 * kAttnKStages + 2 * kAttnVStages + 4 + i); };
-    const uint32_t pv_done = bar(2 * kAttnKStages + 2 * kAttnVStages + 6);
-    const uint32_t max_ready = pv_done + 8;                // the peer's maxima have landed (remote arrive)
-    const uint32_t comb_ready = pv_done + 16;              // rank 1's partial results have landed (rank 0)
+    constexpr int kB0 = 2 * kAttnKStages + 2 * kAttnVStages;
+    const uint32_t qready = bar(kB0);
+    auto sready = [&](int j) { return bar(kB0 + 1 + j); };          // page j's scores are in TMEM
+    auto pvready = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + i); };
+    auto pvfree = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + kAttnPvBufs + i); };
+    const uint32_t pv_done = bar(kB0 + 1 + kAttnCtaPages + 2 * kAttnPvBufs);
+    const uint32_t comb_ready = pv_done + 8;               // rank 1's partial results have landed (rank 0)
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
     int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
 
@@ -250,14 +283,13 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         }
         // pvready: the 4 softmax warps (P^T) and the 8 widening warps (V^T)
         mbar_init(qready, 4);
-        mbar_init(qk_done, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int j = 0; j < kAttnCtaPages; ++j) mbar_init(sready(j), 1);
+        for (int i = 0; i < kAttnPvBufs; ++i) {
             mbar_init(pvready(i), 4 + kAttnWidenWarps);
             mbar_init(pvfree(i), 1);
         }
         mbar_init(pv_done, 1);
-        mbar_init(max_ready, 1);
-        mbar_init(comb_ready, 4);
+        mbar_init(comb_ready, 4);               // the peer's 4 softmax warps (remote)
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -271,12 +303,6 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 id = static_cast<int32_t>(raw);
         }
         pids[threadIdx.x] = id;
-    }
-    if (threadIdx.x < 256) {
-        // code pair (low nibble: token t, high nibble: token t+1) -> their
-        // unscaled e2m1 values as bf16 (exact)
-        const __nv_bfloat162 v = __floats2bfloat162_rn(e2m1_value(threadIdx.x & 15u), e2m1_value(threadIdx.x >> 4));
-        reinterpret_cast<__nv_bfloat162 *>(smem + AttnSmem::kLut)[threadIdx.x] = v;
     }
     if (warp == 4 && lane == 0) {
         prefetch_tmap(&tmap_k);
@@ -364,13 +390,12 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 for (uint32_t k = 0; k < 4; ++k)
                     tc_mma_mx_ss(d, kdesc + 2 * k, qdesc + 2 * k, attn_idesc_qk(k), sfa, sfb, k > 0 ? 1u : 0u);
                 tc_commit(kempty(s));
+                tc_commit(sready(j));
             }
             __syncwarp();
         }
-        if (elect_one()) tc_commit(qk_done);
-        __syncwarp();
         for (int j = 0; j < npages && ok; ++j) {
-            const int b = j & 1, u = j >> 1;
+            const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
             if (!__all_sync(0xffffffffu, wait_bounded(pvready(b), u & 1, abort_flag, kSiteAttnMma))) {
                 ok = false;
                 break;
@@ -398,19 +423,19 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         __syncwarp();
     } else if (warp >= 6) {
         // ---------------------------------------------------------- V widening --
-        // warps 6-9 and 11-14 widen 16 tokens of each page each (warp 10 is
-        // the V copy warp above, warp 15 has no role)
+        // warps 6-9 and 11-14 widen one eighth of each page each (warp 10
+        // is the V copy warp above, warp 15 has no role)
         if (warp == 15) goto done;
         for (int j = 0; j < npages; ++j) {
-            const int b = j & 1, u = j >> 1;
+            const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
             const int vs = j % kAttnVStages;
             if (!__all_sync(0xffffffffu,
                             (u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi)) &&
                                 wait_bounded(vfull(vs), (j / kAttnVStages) & 1, abort_flag, kSiteAttnEpi)))
                 break;
             attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
-                       smem + AttnSmem::kVt + b * 32768, reinterpret_cast<const __nv_bfloat162 *>(smem + AttnSmem::kLut),
-                       warp < 10 ? warp - 6 : warp - 7, lane, ctx - (pbase + j) * kPage);
+                       smem + AttnSmem::kVt + b * 32768, warp < 10 ? warp - 6 : warp - 7, lane,
+                       ctx - (pbase + j) * kPage);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -441,17 +466,20 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             M[h] = -INFINITY;
             S[h] = 0.0f;
         }
-        bool ok = __all_sync(0xffffffffu, wait_bounded(qk_done, 0, abort_flag, kSiteAttnEpi));
-        if (ok) {
+        // pass A: this CTA's per-head max over its valid tokens, page by page
+        // as the QK products complete
+        bool ok = true;
+        for (int j = 0; j < npages; ++j) {
+            if (!__all_sync(0xffffffffu, wait_bounded(sready(j), 0, abort_flag, kSiteAttnEpi))) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            // pass A: per-head max over valid tokens
-            for (int j = 0; j < npages; ++j) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
-                if ((pbase + j) * kPage + tok_m < ctx) {
+            uint32_t v[16];
+            tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
+            if ((pbase + j) * kPage + tok_m < ctx) {
 #pragma unroll
-                    for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __uint_as_float(v[h]) * p.softmax_scale);
-                }
+                for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __uint_as_float(v[h]) * p.softmax_scale);
             }
         }
         // (the named-barrier syncs below run on every path, so the four
@@ -470,29 +498,10 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         for (int h = 0; h < kAttnN; ++h)
             M[h] = fmaxf(fmaxf(red[h], red[kAttnN + h]), fmaxf(red[2 * kAttnN + h], red[3 * kAttnN + h]));
         epi_bar_sync();
-        // The row's max over both CTAs: lane 0 of warp 0 stores this CTA's
-        // maxima into the peer's shared memory and arrives on the peer's
-        // barrier (release, cluster scope); every softmax warp then waits for
-        // the peer's maxima (acquire) and takes the larger value per head.
-        if (warp == 0 && lane == 0) {
-            const uint32_t dst = cluster_map(sbase + AttnSmem::kPeerMax, peer);
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h) st_cluster_f32(dst + 4u * h, M[h]);
-            mbar_arrive_remote(cluster_map(max_ready, peer));
-        }
-        {
-            const bool got = __all_sync(0xffffffffu, wait_cluster_bounded(max_ready, 0, abort_flag, kSiteAttnEpi));
-            if (got) {
-                const float *pm = reinterpret_cast<const float *>(smem + AttnSmem::kPeerMax);
-#pragma unroll
-                for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], pm[h]);
-            }
-            ok = ok && got;
-        }
         // pass B: per page P^T and V^T for the PV MMA
         constexpr float kLog2e = 1.4426950408889634f;
         for (int j = 0; j < npages && ok; ++j) {
-            const int b = j & 1, u = j >> 1;
+            const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
             if (!__all_sync(0xffffffffu,
                             u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi))) {
                 ok = false;
@@ -542,37 +551,57 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
 #pragma unroll
             for (int h = 0; h < kAttnN; ++h) acc[h] = 0u;
         }
-        if (rank != 0) {
-            // hand this CTA's accumulator column and sums to rank 0
-            const uint32_t dst = cluster_map(sbase + AttnSmem::kComb + m * 64u, 0);
+        // Combine the two halves: rank r finalises heads 8r .. 8r+7.  Each
+        // CTA stages the peer's heads of its accumulator (head-major) and
+        // all its sums and maxima in its own shared memory, arrives on the
+        // peer's comb_ready (release, cluster scope), waits for the peer's
+        // arrival on its own, then reads the peer's staged values (one
+        // coalesced 128-byte cluster load per warp and head), rescales both
+        // halves to the row's max, adds, normalises and stores bf16 (a half
+        // with no weight contributes nothing).
+        {
+            float *cm = reinterpret_cast<float *>(smem + AttnSmem::kComb);
 #pragma unroll
-            for (int h = 0; h < kAttnN; ++h) st_cluster_f32(dst + 4u * h, __uint_as_float(acc[h]));
-            if (threadIdx.x == 0) {
-                const uint32_t ds = cluster_map(sbase + AttnSmem::kCombS, 0);
+            for (int h = 0; h < kAttnN; ++h)
+                if ((h >> 3) != static_cast<int>(rank)) cm[(h & 7) * 128 + m] = __uint_as_float(acc[h]);
+            if (threadIdx.x < kAttnN) {
+                float *cs = reinterpret_cast<float *>(smem + AttnSmem::kCombS);
+                float sv = 0.0f, mv = 0.0f;
 #pragma unroll
-                for (int h = 0; h < kAttnN; ++h) st_cluster_f32(ds + 4u * h, S[h]);
+                for (int h = 0; h < kAttnN; ++h) {
+                    sv = h == m ? S[h] : sv;
+                    mv = h == m ? M[h] : mv;
+                }
+                cs[m] = sv;
+                cs[kAttnN + m] = mv;
             }
             fence_cluster();
             __syncwarp();
-            if (lane == 0) mbar_arrive_remote(cluster_map(comb_ready, 0));
-        } else {
-            // rank 0: add rank 1's partial results, normalise, store bf16
-            float a[kAttnN];
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h) a[h] = __uint_as_float(acc[h]);
+            if (lane == 0) mbar_arrive_remote(cluster_map(comb_ready, rank ^ 1u));
             if (__all_sync(0xffffffffu, wait_cluster_bounded(comb_ready, 0, abort_flag, kSiteAttnEpi))) {
-                const float *cm = reinterpret_cast<const float *>(smem + AttnSmem::kComb) + m * kAttnN;
-                const float *cs = reinterpret_cast<const float *>(smem + AttnSmem::kCombS);
+                const uint32_t pm = cluster_map(sbase + AttnSmem::kComb + 4u * m, rank ^ 1u);
+                const uint32_t ps = cluster_map(sbase + AttnSmem::kCombS, rank ^ 1u);
+                float a1[8], s1[8], m1[8];
 #pragma unroll
-                for (int h = 0; h < kAttnN; ++h) {
-                    a[h] += cm[h];
-                    S[h] += cs[h];
+                for (int i = 0; i < 8; ++i) {
+                    a1[i] = ld_cluster_f32(pm + 512u * i);
+                    s1[i] = ld_cluster_f32(ps + 4u * (8 * rank + i));
+                    m1[i] = ld_cluster_f32(ps + 4u * (kAttnN + 8 * rank + i));
+                }
+                __nv_bfloat16 *o = p.out + (item * G) * kDim;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    // this thread's own values of head 8 rank + i (static register indexes)
+                    const float a0 = __uint_as_float(rank ? acc[8 + i] : acc[i]);
+                    const float s0 = rank ? S[8 + i] : S[i], m0 = rank ? M[8 + i] : M[i];
+                    const float mx = s1[i] > 0.0f && m1[i] > m0 ? m1[i] : m0;
+                    const float f0 = s0 > 0.0f ? exp2f((m0 - mx) * kLog2e) : 0.0f;
+                    const float f1 = s1[i] > 0.0f ? exp2f((m1[i] - mx) * kLog2e) : 0.0f;
+                    const float a = a0 * f0 + a1[i] * f1, sum = s0 * f0 + s1[i] * f1;
+                    const int h = 8 * static_cast<int>(rank) + i;
+                    if (h < G) o[h * kDim + m] = __float2bfloat16_rn(sum > 0.0f ? __fdividef(a, sum) : 0.0f);
                 }
             }
-            __nv_bfloat16 *o = p.out + (item * G) * kDim;
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h)
-                if (h < G) o[h * kDim + m] = __float2bfloat16_rn(S[h] > 0.0f ? a[h] / S[h] : 0.0f);
         }
     }
 

@@ -456,9 +456,12 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+// Load from the shared memory of a CTA of the cluster.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
 {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // Arrive on an mbarrier of another CTA of the cluster, releasing this
@@ -468,13 +471,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Phase test with cluster-scope acquire (sees what remote arrivals released).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+// Non-blocking phase test with cluster-scope acquire: sees what remote
+// arrivals released; a spinning waiter notices a remote completion at once.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)

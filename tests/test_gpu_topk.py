@@ -57,11 +57,21 @@ def test_scorer_then_topk_prefill_ragged(k, local, groups):
     _check_chain(w, k, local, groups)
 
 
-@pytest.mark.parametrize("k,local,groups", [(8, 1, 1), (64, 2, 2)])
+@pytest.mark.parametrize("k,local,groups", [(8, 1, 1), (64, 2, 2), (4, 1, 64), (16, 2, 32)])
 def test_scorer_then_topk_decode_ragged(k, local, groups):
+    """Decode rows, including 32 and 64 head groups (one or two heads a
+    group)."""
     w = W.make_workload("tkd", seed=81, q_lens=None, seq_lens=[1, 128, 129, 5000, 0, 16384, 77], decode=True,
                         pool_pages=300, layout="split", k_data_page_stride=8320, k_scale_page_stride=576)
     _check_chain(w, k, local, groups)
+
+
+def test_scorer_then_topk_decode_many_rows():
+    """400 decode rows of mixed lengths, one CTA each."""
+    g = np.random.default_rng(84)
+    lens = [int(x) for x in g.integers(0, 3000, size=400)]
+    w = W.make_workload("tkm", seed=84, q_lens=None, seq_lens=lens, decode=True, pool_pages=10000)
+    _check_chain(w, 6, 1, 1)
 
 
 @pytest.mark.parametrize("P_tokens,offset", [(1100, 0), (4096, 1), (16384, 0)])
