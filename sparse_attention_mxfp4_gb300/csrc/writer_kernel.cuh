@@ -93,7 +93,25 @@ __global__ void __launch_bounds__(256) mx4_write_index_k_kernel(const __grid_con
         int64_t page = 0, tok = 0;
         uint4 x[4] = {};
         if (gi < n_threads) {
+            // the key row is read together with its slot (a padding row is
+            // read too and then ignored), so the two loads overlap
             const int64_t slot = __ldg(p.slot_mapping + t);
+            const uint16_t *src = p.k + t * p.k_row_stride + 32 * g;
+            if (p.vec) {
+                const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[i] = __ldcs(s4 + i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        v[j] = static_cast<uint32_t>(__ldcs(src + 8 * i + 2 * j)) |
+                               (static_cast<uint32_t>(__ldcs(src + 8 * i + 2 * j + 1)) << 16);
+                    x[i] = make_uint4(v[0], v[1], v[2], v[3]);
+                }
+            }
             if (slot >= 0) {
                 page = slot >> 7;
                 tok = slot & 127;
@@ -101,22 +119,6 @@ __global__ void __launch_bounds__(256) mx4_write_index_k_kernel(const __grid_con
                     if (g == 0) atomicOr(&g_mx4_device_status, 0x1u);
                 } else {
                     write = true;
-                    const uint16_t *src = p.k + t * p.k_row_stride + 32 * g;
-                    if (p.vec) {
-                        const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) x[i] = __ldcs(s4 + i);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t v[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                v[j] = static_cast<uint32_t>(__ldcs(src + 8 * i + 2 * j)) |
-                                       (static_cast<uint32_t>(__ldcs(src + 8 * i + 2 * j + 1)) << 16);
-                            x[i] = make_uint4(v[0], v[1], v[2], v[3]);
-                        }
-                    }
                 }
             }
         }
