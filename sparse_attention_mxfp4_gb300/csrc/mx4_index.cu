@@ -280,8 +280,10 @@ mx4_status topk_launch(const float *scores, const int32_t *block_table, const in
             st.sm_count = n;
         }
         if (!st.topk_attr_set[kDecode ? 1 : 0]) {
-            if (cudaFuncSetAttribute(mx4::mx4_topk_kernel<kDecode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     mx4::kTopkMaxPages * 4) != cudaSuccess)
+            if (cudaFuncSetAttribute(mx4::mx4_topk_kernel<kDecode, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     mx4::kTopkMaxPages * 4) != cudaSuccess ||
+                cudaFuncSetAttribute(mx4::mx4_topk_kernel<kDecode, mx4::kTopkSplit>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, mx4::kTopkMaxPages * 4) != cudaSuccess)
                 return MX4_ERR_CUDA;
             st.topk_attr_set[kDecode ? 1 : 0] = true;
         }
@@ -305,12 +307,31 @@ mx4_status topk_launch(const float *scores, const int32_t *block_table, const in
     p.groups = kv_groups;
     p.vec = aligned(scores, 16) && (P % 4) == 0;
     p.num_items = static_cast<int64_t>(num_seqs) * p.rows_per_seq * kv_groups;
-    // one CTA per (row, group) item, at most 8 resident per SM, grid-stride
-    const int64_t grid = p.num_items < 8LL * sms ? p.num_items : 8LL * sms;
     const size_t smem = static_cast<size_t>(P > 0 ? P : 1) * 4;
     cudaGetLastError();
-    mx4::mx4_topk_kernel<kDecode><<<static_cast<unsigned>(grid), mx4::kTopkThreads, smem,
-                                    static_cast<cudaStream_t>(stream)>>>(p);
+    if (p.num_items < 2LL * sms) {
+        // few items: one cluster of kTopkSplit CTAs per item, so a row's
+        // score reads are spread over kTopkSplit SMs
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(p.num_items * mx4::kTopkSplit), 1, 1);
+        cfg.blockDim = dim3(mx4::kTopkThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = mx4::kTopkSplit;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, mx4::mx4_topk_kernel<kDecode, mx4::kTopkSplit>, p) != cudaSuccess)
+            return MX4_ERR_CUDA;
+    } else {
+        // one CTA per (row, group) item, at most 8 resident per SM, grid-stride
+        const int64_t grid = p.num_items < 8LL * sms ? p.num_items : 8LL * sms;
+        mx4::mx4_topk_kernel<kDecode, 1><<<static_cast<unsigned>(grid), mx4::kTopkThreads, smem,
+                                           static_cast<cudaStream_t>(stream)>>>(p);
+    }
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 

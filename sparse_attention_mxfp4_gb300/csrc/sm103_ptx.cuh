@@ -456,6 +456,19 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank)
     return r;
 }
 
+// Stores into the shared memory of a CTA of the cluster (the vector form
+// wants a 16-byte aligned address).
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4_u32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Load from the shared memory of a CTA of the cluster.
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr)
 {

@@ -12,21 +12,29 @@
 //   emit      = physical ids of forced + chosen in ascending page order,
 //               -1 up to topk, and the count.
 //
-// One CTA per (row, group) work item, grid-stride.  The values become
+// One CTA per (row, group) work item, grid-stride; or, when there are fewer
+// items than two per SM, one cluster of kTopkSplit CTAs per item: each CTA
+// of the cluster computes the keys of a quarter of the pages and stores them
+// into the shared memory of the cluster's rank 0, which alone selects (a
+// row's score reads are then spread over four SMs).  The values become
 // order-preserving 32-bit keys in shared memory; an exact MSB-first radix
-// select (4 passes of 8 bits, shared-memory histograms) finds the m-th
-// largest key T and how many keys equal to T are taken; one ordered pass over
-// contiguous per-thread page ranges (a block-wide exclusive scan) ranks the
-// ties by page index and compacts the selected pages in ascending order.
-// Reading the block scores is the bulk of the work: 4 B per (head, page).
+// select (4 passes of 8 bits, shared-memory histograms fed by warp-aggregated
+// atomics) finds the m-th largest key T and how many keys equal to T are
+// taken; one ordered pass over contiguous per-thread page ranges (a
+// block-wide exclusive scan) ranks the ties by page index and compacts the
+// selected pages in ascending order.  Reading the block scores is the bulk of
+// the work: 4 B per (head, page).
 #pragma once
 
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
+
 namespace mx4 {
 
 constexpr int kTopkThreads = 256;
+constexpr int kTopkSplit = 4;          // CTAs (one cluster) per item when items are few
 constexpr int kTopkMaxPages = 16384;   // ceil(max_seq_len / 128) supported (2M tokens)
 
 struct TopkParams {
@@ -83,20 +91,26 @@ __device__ __forceinline__ int topk_block_scan(int x, int *buf, int &total)
     return base + inc - x;
 }
 
-template <bool kDecode>
+// kSplit == 1: grid-stride over items.  kSplit > 1: launched as clusters of
+// kSplit CTAs, exactly one item per cluster (grid = items x kSplit).
 // (at least 4 resident blocks per SM: up to 64 registers a thread)
+template <bool kDecode, int kSplit>
 __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_constant__ TopkParams p)
 {
-    extern __shared__ uint32_t topk_smem[];
-    uint32_t *keys = topk_smem;                                 // [num_pages]
+    extern __shared__ __align__(16) uint32_t topk_smem[];
+    uint32_t *keys = topk_smem;                                 // [num_pages], 16-byte aligned
     __shared__ int hist[256];
     __shared__ int scan_buf[8];
     __shared__ uint32_t sel_prefix;
     __shared__ int sel_remaining;
+    __shared__ int sel_done;
 
     const int tid = threadIdx.x;
     const int hg = 64 / p.groups;
-    for (int64_t item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    const uint32_t rank = kSplit > 1 ? cluster_ctarank() : 0u;
+    const int64_t first = kSplit > 1 ? static_cast<int64_t>(blockIdx.x / kSplit) : static_cast<int64_t>(blockIdx.x);
+    const int64_t step = kSplit > 1 ? p.num_items : static_cast<int64_t>(gridDim.x);
+    for (int64_t item = first; item < p.num_items; item += step) {
         const int g = static_cast<int>(item % p.groups);
         const int64_t rest = item / p.groups;
         const int pos = static_cast<int>(rest % p.rows_per_seq);
@@ -124,44 +138,107 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
         // (a warp reads 32 consecutive pages of one head per load; the head
         // loop is unrolled so many independent loads are in flight)
         const float *src = p.scores + (row * 64 + static_cast<int64_t>(g) * hg) * p.num_pages;
-        if (p.vec) {
-            const int64_t hstride = p.num_pages >> 2;                // float4 per head
-            const int nq = (nc + 3) >> 2;
-            for (int qd = tid; qd < nq; qd += kTopkThreads) {
-                const float4 *s4 = reinterpret_cast<const float4 *>(src) + qd;
-                float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (kSplit > 1) {
+            // Rank r takes the r-th share of the quads (pages); four slices
+            // of 64 threads split the heads, so each thread keeps all its
+            // loads in flight at once, and fold their maxima into this CTA's
+            // keys with atomicMax (keys start at 0, below every value's key);
+            // the other ranks then copy their share into rank 0's keys.
+            const int sl = tid >> 6, st = tid & 63;
+            const int hper = (hg + 3) >> 2;
+            const int h0 = sl * hper < hg ? sl * hper : hg;
+            const int h1 = h0 + hper < hg ? h0 + hper : hg;
+            const uint32_t keys0 = cluster_map(static_cast<uint32_t>(__cvta_generic_to_shared(keys)), 0);
+            if (p.vec) {
+                const int64_t hstride = p.num_pages >> 2;            // float4 per head
+                const int nq = (nc + 3) >> 2;
+                const int share = (nq + kSplit - 1) / kSplit;
+                const int q0 = static_cast<int>(rank) * share < nq ? static_cast<int>(rank) * share : nq;
+                const int q1 = q0 + share < nq ? q0 + share : nq;
+                for (int j = 4 * q0 + tid; j < 4 * q1; j += kTopkThreads) keys[j] = 0u;   // (P % 4 == 0)
+                __syncthreads();
+                for (int qd = q0 + st; qd < q1; qd += 64) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src) + qd;
+                    float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll 16
-                for (int h = 0; h < hg; ++h) {
-                    const float4 x = __ldg(s4 + h * hstride);
-                    m.x = fmaxf(m.x, x.x);
-                    m.y = fmaxf(m.y, x.y);
-                    m.z = fmaxf(m.z, x.z);
-                    m.w = fmaxf(m.w, x.w);
+                    for (int h = h0; h < h1; ++h) {
+                        const float4 x = __ldg(s4 + h * hstride);
+                        m.x = fmaxf(m.x, x.x);
+                        m.y = fmaxf(m.y, x.y);
+                        m.z = fmaxf(m.z, x.z);
+                        m.w = fmaxf(m.w, x.w);
+                    }
+                    atomicMax(&keys[4 * qd + 0], topk_key(m.x));
+                    atomicMax(&keys[4 * qd + 1], topk_key(m.y));
+                    atomicMax(&keys[4 * qd + 2], topk_key(m.z));
+                    atomicMax(&keys[4 * qd + 3], topk_key(m.w));
                 }
-                // pages past nc (up to the quad's end, < P) get keys never read
-                keys[4 * qd + 0] = topk_key(m.x);
-                keys[4 * qd + 1] = topk_key(m.y);
-                keys[4 * qd + 2] = topk_key(m.z);
-                keys[4 * qd + 3] = topk_key(m.w);
-            }
-        } else {
-            for (int j = tid; j < nc; j += kTopkThreads) {
-                float m = -INFINITY;
+                __syncthreads();
+                if (rank != 0)
+                    for (int qd = q0 + tid; qd < q1; qd += kTopkThreads)
+                        st_cluster_v4_u32(keys0 + 16u * qd, keys[4 * qd], keys[4 * qd + 1], keys[4 * qd + 2],
+                                          keys[4 * qd + 3]);
+            } else {
+                const int share = (nc + kSplit - 1) / kSplit;
+                const int j0 = static_cast<int>(rank) * share < nc ? static_cast<int>(rank) * share : nc;
+                const int j1 = j0 + share < nc ? j0 + share : nc;
+                for (int j = j0 + tid; j < j1; j += kTopkThreads) keys[j] = 0u;
+                __syncthreads();
+                for (int j = j0 + st; j < j1; j += 64) {
+                    float m = -INFINITY;
 #pragma unroll 16
-                for (int h = 0; h < hg; ++h) m = fmaxf(m, __ldg(src + static_cast<int64_t>(h) * p.num_pages + j));
-                keys[j] = topk_key(m);
+                    for (int h = h0; h < h1; ++h) m = fmaxf(m, __ldg(src + static_cast<int64_t>(h) * p.num_pages + j));
+                    atomicMax(&keys[j], topk_key(m));
+                }
+                __syncthreads();
+                if (rank != 0)
+                    for (int j = j0 + tid; j < j1; j += kTopkThreads) st_cluster_u32(keys0 + 4u * j, keys[j]);
             }
+            // every rank's keys have landed in rank 0 (release / acquire);
+            // the other ranks are done with the item
+            cluster_sync();
+            if (rank != 0) continue;
+        } else {
+            if (p.vec) {
+                const int64_t hstride = p.num_pages >> 2;            // float4 per head
+                const int nq = (nc + 3) >> 2;
+                for (int qd = tid; qd < nq; qd += kTopkThreads) {
+                    const float4 *s4 = reinterpret_cast<const float4 *>(src) + qd;
+                    float4 m = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll 16
+                    for (int h = 0; h < hg; ++h) {
+                        const float4 x = __ldg(s4 + h * hstride);
+                        m.x = fmaxf(m.x, x.x);
+                        m.y = fmaxf(m.y, x.y);
+                        m.z = fmaxf(m.z, x.z);
+                        m.w = fmaxf(m.w, x.w);
+                    }
+                    // pages past nc (up to the quad's end, < P) get keys never read
+                    keys[4 * qd + 0] = topk_key(m.x);
+                    keys[4 * qd + 1] = topk_key(m.y);
+                    keys[4 * qd + 2] = topk_key(m.z);
+                    keys[4 * qd + 3] = topk_key(m.w);
+                }
+            } else {
+                for (int j = tid; j < nc; j += kTopkThreads) {
+                    float m = -INFINITY;
+#pragma unroll 16
+                    for (int h = 0; h < hg; ++h) m = fmaxf(m, __ldg(src + static_cast<int64_t>(h) * p.num_pages + j));
+                    keys[j] = topk_key(m);
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
 
         // --- radix select of the want-th largest key (only when some are left out) ---
-        uint32_t T = 0;
+        uint32_t T = 0, Tmask = 0xFFFFFFFFu;
         int take_eq = 0;
         const bool all = want >= nc;
         if (!all && want > 0) {
             if (tid == 0) {
                 sel_prefix = 0;
                 sel_remaining = want;
+                sel_done = 0;
             }
             uint32_t mask = 0;
             for (int shift = 24; shift >= 0; shift -= 8) {
@@ -194,12 +271,13 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                     if (tid == first) {
                         // walk this lane's 8 buckets downwards to the one
                         // that reaches rem (unrolled: c stays in registers)
-                        int acc = before, pick = 7;
+                        int acc = before, pick = 7, picked = c[7];
                         bool found = false;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             if (!found && acc + c[i] >= rem) {
                                 pick = i;
+                                picked = c[i];
                                 found = true;
                             } else if (!found) {
                                 acc += c[i];
@@ -208,13 +286,18 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                         const uint32_t digit = 255u - 8u * tid - pick;
                         sel_prefix = prefix | (digit << shift);
                         sel_remaining = rem - acc;
+                        // every key of the chosen bucket is taken: the
+                        // prefix alone decides, no further pass
+                        sel_done = rem - acc == picked ? 1 : 0;
                     }
                 }
                 __syncthreads();
                 mask |= 0xFFu << shift;
+                if (sel_done) break;                 // (uniform: read after the barrier)
             }
             T = sel_prefix;
-            take_eq = sel_remaining;                 // keys equal to T to take, lowest pages first
+            Tmask = mask;
+            take_eq = sel_remaining;                 // keys equal to T (under Tmask) to take, lowest pages first
         }
 
         // --- ordered compaction of the selected pages ---
@@ -224,7 +307,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
         const int j1 = j0 + C < nl ? j0 + C : nl;
         int n_eq = 0;
         if (!all && want > 0)
-            for (int j = j0; j < j1 && j < nc; ++j) n_eq += keys[j] == T;
+            for (int j = j0; j < j1 && j < nc; ++j) n_eq += (keys[j] & Tmask) == T;
         int tot_eq;
         int eq_before = topk_block_scan(n_eq, scan_buf, tot_eq);
         // page j is taken when it is in the forced tail, or all candidates
@@ -237,7 +320,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
             for (int j = j0; j < j1; ++j) {
                 bool take = j >= nc || all;
                 if (!take && pick_some) {
-                    const uint32_t k = keys[j];
+                    const uint32_t k = keys[j] & Tmask;
                     take = k > T || (k == T && r < take_eq);
                     r += k == T;
                 }
@@ -253,7 +336,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
             for (int j = j0; j < j1; ++j) {
                 bool take = j >= nc || all;
                 if (!take && pick_some) {
-                    const uint32_t k = keys[j];
+                    const uint32_t k = keys[j] & Tmask;
                     take = k > T || (k == T && r < take_eq);
                     r += k == T;
                 }
