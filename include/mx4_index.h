@@ -43,7 +43,11 @@
  * Streams: calls enqueue on `stream` (a cudaStream_t; NULL = legacy default
  * stream), never synchronise, and read no device data on the host, so a
  * sequence of calls can be captured in a CUDA graph after a first
- * (warm-up) call on the device.
+ * (warm-up) call on the device.  The scorer, writer and attention kernels
+ * are launched as programmatic dependent launches: their set-up (barriers,
+ * tensor memory, descriptor prefetch) may overlap the end of the previous
+ * kernel of the stream, but every global read and write waits for that
+ * kernel to complete, so stream order semantics are unchanged.
  *
  * Errors: host-checkable faults return a status before anything is
  * launched.  A call with no output cell (num_seqs, max_seq_len or, for

@@ -262,14 +262,6 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
     int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
 
-    int ctx = p.context_lens[item];
-    if (ctx > p.width * kPage) ctx = p.width * kPage;
-    if (ctx < 0) ctx = 0;
-    const int npages_all = (ctx + kPage - 1) / kPage;
-    const int half = (npages_all + 1) / 2;
-    const int pbase = rank == 0 ? 0 : half;                // first page of this CTA
-    const int npages = rank == 0 ? half : npages_all - half;   // pages of this CTA
-
     if (threadIdx.x == 0) {
         // arrivals: TMA / commits count 1; the 4 softmax warps arrive on
         // qready and pvready, the 8 widening warps on vempty and pvready
@@ -293,6 +285,28 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         *abort_flag = 0;
         fence_mbar_init();
     }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_ks);
+    }
+    if (warp == 5) {
+        tmem_alloc(sbase + AttnSmem::kTmemSlot, 512);
+        tmem_relinquish();
+    }
+    // The set-up above touches no global memory, so under a programmatic
+    // dependent launch it overlaps the previous kernel's tail; every global
+    // access follows the wait.
+    griddep_launch_dependents();
+    griddep_wait();
+
+    int ctx = p.context_lens[item];
+    if (ctx > p.width * kPage) ctx = p.width * kPage;
+    if (ctx < 0) ctx = 0;
+    const int npages_all = (ctx + kPage - 1) / kPage;
+    const int half = (npages_all + 1) / 2;
+    const int pbase = rank == 0 ? 0 : half;                // first page of this CTA
+    const int npages = rank == 0 ? half : npages_all - half;   // pages of this CTA
+
     if (threadIdx.x < kAttnMaxPages) {
         int32_t id = 0;
         if (static_cast<int>(threadIdx.x) >= pbase && static_cast<int>(threadIdx.x) < pbase + npages) {
@@ -303,14 +317,6 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 id = static_cast<int32_t>(raw);
         }
         pids[threadIdx.x] = id;
-    }
-    if (warp == 4 && lane == 0) {
-        prefetch_tmap(&tmap_k);
-        prefetch_tmap(&tmap_ks);
-    }
-    if (warp == 5) {
-        tmem_alloc(sbase + AttnSmem::kTmemSlot, 512);
-        tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();

@@ -59,6 +59,38 @@ constexpr int kernel_index()
 }
 
 // Per-device one-time setup: SM count and the dynamic smem opt-in.
+// Launch with clusters of `cluster` CTAs (when > 1) and, when `pdl`, with
+// programmatic stream serialization: such kernels wait for the previous
+// kernel of the stream before their first global access, so their set-up
+// overlaps its tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                      unsigned cluster, bool pdl, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <bool kDecode, bool kLogits, bool kFp8>
 mx4_status device_setup(int *sm_count)
 {
@@ -242,8 +274,9 @@ mx4_status launch(const Args &a)
     // units); each CTA takes a contiguous, equal share of the units.
     const int64_t grid = num_units < sm_count ? num_units : sm_count;
     cudaGetLastError();   // clear a stale error so the check below is ours
-    mx4::mx4_score_kernel<kDecode, kLogits, kFp8>
-        <<<static_cast<unsigned>(grid), mx4::kThreads, SmemLayout::kAlloc, a.stream>>>(tmap_k, tmap_s, p);
+    if (launch_ex(mx4::mx4_score_kernel<kDecode, kLogits, kFp8>, static_cast<unsigned>(grid), mx4::kThreads,
+                  SmemLayout::kAlloc, a.stream, 1, true, tmap_k, tmap_s, p) != cudaSuccess)
+        return MX4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 
@@ -312,19 +345,11 @@ mx4_status topk_launch(const float *scores, const int32_t *block_table, const in
     if (p.num_items < 2LL * sms) {
         // few items: one cluster of kTopkSplit CTAs per item, so a row's
         // score reads are spread over kTopkSplit SMs
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(p.num_items * mx4::kTopkSplit), 1, 1);
-        cfg.blockDim = dim3(mx4::kTopkThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = static_cast<cudaStream_t>(stream);
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = mx4::kTopkSplit;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, mx4::mx4_topk_kernel<kDecode, mx4::kTopkSplit>, p) != cudaSuccess)
+        // (a plain launch: with a programmatic dependent launch the decode
+        // selection measured slower)
+        if (launch_ex(mx4::mx4_topk_kernel<kDecode, mx4::kTopkSplit>,
+                      static_cast<unsigned>(p.num_items * mx4::kTopkSplit), mx4::kTopkThreads, smem,
+                      static_cast<cudaStream_t>(stream), mx4::kTopkSplit, false, p) != cudaSuccess)
             return MX4_ERR_CUDA;
     } else {
         // one CTA per (row, group) item, at most 8 resident per SM, grid-stride
@@ -562,9 +587,11 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     p.softmax_scale = softmax_scale;
     // one cluster of kAttnSplit CTAs per (row, KV head)
     cudaGetLastError();
-    mx4::mx4_attn_kernel<<<static_cast<unsigned>(num_rows * kv_heads * mx4::kAttnSplit), mx4::kAttnThreads,
-                           mx4::AttnSmem::kAlloc,
-                           static_cast<cudaStream_t>(stream)>>>(tmap_k, tmap_ks, p);
+    // (the cluster shape comes from the kernel's own attribute)
+    if (launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(num_rows * kv_heads * mx4::kAttnSplit),
+                  mx4::kAttnThreads, mx4::AttnSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k,
+                  tmap_ks, p) != cudaSuccess)
+        return MX4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 
@@ -622,7 +649,9 @@ mx4_status mx4_index_k_write(const void *k, int64_t num_tokens, int64_t k_row_st
     int64_t blocks = (num_tokens * 4 + 255) / 256;
     if (blocks > 8LL * sms) blocks = 8LL * sms;
     cudaGetLastError();
-    mx4::mx4_write_index_k_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(p);
+    if (launch_ex(mx4::mx4_write_index_k_kernel, static_cast<unsigned>(blocks), 256, 0,
+                  static_cast<cudaStream_t>(stream), 1, true, p) != cudaSuccess)
+        return MX4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 

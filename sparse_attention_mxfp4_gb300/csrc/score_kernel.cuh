@@ -404,6 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // The set-up above touches no global memory, so under a programmatic
+    // dependent launch it overlaps the previous kernel's last CTAs; every
+    // global read and write comes after the wait.  The next kernel may start
+    // its own set-up as this grid's CTAs retire.
+    griddep_launch_dependents();
+    griddep_wait();
 
     const int64_t u_begin = static_cast<int64_t>(blockIdx.x) * p.num_units / gridDim.x;
     const int64_t u_end = static_cast<int64_t>(blockIdx.x + 1) * p.num_units / gridDim.x;

@@ -499,6 +499,17 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t pa
     return ok != 0;
 }
 
+// Programmatic dependent launch: allow the next kernel of the stream to
+// begin launching (its CTAs take SMs as this grid's CTAs retire) ...
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ... and wait until the kernel before this one has completed and its
+// memory operations are visible (returns at once without such a launch).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // All threads of all CTAs of the cluster (release / acquire).
 __device__ __forceinline__ void cluster_sync()
 {

@@ -22,6 +22,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
+
 namespace mx4 {
 
 struct WriteParams {
@@ -82,6 +84,9 @@ __device__ __forceinline__ uint32_t absmax_bits(uint4 x, uint32_t m)
 
 __global__ void __launch_bounds__(256) mx4_write_index_k_kernel(const __grid_constant__ WriteParams p)
 {
+    // programmatic dependent launch: every global access follows the wait
+    griddep_launch_dependents();
+    griddep_wait();
     // Warp-uniform trip count: every lane reaches the shuffles below.
     const int64_t n_threads = p.num_tokens * 4;
     const int64_t n_round = (n_threads + 31) & ~int64_t(31);
