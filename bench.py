@@ -463,6 +463,83 @@ def secondary_attn(peaks, stream, steps=50):
     return res
 
 
+def secondary_decode_step(peaks, stream, topk=16, steps=20):
+    """One decode step of the whole sparse-attention path on the decode
+    workload (64 requests x 131,072 tokens): the new token's index key and
+    its K and V quantised into their caches (three writer calls), the block
+    scores, the top-k pages (the last page forced), and attention of 16 query
+    heads over the selected pages of an MXFP4 K/V cache (one KV head).  The
+    row context for the attention is derived from the selection count on the
+    device.  Timed as one replay of a graph of ``steps`` steps."""
+    import torch
+    import sparse_attention_mxfp4_gb300 as mx4
+    from sparse_attention_mxfp4_gb300 import harness
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    w = W.make_config("decode")
+    case = harness.to_device(w)
+    B, npool = w.total_rows, w.num_pool_pages
+    g = torch.Generator().manual_seed(77)
+    with torch.cuda.stream(stream):
+        keys = torch.randn((3, B, W.DIM), generator=g).to(torch.bfloat16).cuda()
+        lens = w.seq_lens.to(torch.int64)
+        last = torch.tensor([int(w.block_table[b, (int(lens[b]) - 1) // W.PAGE]) for b in range(B)],
+                            dtype=torch.int64)
+        slots = (last * W.PAGE + (lens - 1) % W.PAGE).cuda()
+        # main K and V caches: [pages, 1 KV head, 8704], codes then scales
+        kv = torch.empty((2, npool, 1, W.PAGE_BYTES), dtype=torch.uint8, device="cuda")
+        kv[..., :W.DATA_BYTES].random_(0, 256)
+        kv[..., W.DATA_BYTES:].random_(122, 128)
+        q_att = torch.randn((B, 1, 16, W.DIM), generator=g).to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+        scores = torch.empty(case.out_shape_scores, dtype=torch.float32, device="cuda")
+        sel = torch.empty((B, 1, topk), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((B, 1), dtype=torch.int32, device="cuda")
+        out = torch.empty((B, 1, 16, W.DIM), dtype=torch.bfloat16, device="cuda")
+        sl = case.seq_lens.to(torch.int64)
+        tail = sl - W.PAGE * ((sl + W.PAGE - 1) // W.PAGE - 1)
+        kflat = kv[0].view(-1)
+        vflat = kv[1].view(-1)
+
+        def step():
+            mx4.mx4_index_k_write(keys[0], slots, case.k_data, case.k_scale, w.k_data_page_stride,
+                                  w.k_scale_page_stride, num_pool_pages=npool, stream=stream)
+            mx4.mx4_index_k_write(keys[1], slots, kflat, kflat[W.DATA_BYTES:], W.PAGE_BYTES, W.PAGE_BYTES,
+                                  num_pool_pages=npool, stream=stream)
+            mx4.mx4_index_k_write(keys[2], slots, vflat, vflat[W.DATA_BYTES:], W.PAGE_BYTES, W.PAGE_BYTES,
+                                  num_pool_pages=npool, stream=stream)
+            case.run(out=scores, stream=stream)
+            mx4.mx4_index_topk_decode(scores, case.block_table, case.seq_lens, w.max_seq_len, topk, sel=sel,
+                                      count=cnt, stream=stream)
+            n = cnt[:, 0].to(torch.int64)
+            ctx = torch.where(n > 0, (n - 1) * W.PAGE + tail, torch.zeros_like(n)).to(torch.int32).view(B, 1)
+            mx4.mx4_sparse_pa_decode(q_att, kv[0], kv[1], sel, ctx, w.sm_scale, out, stream=stream)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for _ in range(steps):
+                step()
+        gr.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gr.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / steps * 1e3
+    res = {"us_per_step": round(us, 3), "steps": steps, "rows": B, "context_tokens": int(w.max_seq_len),
+           "topk": topk, "kernels_per_step": 6,
+           "description": "3 writer calls (index K, K, V) + block scorer + top-k + sparse attention "
+                          "(16 query heads, 1 KV head) over the selected pages; plus 2 small torch "
+                          "kernels deriving the attention context from the selection count",
+           "device_status": mx4.mx4_index_get_device_status()}
+    del case, kv, scores, sel, cnt, out, gr
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -567,6 +644,7 @@ def run_ours(args):
             line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
             line["secondary"]["topk"] = secondary_topk(peaks, stream)
             line["secondary"]["sparse_pa_decode"] = secondary_attn(peaks, stream)
+            line["secondary"]["decode_step"] = secondary_decode_step(peaks, stream)
     if ws > 1:
         dist.barrier()
         dist.destroy_process_group()
