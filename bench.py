@@ -421,7 +421,7 @@ def secondary_topk(peaks, stream, topk=16, steps=50):
     return res
 
 
-def secondary_attn(peaks, stream, steps=50):
+def secondary_attn(peaks, stream, steps=50, name="pa-decode"):
     """Sparse paged-attention decode on the pa-decode workload (64 rows x 16
     query heads over 16 selected MXFP4 pages of K and V), timed as one replay
     of a graph of `steps` calls.  Algorithmic bytes: the listed K and V pages
@@ -429,7 +429,7 @@ def secondary_attn(peaks, stream, steps=50):
     import torch
     import sparse_attention_mxfp4_gb300 as mx4
     from sparse_attention_mxfp4_gb300 import workloads as W
-    c = W.make_attn_config("pa-decode")
+    c = W.make_attn_config(name)
     q, kp, vp = c.q.cuda(), c.k_pool.cuda(), c.v_pool.cuda()
     bt, cl = c.block_table.cuda(), c.context_lens.cuda()
     out = torch.empty((c.rows, c.kv_heads, c.groups, W.DIM), dtype=torch.bfloat16, device="cuda")
@@ -645,6 +645,7 @@ def run_ours(args):
             line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
             line["secondary"]["topk"] = secondary_topk(peaks, stream)
             line["secondary"]["sparse_pa_decode"] = secondary_attn(peaks, stream)
+            line["secondary"]["sparse_pa_decode_4kvh"] = secondary_attn(peaks, stream, name="pa-decode-4kvh")
             line["secondary"]["decode_step"] = secondary_decode_step(peaks, stream)
     if ws > 1:
         dist.barrier()

@@ -634,10 +634,16 @@ ATTN_CONFIG_NAMES = ("pa-decode",)
 
 def make_attn_config(name: str, seed: Optional[int] = None) -> AttnCase:
     """Sparse decode attention of the decode workload's shape: 64 requests,
-    one KV head with 16 query heads, 16 selected pages (2,048 tokens) each."""
+    one KV head (or four) with 16 query heads each, 16 selected pages (2,048
+    tokens) per (request, KV head)."""
     if name == "pa-decode":
         return make_attn_case(name, seed=20 if seed is None else seed, rows=64, kv_heads=1, groups=16, width=16,
                               pool_pages=8192,
                               description="64 rows x 1 KV head x 16 query heads, 16 selected pages of an "
                                           "8192-page pool (K+V pools 143 MB), context 1921..2048 tokens")
+    if name == "pa-decode-4kvh":
+        return make_attn_case(name, seed=21 if seed is None else seed, rows=64, kv_heads=4, groups=16, width=16,
+                              pool_pages=4096,
+                              description="64 rows x 4 KV heads x 16 query heads, 16 selected pages per (row, KV "
+                                          "head) of a 4096-page pool (K+V pools 285 MB), context 1921..2048 tokens")
     raise KeyError(name)

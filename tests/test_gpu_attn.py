@@ -99,6 +99,7 @@ def test_attn_empty_rows_are_zero():
     _check(c)
 
 
-def test_attn_full_size_config():
-    c = W.make_attn_config("pa-decode")
+@pytest.mark.parametrize("name", ["pa-decode", "pa-decode-4kvh"])
+def test_attn_full_size_config(name):
+    c = W.make_attn_config(name)
     print("rel_l2", _check(c))
