@@ -258,7 +258,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     auto pvready = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + i); };
     auto pvfree = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + kAttnPvBufs + i); };
     const uint32_t pv_done = bar(kB0 + 1 + kAttnCtaPages + 2 * kAttnPvBufs);
-    const uint32_t comb_ready = pv_done + 8;               // rank 1's partial results have landed (rank 0)
+    const uint32_t comb_ready = pv_done + 8;               // the peer has staged its partial results
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
     int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
 
