@@ -277,15 +277,25 @@ def cpu_baseline_decode(w):
                   cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
                   prefix_lens=None if w.decode else w.prefix_lens.numpy(), max_seq_len=w.max_seq_len,
                   sm_scale=w.sm_scale, rows=rows, num_pool_pages=n, num_threads=cores)
-    t0 = time.perf_counter()
-    if w.cache == "fp8":
-        oracle.score_fp8(k_fp8=kd, k_page_stride=sd, **common)
-    else:
-        oracle.score(k_data=kd, k_scale=ks, k_data_page_stride=sd, k_scale_page_stride=ss, **common)
-    dt = time.perf_counter() - t0
+    def run(**kw):
+        t0 = time.perf_counter()
+        if w.cache == "fp8":
+            oracle.score_fp8(k_fp8=kd, k_page_stride=sd, **kw)
+        else:
+            oracle.score(k_data=kd, k_scale=ks, k_data_page_stride=sd, k_scale_page_stride=ss, **kw)
+        return time.perf_counter() - t0
+
+    dt = run(**common)
+    # one core on the first 4 rows (the decode rows all have the same length),
+    # scaled to the full call by rows
+    one = dict(common, rows=rows[:4], num_threads=1)
+    dt1 = run(**one) * len(rows) / len(one["rows"])
     return {"value": dt * 1e6, "unit": "us/call", "cores": cores, "kind": "oracle",
             "sample": f"full call: all {len(rows)} query rows of the {w.name} workload, fp64, "
-                      f"OpenMP over rows, 1 repetition (not extrapolated)"}
+                      f"OpenMP over rows, 1 repetition (not extrapolated)",
+            "single_core": {"value": round(dt1 * 1e6, 1), "unit": "us/call", "cores": 1,
+                            "sample": f"rows 0..3 of the {w.name} workload on one thread, scaled by rows "
+                                      f"({len(rows)} / 4)"}}
 
 
 def secondary_configs(names, peaks, stream):
