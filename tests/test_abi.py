@@ -183,3 +183,49 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mx4.load_library(missing)
     finally:
         mx4._lib = saved
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(rows=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(kvh=0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(groups=0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(width=-1), mx4.MX4_ERR_INVALID_ARG),
+    (dict(scale=0.0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(scale=-0.5), mx4.MX4_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), mx4.MX4_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), mx4.MX4_ERR_INVALID_ARG),
+    (dict(rows=0, q=None), mx4.MX4_OK),                            # nothing to do
+    (dict(groups=17), mx4.MX4_ERR_UNSUPPORTED),                     # more than 16 query heads a KV head
+    (dict(width=25), mx4.MX4_ERR_UNSUPPORTED),                      # more than 24 listed pages
+    (dict(q=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(vs=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(bt=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(ctx=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(out=None), mx4.MX4_ERR_INVALID_ARG),
+    (dict(pages=0), mx4.MX4_ERR_INVALID_ARG),
+    (dict(kd_hs=8192 - 32), mx4.MX4_ERR_INVALID_ARG),              # narrow code view
+    (dict(vs_hs=512 - 16), mx4.MX4_ERR_INVALID_ARG),               # narrow scale view
+    (dict(kvh=2), mx4.MX4_ERR_INVALID_ARG),                         # page stride below 2 heads
+    (dict(kd_ps=-8704), mx4.MX4_ERR_INVALID_ARG),
+    (dict(kd=A + 16), mx4.MX4_ERR_MISALIGNED),                     # 4-bit TMA view: 32-byte rule
+    (dict(kd_ps=8704 + 16), mx4.MX4_ERR_MISALIGNED),
+    (dict(ks=A + 8192 + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(vd=A + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(vs_ps=8704 + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(q=A + 8), mx4.MX4_ERR_MISALIGNED),
+    (dict(out=A + 1), mx4.MX4_ERR_MISALIGNED),
+    (dict(bt=A + 2), mx4.MX4_ERR_MISALIGNED),
+    (dict(ctx=A + 2), mx4.MX4_ERR_MISALIGNED),
+])
+def test_sparse_attention_rejections(lib, kw, status):
+    """Single-head pools ([pages, 1, 8704]: codes at byte 0, scales at 8192)
+    with one argument broken at a time; every case returns before any CUDA
+    call."""
+    a = dict(q=A, rows=4, kvh=1, groups=16, kd=A, ks=A + 8192, kd_ps=8704, kd_hs=8704, ks_ps=8704, ks_hs=8704,
+             vd=A, vs=A + 8192, vd_ps=8704, vd_hs=8704, vs_ps=8704, vs_hs=8704, bt=A, width=16, ctx=A,
+             scale=0.088388, out=A, pages=64)
+    a.update(kw)
+    assert lib.mx4_sparse_pa_decode(a["q"], a["rows"], a["kvh"], a["groups"], a["kd"], a["ks"], a["kd_ps"],
+                                    a["kd_hs"], a["ks_ps"], a["ks_hs"], a["vd"], a["vs"], a["vd_ps"], a["vd_hs"],
+                                    a["vs_ps"], a["vs_hs"], a["bt"], a["width"], a["ctx"], a["scale"], a["out"],
+                                    a["pages"], None) == status
