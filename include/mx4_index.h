@@ -85,7 +85,8 @@ typedef enum {
  * 2 = MMA waiting for a page's bytes, 3 = MMA waiting for a free
  * accumulator, 4 = epilogue waiting for a free query buffer, 5 = epilogue
  * waiting for an accumulator; attention: 6 = copy issue, 7 = MMA issue,
- * 8 = softmax or widening warps.  Diagnostic only. */
+ * 8 = softmax or widening warps; 9 = a CTA leaving while a copy it armed
+ * had not landed.  Diagnostic only. */
 
 /*
  * Block scores for ragged prefill (causal) rows.  [P1] "Kernels":

@@ -25,7 +25,7 @@
  *   elements and physical page offsets are 64-bit; the per-token ("MQA
  *   logits") output keeps -inf for masked tokens (section "Correctness").
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - nibble order: element 2i is the low nibble of byte i, 2i+1 the high one;
  *   - scale byte g of a token covers elements 32g .. 32g+31;
  *   - token i of a page sits at byte i*64 of the data view, i*4 of the scale view;

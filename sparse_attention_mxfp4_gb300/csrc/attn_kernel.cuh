@@ -364,9 +364,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             for (int i = 0; i < n; ++i) {
                 const int j = issued - 1 - i;
                 const uint32_t full_b = is_k ? kfull(j % nst) : vfull(j % nst);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(full_b, (j / nst) & 1) && globaltimer_ns() - t0 < 2000000ull) {
-                }
+                if (!drain_bounded(full_b, (j / nst) & 1)) break;
             }
         }
         __syncwarp();

@@ -533,7 +533,9 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     if (!q || !k_data || !k_scale || !v_data || !v_scale || !block_table || !context_lens || !out)
         return MX4_ERR_INVALID_ARG;
     if (num_pool_pages < 1) return MX4_ERR_INVALID_ARG;
-    if (num_pool_pages > INT32_MAX || num_rows * kv_heads > INT32_MAX) return MX4_ERR_UNSUPPORTED;
+    // the grid is rows x KV heads x kAttnSplit CTAs, within grid.x's limit of 2^31 - 1
+    if (num_pool_pages > INT32_MAX || num_rows > INT32_MAX / (static_cast<int64_t>(kv_heads) * mx4::kAttnSplit))
+        return MX4_ERR_UNSUPPORTED;
     // views: a page of one head holds 8192 code bytes and 512 scale bytes
     const int64_t strides[8] = {k_data_page_stride, k_data_head_stride, k_scale_page_stride, k_scale_head_stride,
                                 v_data_page_stride, v_data_head_stride, v_scale_page_stride, v_scale_head_stride};

@@ -217,6 +217,8 @@ enum WaitSite : uint32_t {
     kSiteMmaDEmpty = 3,
     kSiteEpiQEmpty = 4,
     kSiteEpiDFull = 5,
+    // 6..8: the attention kernel's wait sites
+    kSiteDrain = 9,    // an armed copy had not landed when the CTA was leaving
 };
 
 // Bounded wait: true when the phase completed; false after the time limit or
@@ -236,6 +238,22 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
             return false;
         }
     }
+}
+
+// Wait for a copy this CTA armed to land before the CTA exits (its shared
+// memory must not be written after that).  Bounded like every other wait;
+// when it gives up, the status word records it (timeout + site 9), because a
+// copy may then still be in flight.
+__device__ __forceinline__ bool drain_bounded(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_mx4_device_status, 0x2u | (0x100u << kSiteDrain));
+            return false;
+        }
+    }
+    return true;
 }
 
 template <bool kDecode>
@@ -624,9 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kStagesPerLane; ++i) {
                 // stages before pst.idx were armed in phase ph, the others in ph^1 (if ever)
                 const uint32_t par = (i < pst.idx) ? pst.ph : (pst.ph ^ 1u);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(full_bar(ln * kStagesPerLane + i), par) && globaltimer_ns() - t0 < 2000000ull) {
-                }
+                if (!drain_bounded(full_bar(ln * kStagesPerLane + i), par)) break;
             }
         }
         __syncwarp();

@@ -516,6 +516,18 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of a cluster barrier, split so that work can run between
+// them: a relaxed arrive (orders nothing, only counts this thread) ...
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// ... and the wait for every thread of the cluster to have arrived.  After
+// it, every CTA of the cluster is known to be running, so its shared memory
+// may be accessed.
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // ------------------------------------------------------ shared descriptors --
 // tcgen05 shared-memory matrix descriptor: start address, leading / stride
 // byte offsets (16-byte units), version 1 (bits 46..48 = 0b001), swizzle mode

@@ -149,6 +149,10 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
             const int h0 = sl * hper < hg ? sl * hper : hg;
             const int h1 = h0 + hper < hg ? h0 + hper : hg;
             const uint32_t keys0 = cluster_map(static_cast<uint32_t>(__cvta_generic_to_shared(keys)), 0);
+            // Rank 0's shared memory may be written only once every CTA of the
+            // cluster is known to have started: arrive here, wait just before
+            // the remote stores, so the barrier overlaps the score reads.
+            cluster_arrive_relaxed();
             if (p.vec) {
                 const int64_t hstride = p.num_pages >> 2;            // float4 per head
                 const int nq = (nc + 3) >> 2;
@@ -174,6 +178,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                     atomicMax(&keys[4 * qd + 3], topk_key(m.w));
                 }
                 __syncthreads();
+                cluster_wait();
                 if (rank != 0)
                     for (int qd = q0 + tid; qd < q1; qd += kTopkThreads)
                         st_cluster_v4_u32(keys0 + 16u * qd, keys[4 * qd], keys[4 * qd + 1], keys[4 * qd + 2],
@@ -191,6 +196,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                     atomicMax(&keys[j], topk_key(m));
                 }
                 __syncthreads();
+                cluster_wait();
                 if (rank != 0)
                     for (int j = j0 + tid; j < j1; j += kTopkThreads) st_cluster_u32(keys0 + 4u * j, keys[j]);
             }

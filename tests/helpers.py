@@ -81,6 +81,24 @@ def compare(got, ref, rtol=RTOL, atol=ATOL, what="scores", extra=None):
             "max_rel_err": rel, "fp32_exact_fraction": exact}
 
 
+def plain_tolerance_stats(got, ref, rtol=RTOL, atol=ATOL):
+    """How far finite fp32 results sit from the plain tolerance
+    |got - ref| <= atol + rtol*|ref|: the fraction of finite cells outside it,
+    the worst absolute and relative error, and the worst error in units of the
+    plain limit."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    fin = np.isfinite(ref)
+    err = np.abs(got[fin] - ref[fin])
+    lim = atol + rtol * np.abs(ref[fin])
+    rel = err / np.maximum(np.abs(ref[fin]), 1e-30)
+    return {"finite_cells": int(fin.sum()), "outside_plain": int((err > lim).sum()),
+            "outside_plain_fraction": float((err > lim).mean()) if fin.any() else 0.0,
+            "max_abs_err": float(err.max()) if fin.any() else 0.0,
+            "max_rel_err": float(rel.max()) if fin.any() else 0.0,
+            "worst_over_plain_limit": float((err / lim).max()) if fin.any() else 0.0}
+
+
 def e4m3_values_numpy(codes):
     """e4m3 (fn) values from the bit fields: bias 7, subnormal step 2^-9,
     S.1111.111 NaN."""

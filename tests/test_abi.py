@@ -197,6 +197,8 @@ def test_binding_fails_loudly_without_library(tmp_path):
     (dict(rows=0, q=None), mx4.MX4_OK),                            # nothing to do
     (dict(groups=17), mx4.MX4_ERR_UNSUPPORTED),                     # more than 16 query heads a KV head
     (dict(width=25), mx4.MX4_ERR_UNSUPPORTED),                      # more than 24 listed pages
+    (dict(rows=1 << 30), mx4.MX4_ERR_UNSUPPORTED),                  # rows x KV heads x 2 CTAs past grid.x's limit
+    (dict(rows=1 << 29, kvh=2, kd_ps=17408, ks_ps=17408, vd_ps=17408, vs_ps=17408), mx4.MX4_ERR_UNSUPPORTED),
     (dict(q=None), mx4.MX4_ERR_INVALID_ARG),
     (dict(vs=None), mx4.MX4_ERR_INVALID_ARG),
     (dict(bt=None), mx4.MX4_ERR_INVALID_ARG),

@@ -80,7 +80,7 @@ def test_fp8_cache_matches_mxfp4_cache_within_the_window(decode):
     assert np.array_equal(np.isneginf(a), np.isneginf(b))
 
 
-@pytest.mark.parametrize("name,n_rows", [("decode-fp8", 8), ("prefill-long-fp8", 24)])
+@pytest.mark.parametrize("name,n_rows", [("decode-fp8", 64), ("prefill-long-fp8", 256)])
 def test_fp8_full_size_sampled(name, n_rows):
     w = W.make_config(name)
     c = harness.to_device(w)

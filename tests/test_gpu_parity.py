@@ -13,7 +13,7 @@ import oracle
 import sparse_attention_mxfp4_gb300 as mx4
 from sparse_attention_mxfp4_gb300 import harness
 from sparse_attention_mxfp4_gb300 import workloads as W
-from helpers import ATOL, RTOL, compare, logits_accum_allowance, oracle_run
+from helpers import ATOL, RTOL, compare, logits_accum_allowance, oracle_run, plain_tolerance_stats
 
 pytestmark = pytest.mark.gpu
 
@@ -124,6 +124,30 @@ def test_prefill_e4m3_q_wide_scales_split_views():
                         scale_lo=100, scale_hi=150, layout="split", k_data_page_stride=8192 + 64,
                         k_scale_page_stride=512 + 48)
     _check(w, real_pool=True)
+
+
+@pytest.mark.parametrize("case", ["e4m3-wide", "mtp-like"])
+def test_wide_scale_logits_against_the_plain_tolerance(case):
+    """Per-token logits with scale bytes 100..150 (2^-27 .. 2^23 within one
+    token): every cell within the summation allowance, and how many cells fall
+    outside the plain 1e-5 / 1e-6 tolerance, with the worst errors, printed
+    (run with -s to see them).  Block scores meet the plain tolerance."""
+    if case == "e4m3-wide":
+        w = W.make_workload("e4m3", seed=22, q_lens=[9, 16], seq_lens=[700, 2000], pool_pages=40, q_e4m3=True,
+                            scale_lo=100, scale_hi=150)
+    else:
+        # the wide-scale MTP shape at 2 of its 32 requests: 8 rows, 32,768 tokens
+        w = W.make_workload("mtp-like", seed=3, q_lens=[8, 8], seq_lens=[32768, 32768],
+                            prefix_lens=[32760, 32760], pool_pages=600, q_e4m3=True, scale_lo=100, scale_hi=150)
+    got_l = _gpu(w, logits=True)
+    _, ref_l = oracle_run(w, logits=True, scores=False)
+    compare(got_l, ref_l, what=f"{w.name} logits", extra=logits_accum_allowance(w))
+    st = plain_tolerance_stats(got_l, ref_l)
+    print(f"\nwide-scale logits {case}: {st}")
+    got = _gpu(w)
+    ref, _ = oracle_run(w)
+    compare(got, ref, what=f"{w.name} scores")
+    assert plain_tolerance_stats(got, ref)["outside_plain"] == 0
 
 
 def test_decode_ragged_split_views():
