@@ -263,20 +263,34 @@ def measure_e2e(case, steps, stream):
     return start.elapsed_time(end) / steps, h2d, d2h
 
 
-def cpu_baseline_decode(w):
-    """The oracle, as it stands, on all 64 requests of the decode workload
-    (one full call), on every host core."""
+# Configurations whose CPU baseline runs the oracle on a seeded sample of
+# query rows (the full call would take minutes), extrapolated by live pairs.
+CPU_SAMPLED_ROWS = {"prefill-long": 256, "chunked": 256, "prefill-long-fp8": 256}
+
+
+def cpu_baseline_config(w):
+    """The oracle, as it stands, on every host core: the full call for
+    prefill-tiny, decode, MTP and decode-fp8; 256 seeded sampled rows for
+    prefill-long, chunked and prefill-long-fp8, extrapolated to the full call
+    by live (row, token) pairs.  A single-core figure beside it for
+    prefill-tiny (the full call) and decode (4 rows, scaled by rows)."""
     import numpy as np
     import oracle
     from sparse_attention_mxfp4_gb300 import workloads as W
     kd, ks, sd, ss, bt, n = W.compact_host(w)
     cores = os.cpu_count() or 1
-    rows = np.arange(w.total_rows)
+    n_sample = CPU_SAMPLED_ROWS.get(w.name)
+    rows = W.sample_rows(w, n_sample, 0) if n_sample else np.arange(w.total_rows)
+    lp = dict(decode=w.decode, seq_lens=w.seq_lens.numpy(), max_seq_len=w.max_seq_len,
+              cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
+              prefix_lens=None if w.decode else w.prefix_lens.numpy())
+    all_pairs = oracle.live_pairs(rows=np.arange(w.total_rows), **lp)
     common = dict(decode=w.decode, q=W.q_numpy(w), q_is_e4m3=w.q_is_e4m3, block_table=bt,
                   block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
                   cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
                   prefix_lens=None if w.decode else w.prefix_lens.numpy(), max_seq_len=w.max_seq_len,
                   sm_scale=w.sm_scale, rows=rows, num_pool_pages=n, num_threads=cores)
+
     def run(**kw):
         t0 = time.perf_counter()
         if w.cache == "fp8":
@@ -286,19 +300,63 @@ def cpu_baseline_decode(w):
         return time.perf_counter() - t0
 
     dt = run(**common)
-    # one core on the first 4 rows (the decode rows all have the same length),
-    # scaled to the full call by rows
-    one = dict(common, rows=rows[:4], num_threads=1)
-    dt1 = run(**one) * len(rows) / len(one["rows"])
-    return {"value": dt * 1e6, "unit": "us/call", "cores": cores, "kind": "oracle",
-            "sample": f"full call: all {len(rows)} query rows of the {w.name} workload, fp64, "
-                      f"OpenMP over rows, 1 repetition (not extrapolated)",
-            "single_core": {"value": round(dt1 * 1e6, 1), "unit": "us/call", "cores": 1,
-                            "sample": f"rows 0..3 of the {w.name} workload on one thread, scaled by rows "
-                                      f"({len(rows)} / 4)"}}
+    if n_sample:
+        pairs = oracle.live_pairs(rows=rows, **lp)
+        dt *= all_pairs / max(1, pairs)
+        sample = (f"{len(rows)} seeded sampled query rows of the {w.name} workload ({pairs} of {all_pairs} live "
+                  f"row-token pairs), fp64, OpenMP over rows; time extrapolated by live pairs")
+    else:
+        sample = (f"full call: all {len(rows)} query rows of the {w.name} workload, fp64, OpenMP over rows, "
+                  f"1 repetition (not extrapolated)")
+    res = {"value": round(dt * 1e6, 1), "unit": "us/call", "cores": cores, "kind": "oracle", "sample": sample,
+           "extrapolated": bool(n_sample)}
+    if w.name in ("prefill-tiny", "decode"):
+        # one core: the whole tiny call; the first 4 decode rows (the rows all
+        # have the same length) scaled to the full call by rows
+        one_rows = rows if w.name == "prefill-tiny" else rows[:4]
+        dt1 = run(**dict(common, rows=one_rows, num_threads=1)) * len(rows) / len(one_rows)
+        res["single_core"] = {"value": round(dt1 * 1e6, 1), "unit": "us/call", "cores": 1,
+                              "sample": "the full call on one thread" if w.name == "prefill-tiny" else
+                              f"rows 0..3 of the {w.name} workload on one thread, scaled by rows "
+                              f"({len(rows)} / 4)"}
+    return res
 
 
-def secondary_configs(names, peaks, stream):
+L2_BYTES = 129 * 1024 * 1024   # GB300 L2 (nominal)
+
+
+def time_calls_rotating(cases, outs, steps, warmup, stream, call=None):
+    """Device time per call with a cold L2: one replay of a graph of ``steps``
+    calls that cycle over ``len(cases)`` disjoint copies of the inputs and
+    outputs (together larger than L2, so no call finds its pages in L2)."""
+    import torch
+    call = call or (lambda c, o: c.run(out=o, stream=stream))
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            call(cases[i % len(cases)], outs[i % len(outs)])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                call(cases[i % len(cases)], outs[i % len(outs)])
+        g.replay()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+    del g
+    return start.elapsed_time(end) / steps
+
+
+# Configurations whose index cache fits in L2: timed warm (the same inputs
+# every call) and cold (rotating over disjoint copies larger than L2).
+COLD_L2_CONFIGS = ("prefill-tiny", "prefill-long", "chunked")
+
+
+def secondary_configs(names, peaks, stream, cpu=True):
     import torch
     from sparse_attention_mxfp4_gb300 import harness
     from sparse_attention_mxfp4_gb300 import workloads as W
@@ -313,15 +371,110 @@ def secondary_configs(names, peaks, stream):
         steps = 200 if name == "prefill-tiny" else (5 if name == "chunked" else 20)
         ms = time_calls(case, out, steps, 3, stream)
         tf = work["flops"] / (ms * 1e-3) / 1e12
-        res[name] = {"us_per_call": round(ms * 1e3, 3), "steps": steps, "cache": w.cache,
-                     "mma_tflops": round(tf, 1),
-                     "frac_of_fp8_dense_peak": round(tf / fp8_peak, 4),
-                     "frac_of_fp4_dense_peak": round(tf / fp4_peak, 4),
-                     "hbm_gbs_algorithmic": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
-                     "frac_of_hbm_peak": round(work["bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                     "flops_per_call": work["flops"], "bytes_per_call": work["bytes"]}
+        r = {"us_per_call": round(ms * 1e3, 3), "steps": steps, "cache": w.cache,
+             "l2": "inputs larger than L2" if work["k_bytes"] > L2_BYTES else "warm: the same inputs every call",
+             "mma_tflops": round(tf, 1),
+             "frac_of_fp8_dense_peak": round(tf / fp8_peak, 4),
+             "frac_of_fp4_dense_peak": round(tf / fp4_peak, 4),
+             "hbm_gbs_algorithmic": round(work["bytes"] / (ms * 1e-3) / 1e9, 1),
+             "frac_of_hbm_peak": round(work["bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+             "flops_per_call": work["flops"], "bytes_per_call": work["bytes"]}
+        if name == "prefill-tiny":
+            # eager calls back to back (no graph): the host's launch path,
+            # tensor-map lookups included, sets the pace of a small call
+            n_eager = 200
+            with torch.cuda.stream(stream):
+                for _ in range(10):
+                    case.run(out=out, stream=stream)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                t0 = time.perf_counter()
+                e0.record(stream)
+                for _ in range(n_eager):
+                    case.run(out=out, stream=stream)
+                e1.record(stream)
+                host_s = time.perf_counter() - t0
+                torch.cuda.synchronize()
+            r["eager"] = {"us_per_call": round(e0.elapsed_time(e1) / n_eager * 1e3, 3), "calls": n_eager,
+                          "host_us_per_call": round(host_s / n_eager * 1e6, 3),
+                          "timing": "CUDA events around eager calls enqueued back to back through the Python "
+                                    "binding (host launch path included)"}
+        if name in COLD_L2_CONFIGS:
+            # disjoint copies of the pool, query and output, rotated so that
+            # together they exceed twice the L2 (at least 2 copies)
+            region = sum(b.numel() for b in case.buffers) + case.q.numel() * case.q.element_size() \
+                + out.numel() * 4
+            n_reg = max(2, -(-2 * L2_BYTES // region))
+            cases = [case] + [harness.to_device(w) for _ in range(n_reg - 1)]
+            outs = [out] + [torch.empty_like(out) for _ in range(n_reg - 1)]
+            csteps = max(n_reg, steps if name != "prefill-tiny" else 2 * n_reg)
+            cms = time_calls_rotating(cases, outs, csteps, n_reg, stream)
+            ctf = work["flops"] / (cms * 1e-3) / 1e12
+            r["cold"] = {"us_per_call": round(cms * 1e3, 3), "steps": csteps, "regions": n_reg,
+                         "region_bytes": region,
+                         "l2": f"cold: {n_reg} disjoint copies of pool, query and output rotated",
+                         "mma_tflops": round(ctf, 1), "frac_of_fp8_dense_peak": round(ctf / fp8_peak, 4),
+                         "frac_of_fp4_dense_peak": round(ctf / fp4_peak, 4)}
+            del cases, outs
+        if cpu:
+            r["cpu_baseline"] = cpu_baseline_config(w)
+        res[name] = r
         del case, out
         torch.cuda.empty_cache()
+    return res
+
+
+DECODE_SWEEP_BATCHES = (1, 4, 16, 64)
+DECODE_SWEEP_CONTEXTS = (8192, 131072)
+
+
+def secondary_decode_sweep(peaks, stream, steps=20):
+    """Decode block scores over B requests x ctx tokens for B in 1, 4, 16, 64
+    and ctx in 8K, 128K (the pages' decode auto-CTA table spans the same
+    range): the pages of the decode workload's 70,000-page pool (split views),
+    block tables drawn by a seeded permutation of its pages, bf16 N(0,1)
+    queries.  When one call's pages fit in L2, the calls rotate over disjoint
+    groups of B requests (distinct pages) covering more than twice the L2."""
+    import torch
+    import sparse_attention_mxfp4_gb300 as mx4
+    from sparse_attention_mxfp4_gb300 import harness
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    w = W.make_config("decode")
+    case = harness.to_device(w)
+    ids = w.page_ids.to(torch.int32)
+    g = torch.Generator().manual_seed(4242)
+    res = {}
+    for ctx in DECODE_SWEEP_CONTEXTS:
+        P = ctx // W.PAGE
+        for B in DECODE_SWEEP_BATCHES:
+            per_call = B * P * W.PAGE_BYTES
+            n_reg = max(1, min(ids.numel() // (B * P), -(-2 * L2_BYTES // per_call)))
+            rows = n_reg * B
+            perm = ids[torch.randperm(ids.numel(), generator=g)[: rows * P]]
+            bt = perm.view(rows, P).contiguous().cuda()
+            q = torch.randn((rows, W.HEADS, W.DIM), generator=g).to(torch.bfloat16).cuda()
+            sl = torch.full((rows,), ctx, dtype=torch.int32, device="cuda")
+            out = torch.empty((rows, W.HEADS, P), dtype=torch.float32, device="cuda")
+            regions = [slice(r * B, (r + 1) * B) for r in range(n_reg)]
+
+            def call(rg, _o):
+                mx4.mx4_index_score_decode(q[rg], case.k_data, case.k_scale, w.k_data_page_stride,
+                                           w.k_scale_page_stride, bt[rg], sl[rg], ctx, w.sm_scale, out[rg],
+                                           num_pool_pages=w.num_pool_pages, stream=stream)
+            n_steps = max(steps, n_reg)
+            ms = time_calls_rotating(regions, regions, n_steps, min(n_reg, 8), stream, call=call)
+            nbytes = per_call + B * W.HEADS * W.DIM * 2 + B * W.HEADS * P * 4 + B * P * 4
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            res[f"B{B}_ctx{ctx // 1024}K"] = {
+                "us_per_call": round(ms * 1e3, 3), "requests": B, "context": ctx, "steps": n_steps,
+                "regions": n_reg, "bytes_per_call": nbytes, "hbm_gbs_algorithmic": round(gbs, 1),
+                "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4),
+                "l2": "inputs larger than L2" if n_reg == 1 else f"cold: {n_reg} disjoint request groups rotated"}
+            del bt, q, sl, out
+    res["device_status"] = mx4.mx4_index_get_device_status()
+    del case
+    torch.cuda.empty_cache()
     return res
 
 
@@ -505,8 +658,7 @@ def secondary_decode_step(peaks, stream, topk=16, steps=20):
         sel = torch.empty((B, 1, topk), dtype=torch.int32, device="cuda")
         cnt = torch.empty((B, 1), dtype=torch.int32, device="cuda")
         out = torch.empty((B, 1, 16, W.DIM), dtype=torch.bfloat16, device="cuda")
-        sl = case.seq_lens.to(torch.int64)
-        tail = sl - W.PAGE * ((sl + W.PAGE - 1) // W.PAGE - 1)
+        ctx = torch.empty((B, 1), dtype=torch.int32, device="cuda")
         kflat = kv[0].view(-1)
         vflat = kv[1].view(-1)
 
@@ -518,10 +670,10 @@ def secondary_decode_step(peaks, stream, topk=16, steps=20):
             mx4.mx4_index_k_write(keys[2], slots, vflat, vflat[W.DATA_BYTES:], W.PAGE_BYTES, W.PAGE_BYTES,
                                   num_pool_pages=npool, stream=stream)
             case.run(out=scores, stream=stream)
+            # the selection also emits each row's context: the live tokens of
+            # its selected pages
             mx4.mx4_index_topk_decode(scores, case.block_table, case.seq_lens, w.max_seq_len, topk, sel=sel,
-                                      count=cnt, stream=stream)
-            n = cnt[:, 0].to(torch.int64)
-            ctx = torch.where(n > 0, (n - 1) * W.PAGE + tail, torch.zeros_like(n)).to(torch.int32).view(B, 1)
+                                      count=cnt, tokens=ctx, stream=stream)
             mx4.mx4_sparse_pa_decode(q_att, kv[0], kv[1], sel, ctx, w.sm_scale, out, stream=stream)
 
         for _ in range(3):
@@ -542,9 +694,9 @@ def secondary_decode_step(peaks, stream, topk=16, steps=20):
     us = e0.elapsed_time(e1) / steps * 1e3
     res = {"us_per_step": round(us, 3), "steps": steps, "rows": B, "context_tokens": int(w.max_seq_len),
            "topk": topk, "kernels_per_step": 6,
-           "description": "3 writer calls (index K, K, V) + block scorer + top-k + sparse attention "
-                          "(16 query heads, 1 KV head) over the selected pages; plus 2 small torch "
-                          "kernels deriving the attention context from the selection count",
+           "description": "3 writer calls (index K, K, V) + block scorer + top-k (which also emits each row's "
+                          "attention context) + sparse attention (16 query heads, 1 KV head) over the selected "
+                          "pages; no other kernel",
            "device_status": mx4.mx4_index_get_device_status()}
     del case, kv, scores, sel, cnt, out, gr
     torch.cuda.empty_cache()
@@ -646,12 +798,13 @@ def run_ours(args):
             "device_status": status,
         }
         if ws == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline_decode(w) if w.decode else None
+            line["cpu_baseline"] = cpu_baseline_config(w)
         if ws == 1 and not args.no_secondary:
             del case, out
             torch.cuda.empty_cache()
             names = [n for n in W.CONFIG_NAMES + W.FP8_CONFIG_NAMES if n != w.name]
-            line["secondary"] = secondary_configs(names, peaks, stream)
+            line["secondary"] = secondary_configs(names, peaks, stream, cpu=not args.no_cpu_baseline)
+            line["secondary"]["decode_sweep"] = secondary_decode_sweep(peaks, stream)
             line["secondary"]["index_k_write"] = secondary_writer(peaks, stream)
             line["secondary"]["topk"] = secondary_topk(peaks, stream)
             line["secondary"]["sparse_pa_decode"] = secondary_attn(peaks, stream)

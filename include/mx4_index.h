@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define MX4_ABI_VERSION 1
+#define MX4_ABI_VERSION 2
 
 typedef enum {
     MX4_OK = 0,
@@ -219,6 +219,11 @@ mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8
  *   sel         int32 [total_rows, kv_groups, topk]: physical page ids of the
  *               selected pages in ascending page order, then -1.
  *   count       int32 [total_rows, kv_groups]: pages selected.
+ *   sel_tokens  int32 [total_rows, kv_groups] or NULL: the live tokens of the
+ *               selected pages (128 for each but the row's last live page,
+ *               which holds L - 128 (ceil(L/128) - 1)); this is the context
+ *               the attention step reads from the emitted list in order
+ *               (mx4_sparse_pa_decode's context_lens).
  *   topk >= 1, 0 <= local_pages <= topk, kv_groups divides 64,
  *   ceil(max_seq_len/128) <= 16384 (MX4_ERR_UNSUPPORTED beyond).
  * The request arguments (block_table, cu_seqlens_q, seq_lens, prefix_lens,
@@ -230,11 +235,13 @@ mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8
 mx4_status mx4_index_topk_prefill(const float *scores, const int32_t *block_table, const int32_t *cu_seqlens_q,
                                   const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
                                   int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
-                                  int32_t *count, void *stream, int num_seqs, int64_t block_table_stride);
+                                  int32_t *count, int32_t *sel_tokens, void *stream, int num_seqs,
+                                  int64_t block_table_stride);
 
 mx4_status mx4_index_topk_decode(const float *scores, const int32_t *block_table, const int32_t *seq_lens,
                                  int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
-                                 int32_t *count, void *stream, int num_seqs, int64_t block_table_stride);
+                                 int32_t *count, int32_t *sel_tokens, void *stream, int num_seqs,
+                                 int64_t block_table_stride);
 
 /*
  * Sparse paged-attention decode over MXFP4 K and V: each row (a decode token

@@ -102,7 +102,7 @@ def _load():
         lib.orc_topk.argtypes = [
             ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+            ctypes.c_int, c_i64p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.orc_pa_decode.restype = ctypes.c_int
         lib.orc_pa_decode.argtypes = [
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -316,11 +316,13 @@ def write_index_k(*, k_bits: np.ndarray, slot_mapping, k_data: np.ndarray, k_sca
 # ------------------------------------------------------------------- top-k --
 def topk(*, decode: bool, scores: np.ndarray, block_table: np.ndarray, block_table_stride: int, seq_lens,
          max_seq_len: int, topk: int, local: int = 1, kv_groups: int = 1, cu_seqlens_q=None,
-         prefix_lens=None, rows=None):
+         prefix_lens=None, rows=None, want_tokens: bool = False):
     """Top-k page selection after the scorer (the readings are stated in
     ``mx4_oracle.c``).  ``scores``: float32 [rows_total, 64, P] block scores.
     Returns (sel int32 [n_rows, kv_groups, topk] physical ids, -1 padded, in
-    ascending page order; count int32 [n_rows, kv_groups])."""
+    ascending page order; count int32 [n_rows, kv_groups]), and with
+    ``want_tokens`` also tokens int32 [n_rows, kv_groups], the live tokens of
+    the selected pages."""
     lib = _load()
     sc = np.ascontiguousarray(scores, dtype=np.float32)
     bt = _i32(block_table).reshape(-1)
@@ -335,12 +337,13 @@ def topk(*, decode: bool, scores: np.ndarray, block_table: np.ndarray, block_tab
     n = rows.shape[0]
     sel = np.empty((n, kv_groups, topk), dtype=np.int32)
     cnt = np.empty((n, kv_groups), dtype=np.int32)
+    tok = np.empty((n, kv_groups), dtype=np.int32)
     st = lib.orc_topk(1 if decode else 0, _ptr(sc), int(max_seq_len), _ptr(bt), int(block_table_stride),
                       _ptr(cu), _ptr(sl), _ptr(pl), num_seqs, int(topk), int(local), int(kv_groups),
-                      rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(sel), _ptr(cnt))
+                      rows.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, _ptr(sel), _ptr(cnt), _ptr(tok))
     if st != 0:
         raise ValueError(f"oracle rejected the inputs (status {st})")
-    return sel, cnt
+    return (sel, cnt, tok) if want_tokens else (sel, cnt)
 
 
 # ------------------------------------------------ sparse paged attention --

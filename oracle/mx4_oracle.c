@@ -502,7 +502,10 @@ int64_t orc_write_index_k(const uint16_t *k, int64_t num_tokens, int64_t k_row_s
  *   - the other topk - forced slots go to the live pages with the largest
  *     values, ties to the lower page index;
  *   - the emit lists the selected pages' physical ids (block_table) in
- *     ascending page order, then -1 up to topk; count = number selected.
+ *     ascending page order, then -1 up to topk; count = number selected;
+ *   - tokens (optional) = the live tokens of the selected pages: the valid
+ *     context of the emitted list, read in list order, for the attention
+ *     step (page j holds min(128, L - 128 j) live tokens).
  * Values are the fp32 block scores as given; every comparison is exact.
  */
 static int orc_cmp_desc_value_asc_index(const void *pa, const void *pb)
@@ -515,14 +518,15 @@ static int orc_cmp_desc_value_asc_index(const void *pa, const void *pb)
 
 /*
  * scores [n_rows_total, 64, P] fp32 (P = ceil(max_seq_len/128)); rows as for
- * orc_score.  sel [n_rows, kv_groups, topk] int32, count [n_rows, kv_groups].
+ * orc_score.  sel [n_rows, kv_groups, topk] int32, count [n_rows, kv_groups],
+ * tokens [n_rows, kv_groups] int32 or NULL.
  * Returns 0, or -1 for a row outside every request, -3 for bad arguments.
  */
 int orc_topk(int decode, const float *scores, int max_seq_len,
              const int32_t *block_table, int64_t block_table_stride,
              const int32_t *cu_seqlens_q, const int32_t *seq_lens, const int32_t *prefix_lens,
              int num_seqs, int topk, int local, int kv_groups,
-             const int64_t *rows, int64_t n_rows, int32_t *sel, int32_t *count)
+             const int64_t *rows, int64_t n_rows, int32_t *sel, int32_t *count, int32_t *tokens)
 {
     const int64_t P = ((int64_t)max_seq_len + ORC_PAGE - 1) / ORC_PAGE;
     int status = 0;
@@ -542,10 +546,12 @@ int orc_topk(int decode, const float *scores, int max_seq_len,
         int b = decode ? (int)r : orc_request_of_row(cu_seqlens_q, num_seqs, r);
         for (int g = 0; g < kv_groups; ++g) {
             int32_t *out = sel + (ri * kv_groups + g) * (int64_t)topk;
-            int64_t L, nl, forced, n_c = 0, n_sel = 0;
+            int64_t L, nl, forced, n_c = 0, n_sel = 0, n_tok = 0;
             for (int i = 0; i < topk; ++i)
                 out[i] = -1;
             count[ri * kv_groups + g] = 0;
+            if (tokens)
+                tokens[ri * kv_groups + g] = 0;
             if (b < 0 || b >= num_seqs) {
                 status = -1;
                 continue;
@@ -573,9 +579,13 @@ int orc_topk(int decode, const float *scores, int max_seq_len,
             for (int64_t i = 0; i < n_c && i < topk - forced; ++i)
                 pick[(int64_t)cand[2 * i + 1]] = 1;
             for (int64_t j = 0; j < nl; ++j)
-                if (pick[j])
+                if (pick[j]) {
                     out[n_sel++] = block_table[(int64_t)b * block_table_stride + j];
+                    n_tok += (L - ORC_PAGE * j < ORC_PAGE) ? L - ORC_PAGE * j : ORC_PAGE;
+                }
             count[ri * kv_groups + g] = (int32_t)n_sel;
+            if (tokens)
+                tokens[ri * kv_groups + g] = (int32_t)n_tok;
         }
     }
     free(cand);

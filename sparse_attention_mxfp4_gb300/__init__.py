@@ -75,45 +75,50 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             raise RuntimeError(
                 f"the CUDA library {path} is not built; run "
                 "`python -c 'import __graft_entry__ as g; g.build()'` first")
-        lib = ctypes.CDLL(path)
-        i32, i64, f32, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
-        prefill_args = [vp, i32, vp, vp, i64, i64, vp, vp, vp, vp, i32, i32, f32, vp, vp, i32, i64, i64]
-        decode_args = [vp, i32, vp, vp, i64, i64, vp, vp, i32, f32, vp, vp, i32, i64, i64]
-        for name, args in (("mx4_index_score_prefill", prefill_args),
-                           ("mx4_index_logits_prefill", prefill_args),
-                           ("mx4_index_score_decode", decode_args),
-                           ("mx4_index_logits_decode", decode_args)):
-            f = getattr(lib, name)
-            f.restype = i32
-            f.argtypes = args
-        prefill_fp8_args = [vp, i32, vp, i64, vp, vp, vp, vp, i32, i32, f32, vp, vp, i32, i64, i64]
-        decode_fp8_args = [vp, i32, vp, i64, vp, vp, i32, f32, vp, vp, i32, i64, i64]
-        for name, args in (("mx4_index_score_prefill_fp8", prefill_fp8_args),
-                           ("mx4_index_logits_prefill_fp8", prefill_fp8_args),
-                           ("mx4_index_score_decode_fp8", decode_fp8_args),
-                           ("mx4_index_logits_decode_fp8", decode_fp8_args)):
-            f = getattr(lib, name)
-            f.restype = i32
-            f.argtypes = args
-        lib.mx4_index_topk_prefill.restype = i32
-        lib.mx4_index_topk_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, i32, i64]
-        lib.mx4_index_topk_decode.restype = i32
-        lib.mx4_index_topk_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i32, i64]
-        lib.mx4_sparse_pa_decode.restype = i32
-        lib.mx4_sparse_pa_decode.argtypes = [vp, i64, i32, i32, vp, vp, i64, i64, i64, i64, vp, vp, i64, i64, i64,
-                                             i64, vp, i32, vp, f32, vp, i64, vp]
-        lib.mx4_quantize_q_e4m3.restype = i32
-        lib.mx4_quantize_q_e4m3.argtypes = [vp, vp, i64, vp]
-        lib.mx4_index_k_write.restype = i32
-        lib.mx4_index_k_write.argtypes = [vp, i64, i64, vp, vp, vp, i64, i64, i64, vp]
-        lib.mx4_index_get_device_status.restype = i32
-        lib.mx4_index_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
-        lib.mx4_status_string.restype = ctypes.c_char_p
-        lib.mx4_status_string.argtypes = [i32]
-        lib.mx4_abi_version.restype = i32
-        lib.mx4_abi_version.argtypes = []
-        _lib = lib
-        return lib
+        _lib = configure_library(ctypes.CDLL(path))
+        return _lib
+
+
+def configure_library(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of every exported entry point
+    on a loaded copy of the library."""
+    i32, i64, f32, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+    prefill_args = [vp, i32, vp, vp, i64, i64, vp, vp, vp, vp, i32, i32, f32, vp, vp, i32, i64, i64]
+    decode_args = [vp, i32, vp, vp, i64, i64, vp, vp, i32, f32, vp, vp, i32, i64, i64]
+    for name, args in (("mx4_index_score_prefill", prefill_args),
+                       ("mx4_index_logits_prefill", prefill_args),
+                       ("mx4_index_score_decode", decode_args),
+                       ("mx4_index_logits_decode", decode_args)):
+        f = getattr(lib, name)
+        f.restype = i32
+        f.argtypes = args
+    prefill_fp8_args = [vp, i32, vp, i64, vp, vp, vp, vp, i32, i32, f32, vp, vp, i32, i64, i64]
+    decode_fp8_args = [vp, i32, vp, i64, vp, vp, i32, f32, vp, vp, i32, i64, i64]
+    for name, args in (("mx4_index_score_prefill_fp8", prefill_fp8_args),
+                       ("mx4_index_logits_prefill_fp8", prefill_fp8_args),
+                       ("mx4_index_score_decode_fp8", decode_fp8_args),
+                       ("mx4_index_logits_decode_fp8", decode_fp8_args)):
+        f = getattr(lib, name)
+        f.restype = i32
+        f.argtypes = args
+    lib.mx4_index_topk_prefill.restype = i32
+    lib.mx4_index_topk_prefill.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, i32, i64]
+    lib.mx4_index_topk_decode.restype = i32
+    lib.mx4_index_topk_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, i32, i64]
+    lib.mx4_sparse_pa_decode.restype = i32
+    lib.mx4_sparse_pa_decode.argtypes = [vp, i64, i32, i32, vp, vp, i64, i64, i64, i64, vp, vp, i64, i64, i64,
+                                         i64, vp, i32, vp, f32, vp, i64, vp]
+    lib.mx4_quantize_q_e4m3.restype = i32
+    lib.mx4_quantize_q_e4m3.argtypes = [vp, vp, i64, vp]
+    lib.mx4_index_k_write.restype = i32
+    lib.mx4_index_k_write.argtypes = [vp, i64, i64, vp, vp, vp, i64, i64, i64, vp]
+    lib.mx4_index_get_device_status.restype = i32
+    lib.mx4_index_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.mx4_status_string.restype = ctypes.c_char_p
+    lib.mx4_status_string.argtypes = [i32]
+    lib.mx4_abi_version.restype = i32
+    lib.mx4_abi_version.argtypes = []
+    return lib
 
 
 def _check(fn: str, status: int):
@@ -273,38 +278,54 @@ def _topk_out(sel, count, rows, groups, topk, like):
     return sel, count
 
 
+def _topk_tokens(tokens, want_tokens, rows, kv_groups, like):
+    import torch
+    if tokens is None and want_tokens:
+        tokens = torch.empty((rows, kv_groups), dtype=torch.int32, device=like.device)
+    if tokens is not None and (tokens.dtype != torch.int32 or tuple(tokens.shape) != (rows, kv_groups)
+                               or not tokens.is_contiguous()):
+        raise ValueError(f"tokens must be a contiguous int32 tensor of shape {(rows, kv_groups)}")
+    return tokens
+
+
 def mx4_index_topk_prefill(scores, block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len, max_seq_len,
-                           topk, *, local_pages=1, kv_groups=1, sel=None, count=None, stream=None):
+                           topk, *, local_pages=1, kv_groups=1, sel=None, count=None, tokens=None,
+                           want_tokens=False, stream=None):
     """Top-k page selection over prefill block scores ``scores`` [rows, 64, P]
     (the scorer's output).  Returns (sel int32 [rows, kv_groups, topk],
-    count int32 [rows, kv_groups])."""
+    count int32 [rows, kv_groups]), plus tokens int32 [rows, kv_groups] (the
+    live tokens of the selected pages) when ``tokens`` is given or
+    ``want_tokens`` is set."""
     import torch
     lib = load_library()
     if scores.dtype != torch.float32 or scores.dim() != 3 or not scores.is_contiguous():
         raise ValueError("scores must be a contiguous float32 [rows, 64, P] tensor")
     sel, count = _topk_out(sel, count, scores.shape[0], kv_groups, topk, scores)
+    tok = _topk_tokens(tokens, want_tokens, scores.shape[0], kv_groups, scores)
     fn = "mx4_index_topk_prefill"
     _check(fn, lib.mx4_index_topk_prefill(
         _ptr(scores), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(prefix_lens), int(max_query_len),
-        int(max_seq_len), int(topk), int(local_pages), int(kv_groups), _ptr(sel), _ptr(count), _stream(stream),
-        int(seq_lens.shape[0]), _bt_stride(block_table)))
-    return sel, count
+        int(max_seq_len), int(topk), int(local_pages), int(kv_groups), _ptr(sel), _ptr(count), _ptr(tok),
+        _stream(stream), int(seq_lens.shape[0]), _bt_stride(block_table)))
+    return (sel, count) if tok is None else (sel, count, tok)
 
 
 def mx4_index_topk_decode(scores, block_table, seq_lens, max_seq_len, topk, *, local_pages=1, kv_groups=1,
-                          sel=None, count=None, stream=None):
-    """Top-k page selection over decode block scores (one row per request)."""
+                          sel=None, count=None, tokens=None, want_tokens=False, stream=None):
+    """Top-k page selection over decode block scores (one row per request);
+    returns as ``mx4_index_topk_prefill``."""
     import torch
     lib = load_library()
     if scores.dtype != torch.float32 or scores.dim() != 3 or not scores.is_contiguous():
         raise ValueError("scores must be a contiguous float32 [rows, 64, P] tensor")
     sel, count = _topk_out(sel, count, scores.shape[0], kv_groups, topk, scores)
+    tok = _topk_tokens(tokens, want_tokens, scores.shape[0], kv_groups, scores)
     fn = "mx4_index_topk_decode"
     _check(fn, lib.mx4_index_topk_decode(
         _ptr(scores), _ptr(block_table), _ptr(seq_lens), int(max_seq_len), int(topk), int(local_pages),
-        int(kv_groups), _ptr(sel), _ptr(count), _stream(stream), int(seq_lens.shape[0]),
+        int(kv_groups), _ptr(sel), _ptr(count), _ptr(tok), _stream(stream), int(seq_lens.shape[0]),
         _bt_stride(block_table)))
-    return sel, count
+    return (sel, count) if tok is None else (sel, count, tok)
 
 
 def mx4_sparse_pa_decode(q, k_pool, v_pool, block_table, context_lens, softmax_scale, out=None, *,

@@ -24,16 +24,18 @@
 //            per-page TMEM slot), B = the Q tile (N = 16 heads, e4m3, unit
 //            scales), D = the page's 16 score columns in TMEM (all pages kept).
 //            Then PV per page with kind::f16: A = V^T (M = 128 head dims,
-//            K = 128 tokens, bf16), B = P^T (N = 16 heads, bf16), D = the
-//            output accumulator (16 columns), accumulated over pages.
+//            K = 128 token positions, bf16), B = P^T (N = 16 heads, bf16,
+//            MN-major), D = the output accumulator (16 columns), accumulated
+//            over pages.
 //   warps 0-3 softmax: thread m reads TMEM lane m (token 4(m%32)+m/32 of each
 //            page) as each page's QK product completes, takes the per-head
 //            max over valid tokens (shuffles across lanes, shared memory
-//            across warps), then per page writes P^T (bf16, natural token
-//            order) for the PV MMA and sums the bf16 P; finally the combine
-//            above and out = acc / sum, stored as bf16.
-//   warps 6-9, 11-14 widen each page's V into V^T (bf16), one (token pair,
-//            32-dim scale group) cell a thread.
+//            across warps), then per page writes P^T (bf16, at the thread's
+//            token position: two 16-byte stores) for the PV MMA and sums the
+//            bf16 P; finally the combine above and out = acc / sum (bf16).
+//   warps 6-9, 11-14 widen each page's V into V^T (bf16) in the same
+//            token-position order, one (position pair, 32-dim scale group)
+//            cell a thread.
 #pragma once
 
 #include <cuda.h>
@@ -106,24 +108,23 @@ static_assert(AttnSmem::kAlloc <= 227 * 1024, "attention shared memory budget");
 // Instruction descriptors.  QK (kind::mxf8f6f4): A = E2M1 (5, bits 7..9),
 // B = E4M3 (0, bits 10..12), N = 16, M = 128, UE8M0 scales (bit 23), scale
 // ids of K block k in bits 4..5 (B) and 29..30 (A).  PV (kind::f16): F32
-// accumulator (1, bits 4..5), A = B = BF16 (1), both K-major, N = 16, M = 128.
+// accumulator (1, bits 4..5), A = B = BF16 (1), A K-major, B MN-major (bit
+// 16), N = 16, M = 128.
 __device__ __forceinline__ uint32_t attn_idesc_qk(uint32_t k)
 {
     constexpr uint32_t kBase = (5u << 7) | (0u << 10) | ((16u >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
     return kBase | (k << 4) | (k << 29);
 }
-constexpr uint32_t kAttnIdescPv = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kAttnIdescPv =
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
-// Byte offset of element (row, k) of a K-major bf16 operand tile with
-// 128-byte swizzling: 64 elements (128 B) per row and atom, 8-row atoms of
-// 1 KB, `rows` rows per K-atom (K-atoms of 64 elements follow each other).
-__device__ __forceinline__ uint32_t sw128_bf16_offset(int row, int k, int rows)
-{
-    const int ka = k >> 6, kk = k & 63;
-    const uint32_t chunk = static_cast<uint32_t>(kk >> 3) ^ static_cast<uint32_t>(row & 7);
-    return static_cast<uint32_t>(ka) * rows * 128u + static_cast<uint32_t>(row >> 3) * 1024u +
-           static_cast<uint32_t>(row & 7) * 128u + chunk * 16u + static_cast<uint32_t>(kk & 7) * 2u;
-}
+// P^T as an MN-major operand without swizzling: for token position k and
+// head h, byte 256 (k / 8) + 128 (h / 8) + 16 (k % 8) + 2 (h % 8).  Each
+// 8 x 8 core matrix (8 positions x 8 heads, 16 bytes a position) is 128
+// contiguous bytes; the two head halves of a group of 8 positions follow each
+// other (stride 128 B along N) and groups follow every 256 B (along K).  One
+// MMA (K = 16) takes two groups.
+__device__ __forceinline__ uint32_t pt_offset(int k) { return 256u * (k >> 3) + 16u * (k & 7); }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -143,10 +144,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 __device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                                      uint32_t site)
 {
-    if (mbar_test_wait_cluster(bar, parity)) return true;
+    const bool stall = stalled_here(site);
+    if (!stall && mbar_test_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_test_wait_cluster(bar, parity)) return true;
+        if (!stall && mbar_test_wait_cluster(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
@@ -159,15 +161,16 @@ __device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t pari
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 // Widen one eighth of a V page (natural layout in smem: 64 code bytes and 4
-// scale bytes per token) into the bf16 V^T operand tile.  The 256 threads of
-// the 8 widening warps each take one (token pair, 32-dim scale group) cell:
-// lane l of warp slot wi takes group qd = l % 4 and the pair
-// pr = 32 (wi % 2) + (8 qd + l / 4 + 8 (wi / 2)) mod 32 (tokens 2 pr, 2 pr + 1),
-// so that
-//   - the two 16-byte code loads of a warp touch 8 distinct 16-byte bank
-//     groups per quarter-warp (lanes with l & 4 load the odd token first),
-//   - at every store the 32 lanes hold 32 distinct pairs mod 32, whose
-//     4-byte cells of one 128-byte-swizzled V^T row lie in 32 distinct banks.
+// scale bytes per token) into the bf16 V^T operand tile, whose K positions
+// follow the token order of the QK product (position m holds token
+// 4(m%32) + m/32).  The 256 threads of the 8 widening warps each take one
+// (position pair, 32-dim scale group) cell: lane l = 8q + 4s + qd of warp
+// slot wi takes group qd and the pair
+// pr = 32 (wi % 2) + (q + 16 s + 4 qd + 4 (wi / 2)) mod 32 (positions 2 pr,
+// 2 pr + 1 = tokens ta, ta + 4), so that (checked exhaustively on the CPU)
+//   - each 16-byte code load of a quarter-warp touches 8 distinct 16-byte
+//     bank groups,
+//   - at every store the 32 lanes write 32 distinct banks.
 // Conversion without a table: an e2m1 code s|E|m (E two bits) placed as
 // bf16 bits (E m) << 6 | s << 15 is the bf16 number 2^-126 times its value
 // (a subnormal for E = 0, exact), so one packed multiply by 2^(b-1) (bf16
@@ -180,25 +183,23 @@ __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc
                                            int valid)
 {
     const int qd = lane & 3;
-    const int pr = 32 * (wi & 1) + ((8 * qd + (lane >> 2) + 8 * (wi >> 1)) & 31);
-    const int t0 = 2 * pr;
-    const bool odd_first = (lane & 4) != 0;
-    const uint4 f = *reinterpret_cast<const uint4 *>(vc + (t0 + (odd_first ? 1 : 0)) * 64 + qd * 16);
-    const uint4 g = *reinterpret_cast<const uint4 *>(vc + (t0 + (odd_first ? 0 : 1)) * 64 + qd * 16);
-    const uint4 a = odd_first ? g : f;     // token t0
-    const uint4 c = odd_first ? f : g;     // token t0 + 1
-    const uint32_t b0 = t0 < valid ? vsc[t0 * 4 + qd] : 0u;
-    const uint32_t b1 = t0 + 1 < valid ? vsc[(t0 + 1) * 4 + qd] : 0u;
+    const int pr = 32 * (wi & 1) + (((lane >> 3) + 16 * ((lane >> 2) & 1) + 4 * qd + 4 * (wi >> 1)) & 31);
+    const int k0 = 2 * pr;                                   // K position of the pair's first token
+    const int ta = token_of_col(k0), tb = ta + 4;            // its two tokens
+    const uint4 a = *reinterpret_cast<const uint4 *>(vc + ta * 64 + qd * 16);
+    const uint4 c = *reinterpret_cast<const uint4 *>(vc + tb * 64 + qd * 16);
+    const uint32_t b0 = ta < valid ? vsc[ta * 4 + qd] : 0u;
+    const uint32_t b1 = tb < valid ? vsc[tb * 4 + qd] : 0u;
     const bool one_step = __all_sync(0xffffffffu, b0 <= 128u && b1 <= 128u);
     uint32_t fbits;
     if (one_step)
-        fbits = (t0 < valid ? (b0 + 126u) << 7 : 0u) | (t0 + 1 < valid ? (b1 + 126u) << 23 : 0u);
+        fbits = (ta < valid ? (b0 + 126u) << 7 : 0u) | (tb < valid ? (b1 + 126u) << 23 : 0u);
     else    // 2^(b-127); byte 0 is the subnormal 2^-127 (bits 0x40)
-        fbits = (t0 < valid ? (b0 ? b0 << 7 : 0x40u) : 0u) | (t0 + 1 < valid ? (b1 ? b1 << 23 : 0x400000u) : 0u);
+        fbits = (ta < valid ? (b0 ? b0 << 7 : 0x40u) : 0u) | (tb < valid ? (b1 ? b1 << 23 : 0x400000u) : 0u);
     const __nv_bfloat162 fac = *reinterpret_cast<const __nv_bfloat162 *>(&fbits);
     const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
     const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
-    // v[i]: head dim 32 qd + i of both tokens (t0 in the low half); the
+    // v[i]: head dim 32 qd + i of both tokens (ta in the low half); the
     // multiply by 0x1040 adds the non-overlapping copies x << 6 and x << 12
     uint32_t v[32];
 #pragma unroll
@@ -214,8 +215,8 @@ __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc
         }
     }
     // the store address of head dim 32 qd + 8 r + e is row[e] + 1024 r
-    const uint32_t cch = static_cast<uint32_t>((t0 & 63) >> 3);    // the pair's 16-byte chunk in a row
-    uint8_t *base = vt + (t0 >> 6) * 16384 + (t0 & 7) * 2 + qd * 4096;   // rows 32 qd ..
+    const uint32_t cch = static_cast<uint32_t>((k0 & 63) >> 3);    // the pair's 16-byte chunk in a row
+    uint8_t *base = vt + (k0 >> 6) * 16384 + (k0 & 7) * 2 + qd * 4096;   // rows 32 qd ..
     uint8_t *row[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) row[e] = base + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4);
@@ -410,9 +411,11 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    // K step of 16 tokens: 32 B inside a 128-byte atom row, next K-atom after 4 steps
+                    // K step of 16 positions: 32 B inside a 128-byte atom row of
+                    // V^T (next K-atom after 4 steps); two 256-byte groups of P^T
+                    // (leading offset 256 B along K, stride offset 128 B along N)
                     const uint64_t a = smem_desc(vt + (ks >> 2) * 16384u + (ks & 3) * 32u, 16, 1024, 2);
-                    const uint64_t bd = smem_desc(pt + (ks >> 2) * 2048u + (ks & 3) * 32u, 16, 1024, 2);
+                    const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
                     tc_mma_f16_ss(tmem_base + kAttnOutCol, a, bd, kAttnIdescPv, (j > 0 || ks > 0) ? 1u : 0u);
                 }
                 tc_commit(pvfree(b));
@@ -512,21 +515,28 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 break;
             }
             tc_fence_after();
-            // P^T[h][t] for this lane's token, natural order
+            // P^T at this lane's token position m (token tok_m): its 16 heads
+            // as two 16-byte stores
             {
                 uint32_t v[16];
                 tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
                 const bool valid = (pbase + j) * kPage + tok_m < ctx;
-                uint8_t *pt = smem + AttnSmem::kPt + b * 4096;
+                uint32_t w[8];
 #pragma unroll
-                for (int h = 0; h < kAttnN; ++h) {
-                    float pr = 0.0f;
-                    if (valid && h < G)
-                        pr = exp2f((__uint_as_float(v[h]) * p.softmax_scale - M[h]) * kLog2e);
-                    const __nv_bfloat16 pb = __float2bfloat16_rn(pr);
-                    S[h] += __bfloat162float(pb);
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + sw128_bf16_offset(h, tok_m, kAttnN)) = pb;
+                for (int h2 = 0; h2 < 8; ++h2) {
+                    float p0 = 0.0f, p1 = 0.0f;
+                    if (valid && 2 * h2 < G)
+                        p0 = exp2f((__uint_as_float(v[2 * h2]) * p.softmax_scale - M[2 * h2]) * kLog2e);
+                    if (valid && 2 * h2 + 1 < G)
+                        p1 = exp2f((__uint_as_float(v[2 * h2 + 1]) * p.softmax_scale - M[2 * h2 + 1]) * kLog2e);
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    S[2 * h2] += __low2float(pb);
+                    S[2 * h2 + 1] += __high2float(pb);
+                    w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
                 }
+                uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(m);
+                *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
             }
             fence_proxy_async_smem();
             __syncwarp();

@@ -118,6 +118,64 @@ mx4_status device_setup(int *sm_count)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Host cache of encoded tensor maps.  A map depends only on the view it
+// describes (device, kind, base pointer, strides, extents), so a call that
+// repeats a view (the usual case: the same pool every step) copies the
+// 128-byte map instead of encoding it again.  Least-recently-used eviction
+// over a small table; guarded by its own mutex.
+enum TmapKind : int { kMapKData = 0, kMapKFp8 = 1, kMapKScale = 2, kMapAttnK = 3, kMapAttnKs = 4 };
+
+struct TmapKey {
+    int dev;
+    int kind;
+    const void *ptr;
+    int64_t s0, s1, pages, heads;
+    bool operator==(const TmapKey &o) const
+    {
+        return dev == o.dev && kind == o.kind && ptr == o.ptr && s0 == o.s0 && s1 == o.s1 && pages == o.pages &&
+               heads == o.heads;
+    }
+};
+
+constexpr int kTmapCacheSize = 64;
+
+struct TmapEntry {
+    TmapKey key;
+    CUtensorMap map;
+    uint64_t used = 0;   // 0 = empty slot
+};
+
+std::mutex g_tmap_mutex;
+TmapEntry g_tmap[kTmapCacheSize];
+uint64_t g_tmap_clock = 0;
+
+// The cached map for `key`, or encode(&map) on a miss (false if encoding failed).
+template <typename Encode>
+bool cached_tmap(const TmapKey &key, CUtensorMap *out, Encode encode)
+{
+    std::lock_guard<std::mutex> lock(g_tmap_mutex);
+    int victim = 0;
+    for (int i = 0; i < kTmapCacheSize; ++i) {
+        if (g_tmap[i].used != 0 && g_tmap[i].key == key) {
+            g_tmap[i].used = ++g_tmap_clock;
+            *out = g_tmap[i].map;
+            return true;
+        }
+        if (g_tmap[i].used < g_tmap[victim].used) victim = i;
+    }
+    if (!encode(out)) return false;
+    g_tmap[victim].key = key;
+    g_tmap[victim].map = *out;
+    g_tmap[victim].used = ++g_tmap_clock;
+    return true;
+}
+
+int current_device()
+{
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 // Page data view as a 4-D tensor of 4-bit elements:
 //   dim0: 128 elements of one token (64 B), dim1: n0 in [0,32) (stride 256 B),
 //   dim2: n1 in [0,4) (stride 64 B), dim3: page id (stride = page stride).
@@ -243,12 +301,18 @@ mx4_status launch(const Args &a)
 
     alignas(64) CUtensorMap tmap_k;
     alignas(64) CUtensorMap tmap_s;
+    const int dev = current_device();
     if (kFp8) {
-        if (!encode_kfp8_map(&tmap_k, a.k_data, a.sd, a.num_pool_pages)) return MX4_ERR_CUDA;
+        const TmapKey kk{dev, kMapKFp8, a.k_data, a.sd, 0, a.num_pool_pages, 0};
+        if (!cached_tmap(kk, &tmap_k, [&](CUtensorMap *m) { return encode_kfp8_map(m, a.k_data, a.sd, a.num_pool_pages); }))
+            return MX4_ERR_CUDA;
         tmap_s = tmap_k;   // unused by the fp8 kernel
     } else {
-        if (!encode_kdata_map(&tmap_k, a.k_data, a.sd, a.num_pool_pages)) return MX4_ERR_CUDA;
-        if (!encode_kscale_map(&tmap_s, a.k_scale, a.ss, a.num_pool_pages)) return MX4_ERR_CUDA;
+        const TmapKey kd{dev, kMapKData, a.k_data, a.sd, 0, a.num_pool_pages, 0};
+        const TmapKey ks{dev, kMapKScale, a.k_scale, a.ss, 0, a.num_pool_pages, 0};
+        if (!cached_tmap(kd, &tmap_k, [&](CUtensorMap *m) { return encode_kdata_map(m, a.k_data, a.sd, a.num_pool_pages); }) ||
+            !cached_tmap(ks, &tmap_s, [&](CUtensorMap *m) { return encode_kscale_map(m, a.k_scale, a.ss, a.num_pool_pages); }))
+            return MX4_ERR_CUDA;
     }
 
     ScoreParams p{};
@@ -283,8 +347,8 @@ mx4_status launch(const Args &a)
 template <bool kDecode>
 mx4_status topk_launch(const float *scores, const int32_t *block_table, const int32_t *cu_seqlens_q,
                        const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len, int max_seq_len,
-                       int topk, int local_pages, int kv_groups, int32_t *sel, int32_t *count, void *stream,
-                       int num_seqs, int64_t block_table_stride)
+                       int topk, int local_pages, int kv_groups, int32_t *sel, int32_t *count, int32_t *tokens,
+                       void *stream, int num_seqs, int64_t block_table_stride)
 {
     if (num_seqs < 0 || max_seq_len < 0 || (!kDecode && max_query_len < 0)) return MX4_ERR_INVALID_ARG;
     if (topk < 1 || local_pages < 0 || local_pages > topk) return MX4_ERR_INVALID_ARG;
@@ -295,8 +359,8 @@ mx4_status topk_launch(const float *scores, const int32_t *block_table, const in
     const int64_t P = (static_cast<int64_t>(max_seq_len) + mx4::kPage - 1) / mx4::kPage;
     if (P > mx4::kTopkMaxPages) return MX4_ERR_UNSUPPORTED;
     if (block_table_stride < P) return MX4_ERR_INVALID_ARG;
-    if (!aligned(scores, 4) || !aligned(sel, 4) || !aligned(count, 4) || !aligned(block_table, 4) ||
-        !aligned(seq_lens, 4))
+    if (!aligned(scores, 4) || !aligned(sel, 4) || !aligned(count, 4) || !aligned(tokens, 4) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4))
         return MX4_ERR_MISALIGNED;
     if (!kDecode && (!aligned(cu_seqlens_q, 4) || !aligned(prefix_lens, 4))) return MX4_ERR_MISALIGNED;
 
@@ -330,6 +394,7 @@ mx4_status topk_launch(const float *scores, const int32_t *block_table, const in
     p.prefix_lens = prefix_lens;
     p.sel = sel;
     p.count = count;
+    p.tokens = tokens;
     p.bt_stride = block_table_stride;
     p.num_seqs = num_seqs;
     p.rows_per_seq = kDecode ? 1 : max_query_len;
@@ -503,18 +568,21 @@ mx4_status mx4_index_logits_decode_fp8(const void *q, int q_is_e4m3, const uint8
 mx4_status mx4_index_topk_prefill(const float *scores, const int32_t *block_table, const int32_t *cu_seqlens_q,
                                   const int32_t *seq_lens, const int32_t *prefix_lens, int max_query_len,
                                   int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
-                                  int32_t *count, void *stream, int num_seqs, int64_t block_table_stride)
+                                  int32_t *count, int32_t *sel_tokens, void *stream, int num_seqs,
+                                  int64_t block_table_stride)
 {
     return topk_launch<false>(scores, block_table, cu_seqlens_q, seq_lens, prefix_lens, max_query_len, max_seq_len,
-                              topk, local_pages, kv_groups, sel, count, stream, num_seqs, block_table_stride);
+                              topk, local_pages, kv_groups, sel, count, sel_tokens, stream, num_seqs,
+                              block_table_stride);
 }
 
 mx4_status mx4_index_topk_decode(const float *scores, const int32_t *block_table, const int32_t *seq_lens,
                                  int max_seq_len, int topk, int local_pages, int kv_groups, int32_t *sel,
-                                 int32_t *count, void *stream, int num_seqs, int64_t block_table_stride)
+                                 int32_t *count, int32_t *sel_tokens, void *stream, int num_seqs,
+                                 int64_t block_table_stride)
 {
     return topk_launch<true>(scores, block_table, nullptr, seq_lens, nullptr, 1, max_seq_len, topk, local_pages,
-                             kv_groups, sel, count, stream, num_seqs, block_table_stride);
+                             kv_groups, sel, count, sel_tokens, stream, num_seqs, block_table_stride);
 }
 
 mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads, int groups,
@@ -567,9 +635,14 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     }
     alignas(64) CUtensorMap tmap_k;
     alignas(64) CUtensorMap tmap_ks;
-    if (!encode_attn_k_map(&tmap_k, k_data, k_data_page_stride, k_data_head_stride, kv_heads, num_pool_pages))
-        return MX4_ERR_CUDA;
-    if (!encode_attn_ks_map(&tmap_ks, k_scale, k_scale_page_stride, k_scale_head_stride, kv_heads, num_pool_pages))
+    const TmapKey kk{dev, kMapAttnK, k_data, k_data_page_stride, k_data_head_stride, num_pool_pages, kv_heads};
+    const TmapKey ks{dev, kMapAttnKs, k_scale, k_scale_page_stride, k_scale_head_stride, num_pool_pages, kv_heads};
+    if (!cached_tmap(kk, &tmap_k, [&](CUtensorMap *m) {
+            return encode_attn_k_map(m, k_data, k_data_page_stride, k_data_head_stride, kv_heads, num_pool_pages);
+        }) ||
+        !cached_tmap(ks, &tmap_ks, [&](CUtensorMap *m) {
+            return encode_attn_ks_map(m, k_scale, k_scale_page_stride, k_scale_head_stride, kv_heads, num_pool_pages);
+        }))
         return MX4_ERR_CUDA;
     mx4::AttnParams p{};
     p.q = q;
@@ -681,5 +754,19 @@ const char *mx4_status_string(int status)
 }
 
 int mx4_abi_version(void) { return MX4_ABI_VERSION; }
+
+#ifdef MX4_STALL_TEST
+// Test build only (compiled with -DMX4_STALL_TEST; not part of the product
+// library or its header): make the waits at `site` (the MX4_DEV_TIMEOUT site
+// numbers) in CTA `cta` of the following launches never see their barrier
+// complete; site -1 turns it off.  Synchronous.
+mx4_status mx4_test_set_stall(int site, int cta)
+{
+    if (cudaMemcpyToSymbol(mx4::g_mx4_stall_site, &site, sizeof site) != cudaSuccess ||
+        cudaMemcpyToSymbol(mx4::g_mx4_stall_cta, &cta, sizeof cta) != cudaSuccess)
+        return MX4_ERR_CUDA;
+    return MX4_OK;
+}
+#endif
 
 }  // extern "C"

@@ -90,7 +90,12 @@ constexpr uint32_t kTmemSfbCol = kTmemSfaCol + 4 * kMmaWarps;
 constexpr uint32_t kStageTxBytes = kDataBytes + kScaleBytes;
 // fp8 index cache: one 16 KB page of 128 tokens x 128 e4m3 bytes, no scales.
 constexpr uint32_t kFp8PageBytes = 128 * 128;
-constexpr uint64_t kWaitLimitNs = 1000000000ull;             // 1 s per wait
+// Every mbarrier wait gives up after this long (1 s; a test build of the
+// library sets a shorter limit to make its stalled waits run out quickly).
+#ifndef MX4_WAIT_LIMIT_NS
+#define MX4_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MX4_WAIT_LIMIT_NS;
 
 static_assert(kTmemSfbCol + 4 * kSfbBufs <= kTmemCols, "TMEM budget");
 
@@ -221,16 +226,38 @@ enum WaitSite : uint32_t {
     kSiteDrain = 9,    // an armed copy had not landed when the CTA was leaving
 };
 
+#ifdef MX4_STALL_TEST
+// Test build only (never in the product library): the waits at one site of
+// one CTA treat their barrier as never completing, as if the arriving side had
+// stalled, so that the time limit and the abort path can be exercised without
+// hanging anything.  Set from the host by mx4_test_set_stall; site -1 = off.
+__device__ int g_mx4_stall_site = -1;
+__device__ int g_mx4_stall_cta = 0;
+__device__ __forceinline__ bool stalled_here(uint32_t site)
+{
+    return static_cast<int>(site) == g_mx4_stall_site && static_cast<int>(blockIdx.x) == g_mx4_stall_cta;
+}
+// Whether some wait of this CTA is stalled (its fast probes are skipped).
+__device__ __forceinline__ bool stall_in_cta()
+{
+    return g_mx4_stall_site >= 0 && static_cast<int>(blockIdx.x) == g_mx4_stall_cta;
+}
+#else
+__device__ __forceinline__ constexpr bool stalled_here(uint32_t) { return false; }
+__device__ __forceinline__ constexpr bool stall_in_cta() { return false; }
+#endif
+
 // Bounded wait: true when the phase completed; false after the time limit or
 // when another role has aborted (then the status word carries the reason:
 // bit 1 = timeout, bit 8 + site = where the wait gave up).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
                                              uint32_t site)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    const bool stall = stalled_here(site);
+    if (!stall && mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (!stall && mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
@@ -600,9 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool tma_next = tc_have;
                 const uint32_t e_bar = empty_bar(ln * kStagesPerLane + pst.idx);
                 const uint32_t e_par = pst.ph ^ 1u;
-                const bool ready = tma_next ? mbar_try_wait3(full_bar(stage), st.ph, dempty_bar(ln), dr.ph ^ 1u,
-                                                             e_bar, e_par)
-                                            : mbar_try_wait2(full_bar(stage), st.ph, dempty_bar(ln), dr.ph ^ 1u);
+                const bool ready = !stall_in_cta() &&
+                                   (tma_next ? mbar_try_wait3(full_bar(stage), st.ph, dempty_bar(ln), dr.ph ^ 1u,
+                                                              e_bar, e_par)
+                                             : mbar_try_wait2(full_bar(stage), st.ph, dempty_bar(ln), dr.ph ^ 1u));
                 if (!__all_sync(0xffffffffu, ready) &&
                     !__all_sync(0xffffffffu,
                                 wait_bounded(full_bar(stage), st.ph, abort_flag, kSiteMmaFull) &&

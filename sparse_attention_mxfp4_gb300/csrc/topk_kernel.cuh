@@ -10,7 +10,8 @@
 //   chosen    = the topk - forced other live pages with the largest values,
 //               ties to the lower page index
 //   emit      = physical ids of forced + chosen in ascending page order,
-//               -1 up to topk, and the count.
+//               -1 up to topk, the count and (optionally) the live tokens of
+//               the selected pages, the context the attention step reads.
 //
 // One CTA per (row, group) work item, grid-stride; or, when there are fewer
 // items than two per SM, one cluster of kTopkSplit CTAs per item: each CTA
@@ -45,6 +46,7 @@ struct TopkParams {
     const int32_t *prefix_lens;    // prefill only
     int32_t *sel;                  // [rows, groups, topk]
     int32_t *count;                // [rows, groups]
+    int32_t *tokens;               // [rows, groups] or null: live tokens of the selected pages
     int64_t bt_stride;
     int64_t num_items;             // num_seqs * rows_per_seq * groups
     int num_seqs;
@@ -337,6 +339,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
         int out_pos = topk_block_scan(n_sel, scan_buf, tot_sel);
         int32_t *dst = p.sel + (row * p.groups + g) * static_cast<int64_t>(p.topk);
         const int32_t *bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+        bool last_taken = false;     // the row's last live page (the only partial one) was selected
         {
             int r = eq_before;
             for (int j = j0; j < j1; ++j) {
@@ -347,10 +350,19 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                     r += k == T;
                 }
                 if (take) dst[out_pos++] = bt[j];
+                if (j == nl - 1) last_taken = take;
             }
         }
         for (int i = tot_sel + tid; i < p.topk; i += kTopkThreads) dst[i] = -1;
         if (tid == 0) p.count[row * p.groups + g] = tot_sel;
+        // every selected page is full except the last live one, which holds
+        // L - 128 (nl - 1) live tokens; its owner (thread 0 when nothing is
+        // live) writes the count
+        if (p.tokens && (nl == 0 ? tid == 0 : (nl - 1 >= j0 && nl - 1 < j1))) {
+            const int64_t full = 128 * static_cast<int64_t>(tot_sel);
+            p.tokens[row * p.groups + g] =
+                static_cast<int32_t>(last_taken ? full - (128 * static_cast<int64_t>(nl) - L) : full);
+        }
         __syncthreads();   // keys and hist are reused by the next item
     }
 }

@@ -13,6 +13,13 @@ from sparse_attention_mxfp4_gb300 import workloads as W
 RTOL = 1e-5
 ATOL = 1e-6
 
+# Decode contexts (pages per row): 9 with a partial last page, 10 partial, 12
+# full, 17 with the 17th partial, 2 partial, 32 partial, 16 full, 58 partial,
+# 31 partial: the last page lands at every offset inside the scorer's 8-page
+# work units and at the end of a CTA's range.  The garbage past each context
+# holds e8m0 bytes 0 and 255 (MXFP4) or the e4m3 NaN codes (fp8).
+RAGGED_DECODE_SEQ_LENS = [1029, 1200, 1536, 2055, 131, 4032, 2048, 7297, 3845]
+
 
 def oracle_run(w: W.Workload, rows=None, logits=False, scores=True, real_pool=False,
                unquantized=False, num_threads=0):

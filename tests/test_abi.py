@@ -34,7 +34,7 @@ def test_header_declarations_match_exports(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mx4_abi_version() == 1
+    assert lib.mx4_abi_version() == 2
     names = [lib.mx4_status_string(i).decode() for i in range(5)]
     assert names == ["MX4_OK", "MX4_ERR_INVALID_ARG", "MX4_ERR_MISALIGNED", "MX4_ERR_UNSUPPORTED",
                      "MX4_ERR_CUDA"]
@@ -164,13 +164,14 @@ def test_fp8_rejections(lib, kw, status):
     (dict(ms=16384 * 128 + 1, bts=16385), mx4.MX4_ERR_UNSUPPORTED),
     (dict(bts=3), mx4.MX4_ERR_INVALID_ARG),                     # narrow block table
     (dict(sc=A + 2), mx4.MX4_ERR_MISALIGNED),
+    (dict(tok=A + 2), mx4.MX4_ERR_MISALIGNED),                   # the optional token count output
     (dict(B=0, sc=None), mx4.MX4_OK),                            # no row
 ])
 def test_topk_rejections(lib, kw, status):
-    a = dict(sc=A, bt=A, sl=A, ms=512, k=4, local=1, groups=1, sel=A, cnt=A, B=1, bts=4)
+    a = dict(sc=A, bt=A, sl=A, ms=512, k=4, local=1, groups=1, sel=A, cnt=A, tok=None, B=1, bts=4)
     a.update(kw)
     assert lib.mx4_index_topk_decode(a["sc"], a["bt"], a["sl"], a["ms"], a["k"], a["local"], a["groups"],
-                                     a["sel"], a["cnt"], None, a["B"], a["bts"]) == status
+                                     a["sel"], a["cnt"], a["tok"], None, a["B"], a["bts"]) == status
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

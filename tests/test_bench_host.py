@@ -107,3 +107,18 @@ def test_profile_traffic_only_for_matching_source(tmp_path, monkeypatch):
     assert bench.profile_traffic("mx4_score_kernel", "decode") is None
     assert bench.profile_traffic("mx4_score_kernel", "no-such-workload") is None
 
+
+
+def test_cpu_baseline_full_and_sampled(monkeypatch):
+    """The CPU baseline runs the oracle on the whole call, or on sampled rows
+    extrapolated by live pairs, and says which."""
+    from sparse_attention_mxfp4_gb300 import workloads as W
+    w = W.make_config("prefill-tiny")
+    full = bench.cpu_baseline_config(w)
+    assert full["kind"] == "oracle" and full["cores"] >= 1 and full["value"] > 0
+    assert not full["extrapolated"] and "full call" in full["sample"]
+    assert full["single_core"]["cores"] == 1
+    monkeypatch.setitem(bench.CPU_SAMPLED_ROWS, "prefill-tiny", 8)
+    part = bench.cpu_baseline_config(w)
+    assert part["extrapolated"] and "8 seeded sampled query rows" in part["sample"]
+    assert part["value"] > 0

@@ -61,16 +61,12 @@ def test_decode_step_chain_on_one_stream(topk):
         mx4.mx4_index_k_write(keys.cuda(), slots.cuda(), c.k_data, c.k_scale, w.k_data_page_stride,
                               w.k_data_page_stride, num_pool_pages=npool, stream=stream)
         scores = c.run(stream=stream)
-        sel, cnt = mx4.mx4_index_topk_decode(scores, c.block_table, c.seq_lens, w.max_seq_len, topk,
-                                             local_pages=1, kv_groups=1, stream=stream)
-        # the selected pages in ascending order end with the (partial) last
-        # page: the row's context is its full selected pages plus that tail
-        sl = c.seq_lens.to(torch.int64)
-        tail = sl - W.PAGE * ((sl + W.PAGE - 1) // W.PAGE - 1)
-        n = cnt[:, 0].to(torch.int64)
-        ctx = torch.where(n > 0, (n - 1) * W.PAGE + tail, torch.zeros_like(n)).to(torch.int32).view(B, 1)
+        # the selection and, for the attention, the live tokens of the selected
+        # pages (listed in ascending order, the partial last page at the end)
+        sel, cnt, ctx = mx4.mx4_index_topk_decode(scores, c.block_table, c.seq_lens, w.max_seq_len, topk,
+                                                  local_pages=1, kv_groups=1, want_tokens=True, stream=stream)
         k_pool = pool[: npool * W.PAGE_BYTES].view(npool, 1, W.PAGE_BYTES)
-        out = mx4.mx4_sparse_pa_decode(q_att.cuda(), k_pool, v_pool.cuda(), sel.view(B, 1, topk), ctx,
+        out = mx4.mx4_sparse_pa_decode(q_att.cuda(), k_pool, v_pool.cuda(), sel.view(B, 1, topk), ctx.view(B, 1),
                                        w.sm_scale, stream=stream)
     torch.cuda.synchronize()
     assert mx4.mx4_index_get_device_status() == 0
@@ -93,16 +89,19 @@ def test_decode_step_chain_on_one_stream(topk):
     compare(sc, ref, what="chain scores")
 
     # 3. the selection over the GPU's scores, bit for bit
-    ref_sel, ref_cnt = oracle.topk(decode=True, scores=sc, block_table=w.block_table.numpy(),
-                                   block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
-                                   max_seq_len=w.max_seq_len, topk=topk, local=1, kv_groups=1)
+    ref_sel, ref_cnt, ref_tok = oracle.topk(decode=True, scores=sc, block_table=w.block_table.numpy(),
+                                            block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
+                                            max_seq_len=w.max_seq_len, topk=topk, local=1, kv_groups=1,
+                                            want_tokens=True)
     np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
     np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    np.testing.assert_array_equal(ctx.cpu().numpy(), ref_tok)
 
-    # 4. attention over the GPU's selection
+    # 4. attention over the GPU's selection, its context the selection's
+    # live tokens
     case = W.AttnCase("chain", q=q_att, k_pool=torch.from_numpy(got_pool[: npool * W.PAGE_BYTES]).view(
         npool, 1, W.PAGE_BYTES), v_pool=v_pool, block_table=sel.cpu().view(B, 1, topk),
-        context_lens=ctx.cpu(), softmax_scale=w.sm_scale)
+        context_lens=ctx.cpu().view(B, 1), softmax_scale=w.sm_scale)
     assert [int(x) for x in case.context_lens[:, 0]] == [
         min(L, (min(topk, (L + 127) // 128) - 1) * 128 + L - 128 * ((L + 127) // 128 - 1)) for L in lens]
     got = out.float().cpu().numpy()

@@ -9,7 +9,8 @@ import torch
 import sparse_attention_mxfp4_gb300 as mx4
 from sparse_attention_mxfp4_gb300 import harness
 from sparse_attention_mxfp4_gb300 import workloads as W
-from helpers import clamp_garbage_scales, compare, logits_accum_allowance, mxfp4_as_fp8, oracle_run
+from helpers import (RAGGED_DECODE_SEQ_LENS, clamp_garbage_scales, compare, logits_accum_allowance, mxfp4_as_fp8,
+                     oracle_run)
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +55,16 @@ def test_fp8_decode_ragged_padded_stride_e4m3_q():
     w = W.make_workload("f8d", seed=71, q_lens=None, seq_lens=[1, 128, 129, 5000, 0, 16384, 77], decode=True,
                         pool_pages=300, cache="fp8", k_data_page_stride=16384 + 80, q_e4m3=True)
     _check(w, real_pool=True)
+
+
+def test_fp8_decode_ragged_last_pages_with_nan_garbage():
+    """Decode over an fp8 cache whose partial last pages hold the e4m3 NaN
+    codes past the live limit, last pages at every offset of a work unit."""
+    w = W.make_workload("f8ragged", seed=26, q_lens=None, seq_lens=RAGGED_DECODE_SEQ_LENS, decode=True,
+                        pool_pages=300, cache="fp8")
+    got = _gpu(w)
+    ref, _ = oracle_run(w)
+    compare(got, ref, what="fp8 ragged decode")
 
 
 def test_fp8_block_table_permutation_bit_identical():

@@ -53,9 +53,11 @@ def test_graph_topk_decode():
     scores = c.run()
     sel = torch.empty((w.total_rows, 2, 6), dtype=torch.int32, device="cuda")
     cnt = torch.empty((w.total_rows, 2), dtype=torch.int32, device="cuda")
+    tok = torch.empty((w.total_rows, 2), dtype=torch.int32, device="cuda")
     _replay_matches(lambda s: mx4.mx4_index_topk_decode(scores, c.block_table, c.seq_lens, w.max_seq_len, 6,
-                                                        local_pages=2, kv_groups=2, sel=sel, count=cnt, stream=s),
-                    [sel, cnt], [-7, -7])
+                                                        local_pages=2, kv_groups=2, sel=sel, count=cnt, tokens=tok,
+                                                        stream=s),
+                    [sel, cnt, tok], [-7, -7, -7])
 
 
 def test_graph_sparse_attention():

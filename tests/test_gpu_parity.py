@@ -13,7 +13,8 @@ import oracle
 import sparse_attention_mxfp4_gb300 as mx4
 from sparse_attention_mxfp4_gb300 import harness
 from sparse_attention_mxfp4_gb300 import workloads as W
-from helpers import ATOL, RTOL, compare, logits_accum_allowance, oracle_run, plain_tolerance_stats
+from helpers import (ATOL, RAGGED_DECODE_SEQ_LENS, RTOL, compare, logits_accum_allowance, oracle_run,
+                     plain_tolerance_stats)
 
 pytestmark = pytest.mark.gpu
 
@@ -152,6 +153,14 @@ def test_wide_scale_logits_against_the_plain_tolerance(case):
 
 def test_decode_ragged_split_views():
     w = W.make_workload("dec", seed=23, q_lens=None, seq_lens=[1, 128, 129, 5000, 0, 16384, 77], decode=True,
+                        pool_pages=300, layout="split", k_data_page_stride=8320, k_scale_page_stride=576)
+    _check(w, real_pool=True)
+
+
+def test_decode_ragged_last_pages():
+    """Decode rows whose last (often partial) page falls at every offset of a
+    work unit, garbage tails with e8m0 bytes 0 and 255, against the oracle."""
+    w = W.make_workload("ragged-dec", seed=25, q_lens=None, seq_lens=RAGGED_DECODE_SEQ_LENS, decode=True,
                         pool_pages=300, layout="split", k_data_page_stride=8320, k_scale_page_stride=576)
     _check(w, real_pool=True)
 

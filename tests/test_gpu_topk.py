@@ -27,9 +27,10 @@ def _topk_gpu(w, scores, k, local, groups, bt=None):
     bt = (w.block_table if bt is None else bt).cuda()
     if w.decode:
         return mx4.mx4_index_topk_decode(scores, bt, w.seq_lens.cuda(), w.max_seq_len, k, local_pages=local,
-                                         kv_groups=groups)
+                                         kv_groups=groups, want_tokens=True)
     return mx4.mx4_index_topk_prefill(scores, bt, w.cu_seqlens_q.cuda(), w.seq_lens.cuda(), w.prefix_lens.cuda(),
-                                      w.max_query_len, w.max_seq_len, k, local_pages=local, kv_groups=groups)
+                                      w.max_query_len, w.max_seq_len, k, local_pages=local, kv_groups=groups,
+                                      want_tokens=True)
 
 
 def _topk_oracle(w, scores_np, k, local, groups, rows=None):
@@ -37,17 +38,18 @@ def _topk_oracle(w, scores_np, k, local, groups, rows=None):
                        block_table_stride=w.block_table_stride, seq_lens=w.seq_lens.numpy(),
                        cu_seqlens_q=None if w.decode else w.cu_seqlens_q.numpy(),
                        prefix_lens=None if w.decode else w.prefix_lens.numpy(), max_seq_len=w.max_seq_len,
-                       topk=k, local=local, kv_groups=groups, rows=rows)
+                       topk=k, local=local, kv_groups=groups, rows=rows, want_tokens=True)
 
 
 def _check_chain(w, k, local, groups):
     c = harness.to_device(w)
     scores = c.run()
-    sel, cnt = _topk_gpu(w, scores, k, local, groups)
+    sel, cnt, tok = _topk_gpu(w, scores, k, local, groups)
     torch.cuda.synchronize()
-    ref_sel, ref_cnt = _topk_oracle(w, scores.cpu().numpy(), k, local, groups)
+    ref_sel, ref_cnt, ref_tok = _topk_oracle(w, scores.cpu().numpy(), k, local, groups)
     np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
     np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref_tok)
 
 
 @pytest.mark.parametrize("k,local,groups", [(4, 1, 1), (1, 1, 1), (3, 0, 2), (16, 4, 4), (5, 5, 64)])
@@ -90,11 +92,12 @@ def test_ties_signed_zeros_and_scalar_path(P_tokens, offset):
     scores = base[offset:].view(vals.shape)
     scores.copy_(vals.cuda())
     for k, local, groups in ((3, 1, 1), (7, 2, 2), (40, 1, 8)):
-        sel, cnt = _topk_gpu(w, scores, k, local, groups)
+        sel, cnt, tok = _topk_gpu(w, scores, k, local, groups)
         torch.cuda.synchronize()
-        ref_sel, ref_cnt = _topk_oracle(w, host, k, local, groups)
+        ref_sel, ref_cnt, ref_tok = _topk_oracle(w, host, k, local, groups)
         np.testing.assert_array_equal(cnt.cpu().numpy(), ref_cnt)
         np.testing.assert_array_equal(sel.cpu().numpy(), ref_sel)
+        np.testing.assert_array_equal(tok.cpu().numpy(), ref_tok)
 
 
 @pytest.mark.parametrize("name,k,rows", [("decode", 16, None), ("decode", 64, None), ("prefill-long", 16, 64)])
@@ -102,13 +105,15 @@ def test_topk_full_size(name, k, rows):
     w = W.make_config(name)
     c = harness.to_device(w)
     scores = c.run()
-    sel, cnt = _topk_gpu(w, scores, k, 1, 1)
+    sel, cnt, tok = _topk_gpu(w, scores, k, 1, 1)
     torch.cuda.synchronize()
     r = None if rows is None else W.sample_rows(w, rows, 1)
     sc_host = scores.cpu().numpy()
-    ref_sel, ref_cnt = _topk_oracle(w, sc_host, k, 1, 1, rows=r)
+    ref_sel, ref_cnt, ref_tok = _topk_oracle(w, sc_host, k, 1, 1, rows=r)
     got_sel = sel.cpu().numpy() if r is None else sel.cpu().numpy()[r]
     got_cnt = cnt.cpu().numpy() if r is None else cnt.cpu().numpy()[r]
+    got_tok = tok.cpu().numpy() if r is None else tok.cpu().numpy()[r]
     np.testing.assert_array_equal(got_cnt, ref_cnt)
     np.testing.assert_array_equal(got_sel, ref_sel)
+    np.testing.assert_array_equal(got_tok, ref_tok)
     del c, scores

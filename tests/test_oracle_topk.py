@@ -123,3 +123,28 @@ def test_prefill_rows_use_their_own_live_limit():
                            cu_seqlens_q=[0, 3], prefix_lens=[254], max_seq_len=512, topk=2, local=1)
     assert list(cnt[:, 0]) == [2, 2, 2]
     assert list(sel[0, 0]) == [20, 21] and list(sel[1, 0]) == [20, 21] and list(sel[2, 0]) == [20, 22]
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 1000, 1024, 4095])
+def test_selected_tokens_special_cases(L):
+    """The live-token count of the selected pages against what the selection
+    fixes on its own: every live page taken gives the whole context L; only
+    the forced tail page (topk 1) gives L's last page, L - 128 (ceil(L/128) -
+    1); when every selected page is full (L a multiple of 128), 128 per page."""
+    rng = np.random.default_rng(L)
+    P = 32
+    sc = rng.standard_normal((1, 64, P)).astype(np.float32)
+    bt = np.arange(P, dtype=np.int32).reshape(1, P)
+    nl = (L + 127) // 128
+    kw = dict(decode=True, scores=sc, block_table=bt, block_table_stride=P, seq_lens=[L], max_seq_len=P * 128,
+              want_tokens=True)
+    _, cnt, tok = oracle.topk(topk=P, local=1, **kw)
+    assert cnt[0, 0] == nl and tok[0, 0] == L
+    _, cnt, tok = oracle.topk(topk=1, local=1, **kw)
+    assert cnt[0, 0] == 1 and tok[0, 0] == L - 128 * (nl - 1)
+    for k, local in ((3, 0), (5, 2)):
+        _, cnt, tok = oracle.topk(topk=k, local=local, **kw)
+        if L % 128 == 0:
+            assert tok[0, 0] == 128 * cnt[0, 0]
+        # a selection without the partial tail page is all full pages
+        assert tok[0, 0] in (128 * cnt[0, 0], 128 * (cnt[0, 0] - 1) + L - 128 * (nl - 1))
