@@ -100,7 +100,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-i", str(self.gpu), "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -128,9 +128,10 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return None
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": [],
+                    "note": "no nvidia-smi sample fell inside the sampling window (warm-up and timed region)"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons), "window": "warm-up calls, graph capture and the timed replay"}
 
 
 def library_source_hash():
@@ -726,7 +727,12 @@ def run_ours(args):
 
     # W eager warm-up calls, then the K timed steps as one replay of a CUDA
     # graph holding K calls (captured and replayed once untimed first), so
-    # the number is device time without host launch gaps.
+    # the number is device time without host launch gaps.  The clock samples
+    # cover the warm-up and the timed replay (a short timed region alone may
+    # fall between two samples).
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             case.run(out=out, stream=stream)
@@ -734,9 +740,6 @@ def run_ours(args):
         graph = capture_calls(case, out, args.steps, stream)
         graph.replay()
         torch.cuda.synchronize()
-    sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
