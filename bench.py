@@ -94,7 +94,22 @@ class ClockSampler:
         self.proc = None
         self.path = os.path.join(tempfile.gettempdir(), f"mx4_clocks_bench_{os.getpid()}.csv")
 
+    def _lines(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for ln in f if ln.count(",") >= 8)
+        except OSError:
+            return 0
+
+    def _wait_for_lines(self, n: int, timeout_s: float):
+        t0 = time.time()
+        while self._lines() < n and time.time() - t0 < timeout_s and self.proc.poll() is None:
+            time.sleep(0.005)
+
     def start(self):
+        """Start sampling and return once the first sample is written
+        (nvidia-smi takes a moment to start; a short timed region would
+        otherwise pass before it)."""
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
@@ -103,10 +118,14 @@ class ClockSampler:
                  "-i", str(self.gpu), "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        self._wait_for_lines(1, 15.0)
 
     def stop(self):
         if self.proc is None:
             return None
+        # one more sample taken after the timed region ended
+        self._wait_for_lines(self._lines() + 1, 2.0)
         self.proc.send_signal(signal.SIGTERM)
         try:
             self.proc.wait(timeout=5)
@@ -131,7 +150,9 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0, "reasons": [],
                     "note": "no nvidia-smi sample fell inside the sampling window (warm-up and timed region)"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons), "window": "warm-up calls, graph capture and the timed replay"}
+                "reasons": sorted(reasons),
+                "window": "every 20 ms from just before the warm-up calls to the first sample after the timed "
+                          "replay (a timed region shorter than 20 ms may fall between two samples)"}
 
 
 def library_source_hash():

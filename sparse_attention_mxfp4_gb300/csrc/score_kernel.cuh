@@ -691,7 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = m % kHeads;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t d_taddr = tmem_base + lane_addr + set * 128u;
-        float *stg = reinterpret_cast<float *>(smem + SmemLayout::kOut) + (set * 128 + m) * kChunk;
+        // this thread's staged page maxima of the current unit, page-major
+        // (page i of the unit at stg[128 i]): the per-page stores of a warp
+        // fill 32 consecutive words, free of bank conflicts
+        float *stg = reinterpret_cast<float *>(smem + SmemLayout::kOut) + set * 128 * kChunk + m;
         const float sm_scale = p.sm_scale;
         Ring dr;
         int st_idx = 0;
@@ -779,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(dempty_bar(set));
-                            stg[j - j0] = mx * sm_scale;
+                            stg[128 * (j - j0)] = mx * sm_scale;
                         } else {
                             float *dst = row_out + static_cast<int64_t>(j) * kPage;
                             const int valid = p.max_seq_len - j * kPage;   // columns that exist
@@ -818,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (has_row) {
                     // no row of the tile sees this page: nothing was computed
                     if (!kLogits) {
-                        stg[j - j0] = -INFINITY;
+                        stg[128 * (j - j0)] = -INFINITY;
                     } else {
                         float *dst = row_out + static_cast<int64_t>(j) * kPage;
                         const int valid = p.max_seq_len - j * kPage;
@@ -832,15 +835,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *dst = row_out + j0;
                 const int n = j1 - j0;
                 if (n == kChunk && (p.out_row_stride & 3) == 0) {
-                    const float4 *src = reinterpret_cast<const float4 *>(stg);
-                    __stcs(reinterpret_cast<float4 *>(dst), src[0]);
-                    __stcs(reinterpret_cast<float4 *>(dst) + 1, src[1]);
+                    __stcs(reinterpret_cast<float4 *>(dst), make_float4(stg[0], stg[128], stg[256], stg[384]));
+                    __stcs(reinterpret_cast<float4 *>(dst) + 1, make_float4(stg[512], stg[640], stg[768], stg[896]));
                 } else if (n == kChunk && (p.out_row_stride & 1) == 0) {
-                    const float2 *src = reinterpret_cast<const float2 *>(stg);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) __stcs(reinterpret_cast<float2 *>(dst) + i, src[i]);
+                    for (int i = 0; i < 4; ++i)
+                        __stcs(reinterpret_cast<float2 *>(dst) + i, make_float2(stg[256 * i], stg[256 * i + 128]));
                 } else {
-                    for (int i = 0; i < n; ++i) dst[i] = stg[i];
+                    for (int i = 0; i < n; ++i) dst[i] = stg[128 * i];
                 }
             }
         }

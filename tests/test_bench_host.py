@@ -122,3 +122,25 @@ def test_cpu_baseline_full_and_sampled(monkeypatch):
     part = bench.cpu_baseline_config(w)
     assert part["extrapolated"] and "8 seeded sampled query rows" in part["sample"]
     assert part["value"] > 0
+
+
+def test_clock_sampler_waits_for_samples(tmp_path, monkeypatch):
+    """The sampler returns from start() only once nvidia-smi has written a
+    sample, and stop() waits for one sample after the timed region, so a
+    region of a few milliseconds still has samples on both sides (a fake
+    nvidia-smi on PATH that starts slowly and then prints every 20 ms)."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\nsleep 0.3\n"
+                    "while true; do echo '0, 1965, 2070, 700.5, 0x4, Not Active, Not Active, Not Active, Active'; "
+                    "sleep 0.02; done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    s.path = str(tmp_path / "clocks.csv")
+    s.start()
+    assert s._lines() >= 1
+    n = s._lines()
+    res = s.stop()
+    assert res["samples"] >= n + 1
+    assert res["sm_mhz"] == 1965.0 and res["sm_max_mhz"] == 2070.0
+    assert res["reasons"] == ["sw_power_cap"]
