@@ -10,32 +10,40 @@
 //     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V.
 //
 // One 2-CTA cluster per row, 512 threads a CTA, each CTA taking half of the
-// row's pages with its own softmax max; at the end each CTA finalises 8 of
-// the 16 heads, reading the peer's partial output, weight sums and maxima
-// from the peer's shared memory (rescaled to the row's max, added,
-// normalised); per CTA:
-//   warp 4   K copies: per page, the K codes (4-D token-permuting TMA view
-//            plus a KV-head dimension, the scorer's smem form) and K scales.
-//   warp 10  V copies: the V codes and scales as two plain bulk copies per
-//            page (natural token order: V is not an MMA operand in MXFP4
-//            form), from the start, four pages deep.
-//   warp 5   MMA: QK per page with tcgen05.mma kind::mxf8f6f4 block_scale,
-//            A = the K page (M = 128 tokens, e2m1, its e8m0 scales copied to a
-//            per-page TMEM slot), B = the Q tile (N = 16 heads, e4m3, unit
-//            scales), D = the page's 16 score columns in TMEM (all pages kept).
-//            Then PV per page with kind::f16: A = V^T (M = 128 head dims,
-//            K = 128 token positions, bf16), B = P^T (N = 16 heads, bf16,
-//            MN-major), D = the output accumulator (16 columns), accumulated
-//            over pages.
+// row's pages.  The pages stream: each page's weights are taken against that
+// page's own per-head maximum m_j, P_j = bf16(2^(x - m_j)) with x the score
+// in log2 units, and its PV product goes to its own TMEM accumulator D_j, so
+// no page waits for the scores of a later one.  With sigma_j = sum_t P_j[t]
+// and M = max_j m_j, at the end
+//     out = sum_j 2^(m_j - M) D_j / sum_j 2^(m_j - M) sigma_j,
+// which is the softmax above up to the bf16 rounding of the weights; the
+// two CTAs then combine their halves the same way, each finalising 8 of the
+// 16 heads from the partial output, weight sums and maxima that the peer
+// pushed into its shared memory.  Per CTA:
+//   warp 4   copies: per page, the K codes (4-D token-permuting TMA view
+//            plus a KV-head dimension, the scorer's smem form) and K scales,
+//            and the V codes and scales as two plain bulk copies (natural
+//            token order), four pages deep each.
+//   warp 5   QK MMAs (one thread): per page as soon as its K page lands,
+//            tcgen05.mma kind::mxf8f6f4 block_scale, A = the K page (M = 128
+//            tokens, e2m1, its e8m0 scales copied to a per-page TMEM slot),
+//            B = the Q tile (N = 16 heads, e4m3, unit scales), D = the page's
+//            16 score columns.
+//   warps 15, 10  PV MMAs (one thread each, even and odd pages): per page as
+//            soon as its operands are written, kind::f16, A = V^T (M = 128
+//            head dims, K = 128 tokens, bf16, MN-major), B = P^T (N = 16
+//            heads, bf16, MN-major), D = the page's 16 accumulator columns.
+//            A warp issues one of these small MMAs every hundred-odd cycles,
+//            so the PV products of a page take two warps to keep up.
 //   warps 0-3 softmax: thread m reads TMEM lane m (token 4(m%32)+m/32 of each
-//            page) as each page's QK product completes, takes the per-head
-//            max over valid tokens (shuffles across lanes, shared memory
-//            across warps), then per page writes P^T (bf16, at the thread's
-//            token position: two 16-byte stores) for the PV MMA and sums the
-//            bf16 P; finally the combine above and out = acc / sum (bf16).
-//   warps 6-9, 11-14 widen each page's V into V^T (bf16) in the same
-//            token-position order, one (position pair, 32-dim scale group)
-//            cell a thread.
+//            page) as each page's QK product completes, takes the page's
+//            per-head max (redux.sync in the warp, shared memory across the
+//            four warps), writes P^T (bf16, at the token's position: two
+//            16-byte stores) and the warp's per-head sums of the bf16
+//            weights; finally folds the D_j and sigma_j with the factors
+//            2^(m_j - M), and the cluster combine.
+//   warps 6-9, 11-14 widen each page's V into V^T (bf16, natural token
+//            order), two (token, 32-dim scale group) cells a thread.
 #pragma once
 
 #include <cuda.h>
@@ -47,23 +55,25 @@
 
 namespace mx4 {
 
-// warps 0-3 softmax (P^T), 4 K copies, 5 MMA, 6-9 and 11-14 V widening,
-// 10 V copies, 15 idle (the block is 16 warps so that 4 sit on each SM
+// warps 0-3 softmax (P^T), 4 copies, 5 QK MMAs, 6-9 and 11-14 V widening,
+// 10 and 15 PV MMAs (the block is 16 warps so that 4 sit on each SM
 // sub-partition: 128 registers a thread)
 constexpr int kAttnThreads = 512;
 constexpr int kAttnWidenWarps = 8;
 constexpr int kAttnMaxPages = 24;       // pages a row may list
 constexpr int kAttnSplit = 2;           // CTAs (one cluster) per row: each takes half of the row's pages
-constexpr int kAttnCtaPages = (kAttnMaxPages + kAttnSplit - 1) / kAttnSplit;   // scores kept in TMEM
+constexpr int kAttnCtaPages = (kAttnMaxPages + kAttnSplit - 1) / kAttnSplit;   // pages a CTA may take
 constexpr int kAttnN = 16;              // query heads per KV head (fewer are zero-padded)
 constexpr int kAttnKStages = 4;
-constexpr int kAttnVStages = 4;        // V pages load from the start, alongside the K pages
-constexpr int kAttnPvBufs = 3;         // V^T / P^T operand buffers: widening runs up to 3 pages ahead of PV
-constexpr uint32_t kAttnSCol = 0;                                    // page j: 16 columns at 16 j
-constexpr uint32_t kAttnOutCol = kAttnCtaPages * kAttnN;              // 192
-constexpr uint32_t kAttnSfaCol = kAttnOutCol + kAttnN;                // 208: 4 per page
-constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnCtaPages;     // 256
+constexpr int kAttnVStages = 4;         // V pages load from the start, alongside the K pages
+constexpr int kAttnPvBufs = 3;          // V^T / P^T operand buffers: widening runs up to 3 pages ahead of PV
+constexpr uint32_t kAttnSCol = 0;                                        // scores of page j: 16 columns at 16 j
+constexpr uint32_t kAttnAccCol = kAttnCtaPages * kAttnN;                 // 192: PV accumulator of page j at + 16 j
+constexpr uint32_t kAttnSfaCol = kAttnAccCol + kAttnCtaPages * kAttnN;   // 384: K scales, 4 per page
+constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnCtaPages;        // 432: unit Q scales
 static_assert(kAttnSfbCol + 4 <= 512, "attention TMEM budget");
+static_assert(kAttnCtaPages % 4 == 0, "the final fold reads accumulators 4 pages at a time");
+static_assert(kAttnKStages == kAttnVStages, "one copy warp runs the K and V stages in step");
 
 enum AttnSite : uint32_t { kSiteAttnProducer = 6, kSiteAttnMma = 7, kSiteAttnEpi = 8 };
 
@@ -91,12 +101,15 @@ struct AttnSmem {
     static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // 3 x 4 KB
     static constexpr uint32_t kQ = kPt + kAttnPvBufs * 4096;             // 16 x 128 B
     static constexpr uint32_t kUnit = kQ + 2048;                         // 512 B of 0x7F
-    static constexpr uint32_t kRed = kUnit + 512;                        // 4 warps x 16 floats
-    static constexpr uint32_t kComb = kRed + 4 * 16 * 4;                 // the peer's 8 heads x 128 (staged)
-    static constexpr uint32_t kCombS = kComb + 128 * 8 * 4;              // this CTA's 16 sums, then 16 maxima
-    static constexpr uint32_t kBars = kCombS + 2 * 16 * 4;
-    // kfull[4] kempty[4] vfull[4] vempty[4] qready sready[12] pvready[3] pvfree[3] pv_done comb_ready
-    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 1 + kAttnCtaPages + 2 * kAttnPvBufs + 2;
+    static constexpr uint32_t kRed = kUnit + 512;                        // [2][16 heads][4 warps] warp maxima
+    static constexpr uint32_t kPmax = kRed + 2 * 16 * 4 * 4;             // [page][16] page maxima (log2 units)
+    static constexpr uint32_t kPsum = kPmax + kAttnCtaPages * 16 * 4;    // [page][16][4 warps] weight sums
+    static constexpr uint32_t kFac = kPsum + kAttnCtaPages * 16 * 4 * 4; // [page][16] 2^(m_j - M)
+    static constexpr uint32_t kFin = kFac + kAttnCtaPages * 16 * 4;      // this CTA's 16 sums, then 16 maxima
+    static constexpr uint32_t kComb = kFin + 2 * 16 * 4;                 // from the peer: [128 dims][8 heads], sums, maxima
+    static constexpr uint32_t kBars = kComb + 128 * 8 * 4 + 2 * 16 * 4;
+    // kfull[4] kempty[4] vfull[4] vempty[4] qready sready[12] pvready[3] pvfree[3] pv_done qk_done comb_ready
+    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 1 + kAttnCtaPages + 2 * kAttnPvBufs + 3;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kPid = kAbort + 4;                         // page ids of the row
@@ -104,29 +117,49 @@ struct AttnSmem {
     static constexpr uint32_t kAlloc = kEnd + 1024;
 };
 static_assert(AttnSmem::kAlloc <= 227 * 1024, "attention shared memory budget");
+static_assert(AttnSmem::kComb % 16 == 0 && AttnSmem::kRed % 16 == 0 && AttnSmem::kPsum % 16 == 0 &&
+                  AttnSmem::kFac % 16 == 0 && AttnSmem::kQ % 1024 == 0 && AttnSmem::kBars % 8 == 0,
+              "attention shared memory alignment");
 
 // Instruction descriptors.  QK (kind::mxf8f6f4): A = E2M1 (5, bits 7..9),
 // B = E4M3 (0, bits 10..12), N = 16, M = 128, UE8M0 scales (bit 23), scale
 // ids of K block k in bits 4..5 (B) and 29..30 (A).  PV (kind::f16): F32
-// accumulator (1, bits 4..5), A = B = BF16 (1), A K-major, B MN-major (bit
-// 16), N = 16, M = 128.
+// accumulator (1, bits 4..5), A = B = BF16 (1), A MN-major (bit 15), B
+// MN-major (bit 16), N = 16, M = 128.
 __device__ __forceinline__ uint32_t attn_idesc_qk(uint32_t k)
 {
     constexpr uint32_t kBase = (5u << 7) | (0u << 10) | ((16u >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24);
     return kBase | (k << 4) | (k << 29);
 }
 constexpr uint32_t kAttnIdescPv =
-    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+    (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
-// P^T as an MN-major operand without swizzling: for token position k and
-// head h, byte 256 (k / 8) + 128 (h / 8) + 16 (k % 8) + 2 (h % 8).  Each
-// 8 x 8 core matrix (8 positions x 8 heads, 16 bytes a position) is 128
-// contiguous bytes; the two head halves of a group of 8 positions follow each
-// other (stride 128 B along N) and groups follow every 256 B (along K).  One
-// MMA (K = 16) takes two groups.
-__device__ __forceinline__ uint32_t pt_offset(int k) { return 256u * (k >> 3) + 16u * (k & 7); }
+// Both PV operands are MN-major without swizzling: an 8 x 8 core matrix is
+// 8 tokens of 16 bytes (8 bf16 along M or N), 128 contiguous bytes; core
+// matrices follow each other every 128 B along M / N (the stride offset)
+// and every LBO bytes along K (the leading offset):
+//   P^T (N = 16 heads):  byte 256 (t / 8) + 128 (h / 8) + 16 (t % 8) + 2 (h % 8), LBO 256
+//   V^T (M = 128 dims):  byte 2048 (t / 8) + 128 (d / 8) + 16 (t % 8) + 2 (d % 8), LBO 2048
+// One MMA (K = 16) takes two groups of 8 tokens of each.
+__device__ __forceinline__ uint32_t pt_offset(int t) { return 256u * (t >> 3) + 16u * (t & 7); }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier 1 over the 4 softmax warps that also ANDs a predicate
+// across them, so that all four leave a loop at the same iteration.
+__device__ __forceinline__ bool epi_bar_and(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
 
 // prmt.b32 in its default mode: result byte i is byte (sel >> 4i) & 7 of
 // {b, a} (a = bytes 0..3), or that byte's sign bit replicated when bit 3 of
@@ -138,100 +171,109 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
     return d;
 }
 
-// Bounded spin on a barrier that the peer CTA completes remotely (cluster-
-// scope acquire, non-blocking tests); on timeout it records the site and
-// aborts like wait_bounded.
-__device__ __forceinline__ bool wait_cluster_bounded(uint32_t bar, uint32_t parity, volatile uint32_t *abort_flag,
-                                                     uint32_t site)
+// Sum 16 per-head values over the 32 lanes of a warp by halving: at each of
+// the first four exchanges a lane keeps half of its heads and sends the other
+// half to its partner, so lane l ends with head (l >> 1) & 15 (bits 4..1 of
+// l), summed over all 32 lanes after the fifth.
+__device__ __forceinline__ float warp_sum16(const float (&x)[16], int lane)
 {
-    const bool stall = stalled_here(site);
-    if (!stall && mbar_test_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (!stall && mbar_test_wait_cluster(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
-            *abort_flag = 1;
-            return false;
-        }
-    }
+    float a[8], b[4], c[2];
+    const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (u4 ? x[i + 8] : x[i]) + __shfl_xor_sync(0xffffffffu, u4 ? x[i] : x[i + 8], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = (u3 ? a[i + 4] : a[i]) + __shfl_xor_sync(0xffffffffu, u3 ? a[i] : a[i + 4], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i] = (u2 ? b[i + 2] : b[i]) + __shfl_xor_sync(0xffffffffu, u2 ? b[i] : b[i + 2], 4);
+    const float d = (u1 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, u1 ? c[0] : c[1], 2);
+    return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// Maximum over the 32 lanes of a warp, in every lane (NaN inputs are
+// ignored, like fmaxf).
+__device__ __forceinline__ float warp_max(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
 
-// Widen one eighth of a V page (natural layout in smem: 64 code bytes and 4
-// scale bytes per token) into the bf16 V^T operand tile, whose K positions
-// follow the token order of the QK product (position m holds token
-// 4(m%32) + m/32).  The 256 threads of the 8 widening warps each take one
-// (position pair, 32-dim scale group) cell: lane l = 8q + 4s + qd of warp
-// slot wi takes group qd and the pair
-// pr = 32 (wi % 2) + (q + 16 s + 4 qd + 4 (wi / 2)) mod 32 (positions 2 pr,
-// 2 pr + 1 = tokens ta, ta + 4), so that (checked exhaustively on the CPU)
-//   - each 16-byte code load of a quarter-warp touches 8 distinct 16-byte
-//     bank groups,
-//   - at every store the 32 lanes write 32 distinct banks.
-// Conversion without a table: an e2m1 code s|E|m (E two bits) placed as
-// bf16 bits (E m) << 6 | s << 15 is the bf16 number 2^-126 times its value
-// (a subnormal for E = 0, exact), so one packed multiply by 2^(b-1) (bf16
-// bits (b + 126) << 7; b = the token's e8m0 byte) gives the scaled value;
-// when some lane has b > 128 that factor overflows bf16, and the warp
-// multiplies by 2^126 and 2^(b-127) instead.  Tokens at or past `valid` get
-// a zero factor.  Each pair lands in one 4-byte store (adjacent K positions
-// of one V^T row).
+// Wait for bar0 and, when need1, bar1 as well: one probe of both first (one
+// round trip), then bounded waits as wait_bounded.
+__device__ __forceinline__ bool wait2_bounded(uint32_t bar0, uint32_t parity0, bool need1, uint32_t bar1,
+                                              uint32_t parity1, volatile uint32_t *abort_flag, uint32_t site)
+{
+    if (!stalled_here(site) && (need1 ? mbar_try_wait2(bar0, parity0, bar1, parity1) : mbar_try_wait(bar0, parity0)))
+        return true;
+    return wait_bounded(bar0, parity0, abort_flag, site) && (!need1 || wait_bounded(bar1, parity1, abort_flag, site));
+}
+
+// Bytes each CTA pushes into its peer for the combine: 128 dims x 8 heads of
+// the partial output, then 16 weight sums and 16 maxima.
+constexpr uint32_t kCombBytes = 128 * 8 * 4 + 2 * 16 * 4;
+
+// Widen a V page (natural layout in smem: 64 code bytes and 4 scale bytes
+// per token) into the bf16 V^T operand.  The 256 threads of the 8 widening
+// warps each take two (token, 32-dim scale group) cells: lane l = 8 q + i of
+// warp slot wi takes the tokens t = 8 (wi + 8 r) + i (r = 0, 1) in group
+// g = (i / 2 + q) % 4, so that the 16-byte code loads of a quarter-warp
+// touch 8 distinct 16-byte bank groups (their (t % 2, g) all differ) and so
+// do its 16-byte stores (their t % 8 all differ); the four quarters cover a
+// token's four groups.  Conversion without a table: an e2m1 code s|E|m (E
+// two bits) placed as bf16 bits (E m) << 6 | s << 15 is the bf16 number
+// 2^-126 times its value (a subnormal for E = 0, exact), so one packed
+// multiply by 2^(b-1) (bf16 bits (b + 126) << 7; b = the cell's e8m0 byte)
+// gives the scaled value; when some lane has b > 128 that factor overflows
+// bf16, and the warp multiplies by 2^126 and 2^(b-127) instead.  Tokens at
+// or past `valid` get a zero factor.  A cell's 32 dims are 16 pairs of
+// neighbours (the low and high nibble of one code byte, under one scale),
+// stored as four 16-byte rows of 8 dims.
 __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc, uint8_t *vt, int wi, int lane,
                                            int valid)
 {
-    const int qd = lane & 3;
-    const int pr = 32 * (wi & 1) + (((lane >> 3) + 16 * ((lane >> 2) & 1) + 4 * qd + 4 * (wi >> 1)) & 31);
-    const int k0 = 2 * pr;                                   // K position of the pair's first token
-    const int ta = token_of_col(k0), tb = ta + 4;            // its two tokens
-    const uint4 a = *reinterpret_cast<const uint4 *>(vc + ta * 64 + qd * 16);
-    const uint4 c = *reinterpret_cast<const uint4 *>(vc + tb * 64 + qd * 16);
-    const uint32_t b0 = ta < valid ? vsc[ta * 4 + qd] : 0u;
-    const uint32_t b1 = tb < valid ? vsc[tb * 4 + qd] : 0u;
-    const bool one_step = __all_sync(0xffffffffu, b0 <= 128u && b1 <= 128u);
-    uint32_t fbits;
-    if (one_step)
-        fbits = (ta < valid ? (b0 + 126u) << 7 : 0u) | (tb < valid ? (b1 + 126u) << 23 : 0u);
-    else    // 2^(b-127); byte 0 is the subnormal 2^-127 (bits 0x40)
-        fbits = (ta < valid ? (b0 ? b0 << 7 : 0x40u) : 0u) | (tb < valid ? (b1 ? b1 << 23 : 0x400000u) : 0u);
-    const __nv_bfloat162 fac = *reinterpret_cast<const __nv_bfloat162 *>(&fbits);
-    const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t wc[4] = {c.x, c.y, c.z, c.w};
-    // v[i]: head dim 32 qd + i of both tokens (ta in the low half); the
-    // multiply by 0x1040 adds the non-overlapping copies x << 6 and x << 12
-    uint32_t v[32];
+    const int i = lane & 7, q = lane >> 3;
+    const int g = ((i >> 1) + q) & 3;
+    int t[2];
+    uint4 c[2];
+    uint32_t sb[2];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const uint32_t ae = wa[w] & 0x0F0F0F0Fu, ce = wc[w] & 0x0F0F0F0Fu;                  // even dims
-        const uint32_t ao = (wa[w] >> 4) & 0x0F0F0F0Fu, co = (wc[w] >> 4) & 0x0F0F0F0Fu;    // odd dims
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            // byte j of each token in bytes 0 and 2, zeros in bytes 1 and 3
-            const uint32_t sel = static_cast<uint32_t>(j | ((8 + j) << 4) | ((4 + j) << 8) | ((12 + j) << 12));
-            v[8 * w + 2 * j] = (prmt(ae, ce, sel) * 0x1040u) & 0x81C081C0u;
-            v[8 * w + 2 * j + 1] = (prmt(ao, co, sel) * 0x1040u) & 0x81C081C0u;
-        }
+    for (int r = 0; r < 2; ++r) {
+        t[r] = 8 * (wi + 8 * r) + i;
+        c[r] = *reinterpret_cast<const uint4 *>(vc + t[r] * 64 + g * 16);
+        sb[r] = t[r] < valid ? vsc[t[r] * 4 + g] : 0u;
     }
-    // the store address of head dim 32 qd + 8 r + e is row[e] + 1024 r
-    const uint32_t cch = static_cast<uint32_t>((k0 & 63) >> 3);    // the pair's 16-byte chunk in a row
-    uint8_t *base = vt + (k0 >> 6) * 16384 + (k0 & 7) * 2 + qd * 4096;   // rows 32 qd ..
-    uint8_t *row[8];
+    const bool one_step = __all_sync(0xffffffffu, sb[0] <= 128u && sb[1] <= 128u);
+    const uint32_t k126 = 0x7E807E80u;                             // 2^126 in both halves
+    const __nv_bfloat162 two126 = *reinterpret_cast<const __nv_bfloat162 *>(&k126);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) row[e] = base + e * 128 + ((cch ^ static_cast<uint32_t>(e)) << 4);
-    if (one_step) {
+    for (int r = 0; r < 2; ++r) {
+        uint32_t fb;
+        if (one_step)
+            fb = t[r] < valid ? (sb[r] + 126u) << 7 : 0u;
+        else    // 2^(b-127); byte 0 is the subnormal 2^-127 (bits 0x40)
+            fb = t[r] < valid ? (sb[r] ? sb[r] << 7 : 0x40u) : 0u;
+        fb |= fb << 16;
+        const __nv_bfloat162 fac = *reinterpret_cast<const __nv_bfloat162 *>(&fb);
+        const uint32_t wd[4] = {c[r].x, c[r].y, c[r].z, c[r].w};
+        uint8_t *dst = vt + 2048 * (t[r] >> 3) + 16 * (t[r] & 7) + 512 * g;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<__nv_bfloat162 *>(row[i & 7] + (i >> 3) * 1024) =
-                __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i]), fac);
-    } else {
-        const uint32_t k126 = 0x7E807E80u;                             // 2^126 in both halves
-        const __nv_bfloat162 two126 = *reinterpret_cast<const __nv_bfloat162 *>(&k126);
+        for (int w = 0; w < 4; ++w) {
+            // code byte jb of word w: dims 32 g + 8 w + 2 jb (low nibble) and
+            // 32 g + 8 w + 2 jb + 1 (high nibble); the multiply by 0x1040 adds
+            // the non-overlapping copies x << 6 and x << 12
+            const uint32_t lo = wd[w] & 0x0F0F0F0Fu, hi = (wd[w] >> 4) & 0x0F0F0F0Fu;
+            uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            *reinterpret_cast<__nv_bfloat162 *>(row[i & 7] + (i >> 3) * 1024) =
-                __hmul2(__hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&v[i]), two126), fac);
+            for (int jb = 0; jb < 4; ++jb) {
+                const uint32_t sel = static_cast<uint32_t>(jb | ((8 + jb) << 4) | ((4 + jb) << 8) | ((12 + jb) << 12));
+                const uint32_t x = (prmt(lo, hi, sel) * 0x1040u) & 0x81C081C0u;
+                __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&x);
+                if (!one_step) v = __hmul2(v, two126);
+                v = __hmul2(v, fac);
+                o[jb] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+            *reinterpret_cast<uint4 *>(dst + 128 * w) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
     }
 }
 
@@ -259,7 +301,8 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     auto pvready = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + i); };
     auto pvfree = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + kAttnPvBufs + i); };
     const uint32_t pv_done = bar(kB0 + 1 + kAttnCtaPages + 2 * kAttnPvBufs);
-    const uint32_t comb_ready = pv_done + 8;               // the peer has staged its partial results
+    const uint32_t qk_done = pv_done + 8;
+    const uint32_t comb_ready = pv_done + 16;              // the peer has pushed its partial results
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
     int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
 
@@ -274,15 +317,17 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             mbar_init(vfull(i), 1);
             mbar_init(vempty(i), kAttnWidenWarps);
         }
-        // pvready: the 4 softmax warps (P^T) and the 8 widening warps (V^T)
         mbar_init(qready, 4);
         for (int j = 0; j < kAttnCtaPages; ++j) mbar_init(sready(j), 1);
         for (int i = 0; i < kAttnPvBufs; ++i) {
             mbar_init(pvready(i), 4 + kAttnWidenWarps);
             mbar_init(pvfree(i), 1);
         }
-        mbar_init(pv_done, 1);
-        mbar_init(comb_ready, 4);               // the peer's 4 softmax warps (remote)
+        mbar_init(pv_done, 2);                  // one commit from each PV warp
+        mbar_init(qk_done, 1);
+        // completed by the bytes the peer pushes (st.async complete_tx)
+        mbar_init(comb_ready, 1);
+        mbar_arrive_expect_tx(comb_ready, kCombBytes);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -326,34 +371,30 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<uint32_t *>(smem + AttnSmem::kTmemSlot);
 
-    if (warp == 4 || warp == 10) {
+    if (warp == 4) {
         // ------------------------------------------------------------ copies --
-        // warp 4: the K pages (TMA); warp 10: the V pages (bulk copies), from
-        // the start so they overlap the QK phase
+        // K page j once QK of page j - 4 is done, V page j once the widening
+        // of page j - 4 is done; both from the start so they overlap the QK
+        // products
         const uint64_t policy = l2_policy_evict_first();
-        const bool is_k = warp == 4;
-        const int nst = is_k ? kAttnKStages : kAttnVStages;
         int issued = 0;
         for (int j = 0; j < npages; ++j) {
-            const int s = j % nst, u = j / nst;
-            const uint32_t empty_b = is_k ? kempty(s) : vempty(s);
-            if (!__all_sync(0xffffffffu, wait_bounded(empty_b, (u & 1) ^ 1u, abort_flag, kSiteAttnProducer)))
+            const int s = j % kAttnKStages, u = j / kAttnKStages;     // kAttnVStages == kAttnKStages
+            if (!__all_sync(0xffffffffu, wait2_bounded(kempty(s), (u & 1) ^ 1u, true, vempty(s), (u & 1) ^ 1u,
+                                                       abort_flag, kSiteAttnProducer)))
                 break;
             if (elect_one()) {
                 const int64_t pg = pids[pbase + j];
-                if (is_k) {
-                    mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
-                    tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh,
-                                static_cast<int>(pg), policy);
-                    tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, kvh,
-                                static_cast<int>(pg), policy);
-                } else {
-                    mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
-                    bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + kvh * p.vd_hs,
-                              kDataBytes, vfull(s), policy);
-                    bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + kvh * p.vs_hs,
-                              kScaleBytes, vfull(s), policy);
-                }
+                mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
+                tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh,
+                            static_cast<int>(pg), policy);
+                tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, kvh,
+                            static_cast<int>(pg), policy);
+                mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
+                bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + kvh * p.vd_hs,
+                          kDataBytes, vfull(s), policy);
+                bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + kvh * p.vs_hs,
+                          kScaleBytes, vfull(s), policy);
             }
             __syncwarp();
             ++issued;
@@ -361,84 +402,82 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         // no copy may be in flight when the CTA exits: the last use of each
         // stage this warp armed completes (bounded)
         if (lane == 0) {
-            const int n = issued < nst ? issued : nst;
+            const int n = issued < kAttnKStages ? issued : kAttnKStages;
             for (int i = 0; i < n; ++i) {
                 const int j = issued - 1 - i;
-                const uint32_t full_b = is_k ? kfull(j % nst) : vfull(j % nst);
-                if (!drain_bounded(full_b, (j / nst) & 1)) break;
+                if (!drain_bounded(kfull(j % kAttnKStages), (j / kAttnKStages) & 1)) break;
+                if (!drain_bounded(vfull(j % kAttnKStages), (j / kAttnKStages) & 1)) break;
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 5 || warp == 10 || warp == 15) {
         // ----------------------------------------------------------------- MMA --
-        bool ok = __all_sync(0xffffffffu, wait_bounded(qready, 0, abort_flag, kSiteAttnMma));
-        const uint32_t sfb = tmem_base + kAttnSfbCol;
-        const uint64_t qdesc = smem_desc(sbase + AttnSmem::kQ, 16, 1024, 2);
-        if (ok) {
-            tc_fence_after();
-            if (elect_one()) tc_cp_32x128b_warpx4(sfb, smem_desc(sbase + AttnSmem::kUnit, 16, 128, 0));
-            __syncwarp();
-        }
-        for (int j = 0; j < npages && ok; ++j) {
-            const int s = j % kAttnKStages, u = j / kAttnKStages;
-            if (!__all_sync(0xffffffffu, wait_bounded(kfull(s), u & 1, abort_flag, kSiteAttnMma))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (elect_one()) {
-                const uint32_t sfa = tmem_base + kAttnSfaCol + 4u * j;
-                tc_cp_32x128b_warpx4(sfa, smem_desc(sbase + AttnSmem::kKs + s * kScaleBytes, 16, 128, 0));
-                const uint64_t kdesc = smem_desc(sbase + AttnSmem::kK + s * kTileBytes, 16, 1024, 2);
-                const uint32_t d = tmem_base + kAttnSCol + kAttnN * j;
-#pragma unroll
-                for (uint32_t k = 0; k < 4; ++k)
-                    tc_mma_mx_ss(d, kdesc + 2 * k, qdesc + 2 * k, attn_idesc_qk(k), sfa, sfb, k > 0 ? 1u : 0u);
-                tc_commit(kempty(s));
-                tc_commit(sready(j));
-            }
-            __syncwarp();
-        }
-        for (int j = 0; j < npages && ok; ++j) {
-            const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
-            if (!__all_sync(0xffffffffu, wait_bounded(pvready(b), u & 1, abort_flag, kSiteAttnMma))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            if (elect_one()) {
-                const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
-                const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    // K step of 16 positions: 32 B inside a 128-byte atom row of
-                    // V^T (next K-atom after 4 steps); two 256-byte groups of P^T
-                    // (leading offset 256 B along K, stride offset 128 B along N)
-                    const uint64_t a = smem_desc(vt + (ks >> 2) * 16384u + (ks & 3) * 32u, 16, 1024, 2);
-                    const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
-                    tc_mma_f16_ss(tmem_base + kAttnOutCol, a, bd, kAttnIdescPv, (j > 0 || ks > 0) ? 1u : 0u);
+        // Separate issuing warps, so that neither kind of product waits
+        // behind the other: warp 5 issues the QK products as the K pages
+        // land, warps 15 and 10 the PV products of the even and odd pages as
+        // V^T and P^T are written.  Each waits for its own products to
+        // complete before the CTA frees TMEM.
+        if (lane == 0) {
+            const bool is_qk = warp == 5;
+            bool ok = true;
+            if (is_qk) {
+                ok = wait_bounded(qready, 0, abort_flag, kSiteAttnMma);
+                const uint32_t sfb = tmem_base + kAttnSfbCol;
+                const uint64_t qdesc = smem_desc(sbase + AttnSmem::kQ, 16, 1024, 2);
+                if (ok) {
+                    tc_fence_after();
+                    tc_cp_32x128b_warpx4(sfb, smem_desc(sbase + AttnSmem::kUnit, 16, 128, 0));
                 }
-                tc_commit(pvfree(b));
+                for (int j = 0; j < npages && ok; ++j) {
+                    const int s = j % kAttnKStages;
+                    if (!(ok = wait_bounded(kfull(s), (j / kAttnKStages) & 1, abort_flag, kSiteAttnMma))) break;
+                    tc_fence_after();
+                    const uint32_t sfa = tmem_base + kAttnSfaCol + 4u * j;
+                    tc_cp_32x128b_warpx4(sfa, smem_desc(sbase + AttnSmem::kKs + s * kScaleBytes, 16, 128, 0));
+                    const uint64_t kdesc = smem_desc(sbase + AttnSmem::kK + s * kTileBytes, 16, 1024, 2);
+                    const uint32_t d = tmem_base + kAttnSCol + kAttnN * j;
+#pragma unroll
+                    for (uint32_t k = 0; k < 4; ++k)
+                        tc_mma_mx_ss(d, kdesc + 2 * k, qdesc + 2 * k, attn_idesc_qk(k), sfa, sfb, k > 0 ? 1u : 0u);
+                    tc_commit(kempty(s));
+                    tc_commit(sready(j));
+                }
+            } else {
+                // page j waits here only after page j - 2 was ready, hence
+                // page j - 3 (the previous phase of its buffer's barrier) too
+                for (int j = warp == 15 ? 0 : 1; j < npages && ok; j += 2) {
+                    const int b = j % kAttnPvBufs;
+                    if (!(ok = wait_bounded(pvready(b), (j / kAttnPvBufs) & 1, abort_flag, kSiteAttnMma))) break;
+                    tc_fence_after();
+                    const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
+                    const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
+                    const uint32_t d = tmem_base + kAttnAccCol + kAttnN * j;
+#pragma unroll
+                    for (uint32_t ks = 0; ks < 8; ++ks) {
+                        // K step of 16 tokens: two 8-token groups of each operand
+                        const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
+                        const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
+                        tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : 0u);
+                    }
+                    tc_commit(pvfree(b));
+                }
             }
-            __syncwarp();
-        }
-        if (elect_one()) tc_commit(pv_done);
-        __syncwarp();
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(pv_done, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            // every product issued above completes before TMEM is read or freed
+            const uint32_t done_b = is_qk ? qk_done : pv_done;
+            tc_commit(done_b);
+            const uint64_t t1 = globaltimer_ns();
+            while (!mbar_try_wait(done_b, 0) && globaltimer_ns() - t1 < kWaitLimitNs) {
+            }
         }
         __syncwarp();
     } else if (warp >= 6) {
         // ---------------------------------------------------------- V widening --
-        // warps 6-9 and 11-14 widen one eighth of each page each (warp 10
-        // is the V copy warp above, warp 15 has no role)
-        if (warp == 15) goto done;
+        // warps 6-9 and 11-14 (warps 10 and 15 are PV issuers)
         for (int j = 0; j < npages; ++j) {
             const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
             const int vs = j % kAttnVStages;
-            if (!__all_sync(0xffffffffu,
-                            (u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi)) &&
-                                wait_bounded(vfull(vs), (j / kAttnVStages) & 1, abort_flag, kSiteAttnEpi)))
+            if (!__all_sync(0xffffffffu, wait2_bounded(vfull(vs), (j / kAttnVStages) & 1, u > 0, pvfree(b),
+                                                       (u - 1) & 1, abort_flag, kSiteAttnEpi)))
                 break;
             attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
                        smem + AttnSmem::kVt + b * 32768, warp < 10 ? warp - 6 : warp - 7, lane,
@@ -456,6 +495,11 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
         const int tok_m = token_of_col(m);               // token of lane m within each page
         const int G = p.groups;
+        float *red = reinterpret_cast<float *>(smem + AttnSmem::kRed);
+        float *pmax = reinterpret_cast<float *>(smem + AttnSmem::kPmax);
+        float *fac = reinterpret_cast<float *>(smem + AttnSmem::kFac);
+        float *fin = reinterpret_cast<float *>(smem + AttnSmem::kFin);
+        float *psum = reinterpret_cast<float *>(smem + AttnSmem::kPsum);
         {
             // Q tile (16 rows x 128 B, SW128) and the unit scale block
             const int h = m >> 3, c = m & 7;
@@ -467,159 +511,148 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             __syncwarp();
             if (lane == 0) mbar_arrive(qready);
         }
-        float M[kAttnN], S[kAttnN];
-#pragma unroll
-        for (int h = 0; h < kAttnN; ++h) {
-            M[h] = -INFINITY;
-            S[h] = 0.0f;
-        }
-        // pass A: this CTA's per-head max over its valid tokens, page by page
-        // as the QK products complete
+        // scores in log2 units: x = s * softmax_scale * log2(e)
+        const float sl = p.softmax_scale * 1.4426950408889634f;
+        const int hl = lane & 15;
         bool ok = true;
-        for (int j = 0; j < npages; ++j) {
-            if (!__all_sync(0xffffffffu, wait_bounded(sready(j), 0, abort_flag, kSiteAttnEpi))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
-            if ((pbase + j) * kPage + tok_m < ctx) {
-#pragma unroll
-                for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __uint_as_float(v[h]) * p.softmax_scale);
-            }
-        }
         // (the named-barrier syncs below run on every path, so the four
         // warps always pass the same number of them)
-        float *red = reinterpret_cast<float *>(smem + AttnSmem::kRed);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], o));
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h) red[warp * kAttnN + h] = M[h];
-        }
-        epi_bar_sync();
-#pragma unroll
-        for (int h = 0; h < kAttnN; ++h)
-            M[h] = fmaxf(fmaxf(red[h], red[kAttnN + h]), fmaxf(red[2 * kAttnN + h], red[3 * kAttnN + h]));
-        epi_bar_sync();
-        // pass B: per page P^T and V^T for the PV MMA
-        constexpr float kLog2e = 1.4426950408889634f;
-        for (int j = 0; j < npages && ok; ++j) {
+        for (int j = 0; j < npages; ++j) {
             const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
-            if (!__all_sync(0xffffffffu,
-                            u == 0 || wait_bounded(pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // P^T at this lane's token position m (token tok_m): its 16 heads
-            // as two 16-byte stores
-            {
+            const bool okw = __all_sync(
+                0xffffffffu, wait2_bounded(sready(j), 0, u > 0, pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi));
+            const bool valid = (pbase + j) * kPage + tok_m < ctx;
+            float x[16];
+            if (okw) {
+                tc_fence_after();
                 uint32_t v[16];
                 tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
-                const bool valid = (pbase + j) * kPage + tok_m < ctx;
-                uint32_t w[8];
+                float wm = 0.0f;
 #pragma unroll
-                for (int h2 = 0; h2 < 8; ++h2) {
-                    float p0 = 0.0f, p1 = 0.0f;
-                    if (valid && 2 * h2 < G)
-                        p0 = exp2f((__uint_as_float(v[2 * h2]) * p.softmax_scale - M[2 * h2]) * kLog2e);
-                    if (valid && 2 * h2 + 1 < G)
-                        p1 = exp2f((__uint_as_float(v[2 * h2 + 1]) * p.softmax_scale - M[2 * h2 + 1]) * kLog2e);
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                    S[2 * h2] += __low2float(pb);
-                    S[2 * h2 + 1] += __high2float(pb);
-                    w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
+                for (int h = 0; h < kAttnN; ++h) {
+                    x[h] = valid ? __uint_as_float(v[h]) * sl : -INFINITY;
+                    const float r = warp_max(x[h]);
+                    wm = hl == h ? r : wm;
                 }
-                uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(m);
-                *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                if (lane < kAttnN) red[((j & 1) * 16 + lane) * 4 + warp] = wm;
             }
+            ok = epi_bar_and(okw);
+            if (!ok) break;
+            // the page's max of head hl over the four warps, then every head's
+            const float4 r4 = reinterpret_cast<const float4 *>(red)[(j & 1) * 16 + hl];
+            const float mh = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+            if (warp == 0 && lane < kAttnN) pmax[j * 16 + lane] = mh;
+            uint32_t w[8];
+            float ps[16];
+#pragma unroll
+            for (int h2 = 0; h2 < 8; ++h2) {
+                const float m0 = __shfl_sync(0xffffffffu, mh, 2 * h2);
+                const float m1 = __shfl_sync(0xffffffffu, mh, 2 * h2 + 1);
+                const float p0 = valid && 2 * h2 < G ? ex2_approx(x[2 * h2] - m0) : 0.0f;
+                const float p1 = valid && 2 * h2 + 1 < G ? ex2_approx(x[2 * h2 + 1] - m1) : 0.0f;
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                ps[2 * h2] = __low2float(pb);
+                ps[2 * h2 + 1] = __high2float(pb);
+                w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
+            }
+            uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(tok_m);
+            *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+            // P^T visible to the tensor core
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(pvready(b));
-        }
-        // the normaliser: sum of the bf16 weights over all lanes
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h) S[h] += __shfl_xor_sync(0xffffffffu, S[h], o);
-        if (lane == 0) {
-#pragma unroll
-            for (int h = 0; h < kAttnN; ++h) red[warp * kAttnN + h] = S[h];
+            // this warp's per-head sums of the bf16 weights (lanes 2 h, 2 h + 1
+            // hold head h)
+            const float wsum = warp_sum16(ps, lane);
+            if ((lane & 1) == 0) psum[(j * 16 + (lane >> 1)) * 4 + warp] = wsum;
         }
         epi_bar_sync();
-#pragma unroll
-        for (int h = 0; h < kAttnN; ++h) S[h] = (red[h] + red[kAttnN + h]) + (red[2 * kAttnN + h] + red[3 * kAttnN + h]);
-        // output: lane m holds head dim m of every head
+        // per head (threads 0-15): M = max_j m_j, the page factors
+        // 2^(m_j - M) and the CTA's weight sum
+        const int nj = ok ? npages : 0;
+        if (m < kAttnN) {
+            float M = -INFINITY, S = 0.0f;
+            for (int j = 0; j < nj; ++j) M = fmaxf(M, pmax[j * 16 + m]);
+            for (int j = 0; j < nj; ++j) {
+                const float f = ex2_approx(pmax[j * 16 + m] - M);
+                const float4 s4 = reinterpret_cast<const float4 *>(psum)[j * 16 + m];
+                fac[j * 16 + m] = f;
+                S += f * ((s4.x + s4.y) + (s4.z + s4.w));
+            }
+            fin[m] = S;
+            fin[kAttnN + m] = M;
+        }
         if (ok && npages > 0)
             ok = __all_sync(0xffffffffu, wait_bounded(pv_done, 0, abort_flag, kSiteAttnEpi));
-        uint32_t acc[16];
+        epi_bar_sync();
+        // lane m of the accumulators holds head dim m of every head
+        float acc[kAttnN];
+#pragma unroll
+        for (int h = 0; h < kAttnN; ++h) acc[h] = 0.0f;
         if (ok && npages > 0) {
             tc_fence_after();
-            tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnOutCol, acc);
-        } else {
+            for (int j0 = 0; j0 < npages; j0 += 4) {
+                uint32_t v[64];
+                tmem_ld_32x32b_x64(tmem_base + lane_addr + kAttnAccCol + kAttnN * j0, v);
 #pragma unroll
-            for (int h = 0; h < kAttnN; ++h) acc[h] = 0u;
+                for (int jj = 0; jj < 4; ++jj) {
+                    if (j0 + jj < npages) {
+                        const float4 *f4 = reinterpret_cast<const float4 *>(fac) + (j0 + jj) * 4;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const float4 f = f4[q4];
+                            acc[4 * q4 + 0] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 0]), f.x, acc[4 * q4 + 0]);
+                            acc[4 * q4 + 1] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 1]), f.y, acc[4 * q4 + 1]);
+                            acc[4 * q4 + 2] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 2]), f.z, acc[4 * q4 + 2]);
+                            acc[4 * q4 + 3] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 3]), f.w, acc[4 * q4 + 3]);
+                        }
+                    }
+                }
+            }
         }
         // Combine the two halves: rank r finalises heads 8r .. 8r+7.  Each
-        // CTA stages the peer's heads of its accumulator (head-major) and
-        // all its sums and maxima in its own shared memory, arrives on the
-        // peer's comb_ready (release, cluster scope), waits for the peer's
-        // arrival on its own, then reads the peer's staged values (one
-        // coalesced 128-byte cluster load per warp and head), rescales both
-        // halves to the row's max, adds, normalises and stores bf16 (a half
-        // with no weight contributes nothing).
+        // CTA pushes the peer's heads of its accumulator ([dim][8 heads]) and
+        // its 16 sums and maxima into the peer's shared memory with st.async,
+        // whose bytes complete the peer's comb_ready; it then waits for its
+        // own comb_ready, rescales both halves to the row's max, adds,
+        // normalises and stores bf16 (a half with no weight contributes
+        // nothing).
         {
-            float *cm = reinterpret_cast<float *>(smem + AttnSmem::kComb);
+            const uint32_t peer = rank ^ 1u;
+            const uint32_t pc = cluster_map(sbase + AttnSmem::kComb, peer);
+            const uint32_t pbar = cluster_map(comb_ready, peer);
+            float a8[8];
 #pragma unroll
-            for (int h = 0; h < kAttnN; ++h)
-                if ((h >> 3) != static_cast<int>(rank)) cm[(h & 7) * 128 + m] = __uint_as_float(acc[h]);
-            if (threadIdx.x < kAttnN) {
-                float *cs = reinterpret_cast<float *>(smem + AttnSmem::kCombS);
-                float sv = 0.0f, mv = 0.0f;
-#pragma unroll
-                for (int h = 0; h < kAttnN; ++h) {
-                    sv = h == m ? S[h] : sv;
-                    mv = h == m ? M[h] : mv;
-                }
-                cs[m] = sv;
-                cs[kAttnN + m] = mv;
-            }
-            fence_cluster();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(cluster_map(comb_ready, rank ^ 1u));
-            if (__all_sync(0xffffffffu, wait_cluster_bounded(comb_ready, 0, abort_flag, kSiteAttnEpi))) {
-                const uint32_t pm = cluster_map(sbase + AttnSmem::kComb + 4u * m, rank ^ 1u);
-                const uint32_t ps = cluster_map(sbase + AttnSmem::kCombS, rank ^ 1u);
-                float a1[8], s1[8], m1[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    a1[i] = ld_cluster_f32(pm + 512u * i);
-                    s1[i] = ld_cluster_f32(ps + 4u * (8 * rank + i));
-                    m1[i] = ld_cluster_f32(ps + 4u * (kAttnN + 8 * rank + i));
-                }
+            for (int i = 0; i < 8; ++i) a8[i] = peer ? acc[8 + i] : acc[i];
+            st_async_v4_u32(pc + 32u * m, __float_as_uint(a8[0]), __float_as_uint(a8[1]), __float_as_uint(a8[2]),
+                            __float_as_uint(a8[3]), pbar);
+            st_async_v4_u32(pc + 32u * m + 16u, __float_as_uint(a8[4]), __float_as_uint(a8[5]),
+                            __float_as_uint(a8[6]), __float_as_uint(a8[7]), pbar);
+            if (m < 2 * kAttnN) st_async_u32(pc + 4096u + 4u * m, __float_as_uint(fin[m]), pbar);
+            if (__all_sync(0xffffffffu, wait_bounded(comb_ready, 0, abort_flag, kSiteAttnEpi))) {
+                const float *cm = reinterpret_cast<const float *>(smem + AttnSmem::kComb);
+                const float4 c0 = reinterpret_cast<const float4 *>(cm)[2 * m];
+                const float4 c1 = reinterpret_cast<const float4 *>(cm)[2 * m + 1];
+                const float a1[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
                 __nv_bfloat16 *o = p.out + (item * G) * kDim;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    // this thread's own values of head 8 rank + i (static register indexes)
-                    const float a0 = __uint_as_float(rank ? acc[8 + i] : acc[i]);
-                    const float s0 = rank ? S[8 + i] : S[i], m0 = rank ? M[8 + i] : M[i];
-                    const float mx = s1[i] > 0.0f && m1[i] > m0 ? m1[i] : m0;
-                    const float f0 = s0 > 0.0f ? exp2f((m0 - mx) * kLog2e) : 0.0f;
-                    const float f1 = s1[i] > 0.0f ? exp2f((m1[i] - mx) * kLog2e) : 0.0f;
-                    const float a = a0 * f0 + a1[i] * f1, sum = s0 * f0 + s1[i] * f1;
                     const int h = 8 * static_cast<int>(rank) + i;
+                    // this thread's own values of head h (static register indexes)
+                    const float a0 = rank ? acc[8 + i] : acc[i];
+                    const float s0 = fin[h], m0 = fin[kAttnN + h];
+                    const float s1 = cm[1024 + h], m1 = cm[1024 + kAttnN + h];
+                    const float mx = s1 > 0.0f && m1 > m0 ? m1 : m0;
+                    const float f0 = s0 > 0.0f ? ex2_approx(m0 - mx) : 0.0f;
+                    const float f1 = s1 > 0.0f ? ex2_approx(m1 - mx) : 0.0f;
+                    const float a = a0 * f0 + a1[i] * f1, sum = s0 * f0 + s1 * f1;
                     if (h < G) o[h * kDim + m] = __float2bfloat16_rn(sum > 0.0f ? __fdividef(a, sum) : 0.0f);
                 }
             }
         }
     }
 
-done:
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {
