@@ -9,8 +9,10 @@
 // leak):
 //     s[t] = softmax_scale * sum_d q[h,d] K[t,d],  out[h,:] = softmax(s) V.
 //
-// One 2-CTA cluster per row, 512 threads a CTA, each CTA taking half of the
-// row's pages.  The pages stream: each page's weights are taken against that
+// 2-CTA clusters, 512 threads a CTA; a cluster takes rows c, c + C, c + 2C,
+// ... (C clusters, at most as many as fit on the GPU at once), each CTA half
+// of each row's pages, so that one row's tail overlaps the next row's
+// copies.  The pages stream: each page's weights are taken against that
 // page's own per-head maximum m_j, P_j = bf16(2^(x - m_j)) with x the score
 // in log2 units, and its PV product goes to its own TMEM accumulator D_j, so
 // no page waits for the scores of a later one.  With sigma_j = sum_t P_j[t]
@@ -62,18 +64,25 @@ constexpr int kAttnThreads = 512;
 constexpr int kAttnWidenWarps = 8;
 constexpr int kAttnMaxPages = 24;       // pages a row may list
 constexpr int kAttnSplit = 2;           // CTAs (one cluster) per row: each takes half of the row's pages
-constexpr int kAttnCtaPages = (kAttnMaxPages + kAttnSplit - 1) / kAttnSplit;   // pages a CTA may take
+constexpr int kAttnCtaPages = (kAttnMaxPages + kAttnSplit - 1) / kAttnSplit;   // pages a CTA takes of a row
+constexpr int kAttnSlots = kAttnCtaPages;   // TMEM score / accumulator slots, a ring over the CTA's pages
 constexpr int kAttnN = 16;              // query heads per KV head (fewer are zero-padded)
 constexpr int kAttnKStages = 4;
 constexpr int kAttnVStages = 4;         // V pages load from the start, alongside the K pages
 constexpr int kAttnPvBufs = 3;          // V^T / P^T operand buffers: widening runs up to 3 pages ahead of PV
-constexpr uint32_t kAttnSCol = 0;                                        // scores of page j: 16 columns at 16 j
-constexpr uint32_t kAttnAccCol = kAttnCtaPages * kAttnN;                 // 192: PV accumulator of page j at + 16 j
-constexpr uint32_t kAttnSfaCol = kAttnAccCol + kAttnCtaPages * kAttnN;   // 384: K scales, 4 per page
-constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnCtaPages;        // 432: unit Q scales
+// The CTA's g-th page (counted over all its rows) uses slot g % kAttnSlots.
+// A QK product into a slot comes only after the softmax has read the scores
+// of the page 7 before it (K and V copies go in step, V waits on the
+// widening, the widening on PV, PV on the softmax), and a row's PV products
+// only after the softmax has folded the row before, so 12 slots are never
+// overwritten early.
+constexpr uint32_t kAttnSCol = 0;                                     // scores of slot i: 16 columns at 16 i
+constexpr uint32_t kAttnAccCol = kAttnSlots * kAttnN;                 // 192: PV accumulator of slot i at + 16 i
+constexpr uint32_t kAttnSfaCol = kAttnAccCol + kAttnSlots * kAttnN;   // 384: K scales, 4 per slot
+constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnSlots;        // 432: unit Q scales
 static_assert(kAttnSfbCol + 4 <= 512, "attention TMEM budget");
-static_assert(kAttnCtaPages % 4 == 0, "the final fold reads accumulators 4 pages at a time");
 static_assert(kAttnKStages == kAttnVStages, "one copy warp runs the K and V stages in step");
+static_assert(kAttnCtaPages <= 32, "the copy warp holds a row's page ids one per lane");
 
 enum AttnSite : uint32_t { kSiteAttnProducer = 6, kSiteAttnMma = 7, kSiteAttnEpi = 8 };
 
@@ -90,6 +99,7 @@ struct AttnParams {
     int groups;
     int width;
     float softmax_scale;
+    int64_t num_items;                // rows * kv_heads
 };
 
 struct AttnSmem {
@@ -99,26 +109,25 @@ struct AttnSmem {
     static constexpr uint32_t kVs = kV + kAttnVStages * kDataBytes;      // V scales
     static constexpr uint32_t kVt = ((kVs + kAttnVStages * kScaleBytes) + 1023) & ~1023u;   // 3 x 32 KB
     static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // 3 x 4 KB
-    static constexpr uint32_t kQ = kPt + kAttnPvBufs * 4096;             // 16 x 128 B
-    static constexpr uint32_t kUnit = kQ + 2048;                         // 512 B of 0x7F
+    static constexpr uint32_t kQ = kPt + kAttnPvBufs * 4096;             // 2 x (16 x 128 B), by row parity
+    static constexpr uint32_t kUnit = kQ + 2 * 2048;                     // 512 B of 0x7F
     static constexpr uint32_t kRed = kUnit + 512;                        // [2][16 heads][4 warps] warp maxima
-    static constexpr uint32_t kPmax = kRed + 2 * 16 * 4 * 4;             // [page][16] page maxima (log2 units)
+    static constexpr uint32_t kPmax = kRed + 2 * 16 * 4 * 4;             // [page][16] page maxima, then factors
     static constexpr uint32_t kPsum = kPmax + kAttnCtaPages * 16 * 4;    // [page][16][4 warps] weight sums
-    static constexpr uint32_t kFac = kPsum + kAttnCtaPages * 16 * 4 * 4; // [page][16] 2^(m_j - M)
-    static constexpr uint32_t kFin = kFac + kAttnCtaPages * 16 * 4;      // this CTA's 16 sums, then 16 maxima
-    static constexpr uint32_t kComb = kFin + 2 * 16 * 4;                 // from the peer: [128 dims][8 heads], sums, maxima
-    static constexpr uint32_t kBars = kComb + 128 * 8 * 4 + 2 * 16 * 4;
-    // kfull[4] kempty[4] vfull[4] vempty[4] qready sready[12] pvready[3] pvfree[3] pv_done qk_done comb_ready
-    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 1 + kAttnCtaPages + 2 * kAttnPvBufs + 3;
+    static constexpr uint32_t kFin = kPsum + kAttnCtaPages * 16 * 4 * 4; // this CTA's 16 sums, then 16 maxima
+    static constexpr uint32_t kComb = kFin + 2 * 16 * 4;                 // 2 x from the peer (by row parity)
+    static constexpr uint32_t kBars = kComb + 2 * (128 * 8 * 4 + 2 * 16 * 4);
+    // kfull[4] kempty[4] vfull[4] vempty[4] qready[2] qfree[2] sready[12] pvready[3] pvfree[3] pv_done qk_done
+    // comb_ready[2] pv_fin[2]
+    static constexpr uint32_t kNumBars = 2 * kAttnKStages + 2 * kAttnVStages + 4 + kAttnSlots + 2 * kAttnPvBufs + 6;
     static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kPid = kAbort + 4;                         // page ids of the row
-    static constexpr uint32_t kEnd = kPid + 4 * kAttnMaxPages;
+    static constexpr uint32_t kEnd = kAbort + 4;
     static constexpr uint32_t kAlloc = kEnd + 1024;
 };
 static_assert(AttnSmem::kAlloc <= 227 * 1024, "attention shared memory budget");
 static_assert(AttnSmem::kComb % 16 == 0 && AttnSmem::kRed % 16 == 0 && AttnSmem::kPsum % 16 == 0 &&
-                  AttnSmem::kFac % 16 == 0 && AttnSmem::kQ % 1024 == 0 && AttnSmem::kBars % 8 == 0,
+                  AttnSmem::kPmax % 16 == 0 && AttnSmem::kQ % 1024 == 0 && AttnSmem::kBars % 8 == 0,
               "attention shared memory alignment");
 
 // Instruction descriptors.  QK (kind::mxf8f6f4): A = E2M1 (5, bits 7..9),
@@ -277,6 +286,42 @@ __device__ __forceinline__ void attn_widen(const uint8_t *vc, const uint8_t *vsc
     }
 }
 
+// One row's share for this CTA: the clamped context, its pages and the KV
+// head.  Every role reads it for itself (a cached load of context_lens).
+struct AttnItem {
+    int ctx, npages, pbase, kvh;
+};
+
+__device__ __forceinline__ AttnItem attn_item(const AttnParams &p, int64_t item, uint32_t rank)
+{
+    AttnItem it;
+    int ctx = p.context_lens[item];
+    if (ctx > p.width * kPage) ctx = p.width * kPage;
+    if (ctx < 0) ctx = 0;
+    const int all = (ctx + kPage - 1) / kPage;
+    const int half = (all + 1) / 2;
+    it.ctx = ctx;
+    it.pbase = rank == 0 ? 0 : half;
+    it.npages = rank == 0 ? half : all - half;
+    it.kvh = static_cast<int>(item % p.kv_heads);
+    return it;
+}
+
+// Position in a ring of N stages / buffers / slots and the parity of the
+// pass over it, advanced once per page (no division on the page counter).
+template <int N>
+struct PageRing {
+    int idx = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next()
+    {
+        if (++idx == N) {
+            idx = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
 __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThreads, 1)
     mx4_attn_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_ks,
                     const __grid_constant__ AttnParams p)
@@ -286,9 +331,9 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t item = blockIdx.x / kAttnSplit;          // row * kv_heads + kv head
-    const int kvh = static_cast<int>(item % p.kv_heads);
-    const uint32_t rank = cluster_ctarank();               // this CTA's half of the row's pages
+    const uint32_t rank = cluster_ctarank();               // this CTA's half of each row's pages
+    const int64_t item0 = blockIdx.x / kAttnSplit;         // this cluster's first row (row * kv_heads + kv head)
+    const int64_t nclus = gridDim.x / kAttnSplit;          // rows item0, item0 + nclus, ...
 
     auto bar = [&](int i) { return sbase + AttnSmem::kBars + 8u * i; };
     auto kfull = [&](int i) { return bar(i); };
@@ -296,19 +341,23 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     auto vfull = [&](int i) { return bar(2 * kAttnKStages + i); };
     auto vempty = [&](int i) { return bar(2 * kAttnKStages + kAttnVStages + i); };
     constexpr int kB0 = 2 * kAttnKStages + 2 * kAttnVStages;
-    const uint32_t qready = bar(kB0);
-    auto sready = [&](int j) { return bar(kB0 + 1 + j); };          // page j's scores are in TMEM
-    auto pvready = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + i); };
-    auto pvfree = [&](int i) { return bar(kB0 + 1 + kAttnCtaPages + kAttnPvBufs + i); };
-    const uint32_t pv_done = bar(kB0 + 1 + kAttnCtaPages + 2 * kAttnPvBufs);
+    auto qready = [&](int i) { return bar(kB0 + i); };              // Q buffer i staged
+    auto qfree = [&](int i) { return bar(kB0 + 2 + i); };           // Q buffer i no longer read
+    auto sready = [&](int i) { return bar(kB0 + 4 + i); };          // slot i's scores are in TMEM
+    auto pvready = [&](int i) { return bar(kB0 + 4 + kAttnSlots + i); };
+    auto pvfree = [&](int i) { return bar(kB0 + 4 + kAttnSlots + kAttnPvBufs + i); };
+    const uint32_t pv_done = bar(kB0 + 4 + kAttnSlots + 2 * kAttnPvBufs);   // a row's PV products done
     const uint32_t qk_done = pv_done + 8;
-    const uint32_t comb_ready = pv_done + 16;              // the peer has pushed its partial results
+    auto comb_ready = [&](int i) { return pv_done + 16 + 8u * i; }; // the peer's push for a row of parity i
+    auto pv_fin = [&](int i) { return pv_done + 32 + 8u * i; };     // a PV warp's products all done
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(smem + AttnSmem::kAbort);
-    int32_t *pids = reinterpret_cast<int32_t *>(smem + AttnSmem::kPid);
 
     if (threadIdx.x == 0) {
         // arrivals: TMA / commits count 1; the 4 softmax warps arrive on
-        // qready and pvready, the 8 widening warps on vempty and pvready
+        // qready and pvready, the 8 widening warps on vempty and pvready;
+        // pv_done takes two a row: a commit from each PV warp that had pages
+        // in the row, the softmax arriving for one that had none (so that
+        // neither runs a phase ahead of the softmax's wait)
         for (int i = 0; i < kAttnKStages; ++i) {
             mbar_init(kfull(i), 1);
             mbar_init(kempty(i), 1);
@@ -317,17 +366,25 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             mbar_init(vfull(i), 1);
             mbar_init(vempty(i), kAttnWidenWarps);
         }
-        mbar_init(qready, 4);
-        for (int j = 0; j < kAttnCtaPages; ++j) mbar_init(sready(j), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qready(i), 4);
+            mbar_init(qfree(i), 1);
+        }
+        for (int i = 0; i < kAttnSlots; ++i) mbar_init(sready(i), 1);
         for (int i = 0; i < kAttnPvBufs; ++i) {
             mbar_init(pvready(i), 4 + kAttnWidenWarps);
             mbar_init(pvfree(i), 1);
         }
-        mbar_init(pv_done, 2);                  // one commit from each PV warp
+        mbar_init(pv_done, 2);
         mbar_init(qk_done, 1);
-        // completed by the bytes the peer pushes (st.async complete_tx)
-        mbar_init(comb_ready, 1);
-        mbar_arrive_expect_tx(comb_ready, kCombBytes);
+        mbar_init(pv_fin(0), 1);
+        mbar_init(pv_fin(1), 1);
+        // completed by the bytes the peer pushes (st.async complete_tx);
+        // re-armed for the row after next once a push has been read
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(comb_ready(i), 1);
+            mbar_arrive_expect_tx(comb_ready(i), kCombBytes);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -344,69 +401,85 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     // access follows the wait.
     griddep_launch_dependents();
     griddep_wait();
-
-    int ctx = p.context_lens[item];
-    if (ctx > p.width * kPage) ctx = p.width * kPage;
-    if (ctx < 0) ctx = 0;
-    const int npages_all = (ctx + kPage - 1) / kPage;
-    const int half = (npages_all + 1) / 2;
-    const int pbase = rank == 0 ? 0 : half;                // first page of this CTA
-    const int npages = rank == 0 ? half : npages_all - half;   // pages of this CTA
-
-    if (threadIdx.x < kAttnMaxPages) {
-        int32_t id = 0;
-        if (static_cast<int>(threadIdx.x) >= pbase && static_cast<int>(threadIdx.x) < pbase + npages) {
-            const int64_t raw = p.block_table[item * p.width + threadIdx.x];
-            if (raw < 0 || raw >= p.num_pool_pages)
-                atomicOr(&g_mx4_device_status, 0x1u);
-            else
-                id = static_cast<int32_t>(raw);
-        }
-        pids[threadIdx.x] = id;
-    }
     tc_fence_before();
     __syncthreads();
-    // the peer's barriers are initialised before anyone arrives on them remotely
+    // the peer's barriers are initialised before anyone pushes into them
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<uint32_t *>(smem + AttnSmem::kTmemSlot);
 
     if (warp == 4) {
         // ------------------------------------------------------------ copies --
-        // K page j once QK of page j - 4 is done, V page j once the widening
-        // of page j - 4 is done; both from the start so they overlap the QK
-        // products
+        // K page g once QK of page g - 4 is done, V page g once the widening
+        // of page g - 4 is done; they run ahead into the next rows.  Lane j
+        // holds the row's j-th page id, and the next row's context and ids
+        // are loaded while this row's pages stream.
         const uint64_t policy = l2_policy_evict_first();
-        int issued = 0;
-        for (int j = 0; j < npages; ++j) {
-            const int s = j % kAttnKStages, u = j / kAttnKStages;     // kAttnVStages == kAttnKStages
-            if (!__all_sync(0xffffffffu, wait2_bounded(kempty(s), (u & 1) ^ 1u, true, vempty(s), (u & 1) ^ 1u,
-                                                       abort_flag, kSiteAttnProducer)))
-                break;
-            if (elect_one()) {
-                const int64_t pg = pids[pbase + j];
-                mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
-                tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, kvh,
-                            static_cast<int>(pg), policy);
-                tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, kvh,
-                            static_cast<int>(pg), policy);
-                mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
-                bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + kvh * p.vd_hs,
-                          kDataBytes, vfull(s), policy);
-                bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + kvh * p.vs_hs,
-                          kScaleBytes, vfull(s), policy);
+        int64_t g = 0;
+        bool ok = true;
+        auto load_ids = [&](int64_t item, const AttnItem &it) {
+            int32_t id = 0;
+            if (lane < it.npages) {
+                const int64_t raw = p.block_table[item * p.width + it.pbase + lane];
+                if (raw < 0 || raw >= p.num_pool_pages)
+                    atomicOr(&g_mx4_device_status, 0x1u);
+                else
+                    id = static_cast<int32_t>(raw);
             }
-            __syncwarp();
-            ++issued;
+            return id;
+        };
+        AttnItem it = attn_item(p, item0, rank);
+        int32_t id = load_ids(item0, it);
+        PageRing<kAttnKStages> krg;
+        for (int64_t item = item0; item < p.num_items && ok; item += nclus) {
+            AttnItem nit{};
+            int32_t nid = 0;
+            bool fetched = false;
+            auto fetch_next = [&]() {
+                if (!fetched && item + nclus < p.num_items) {
+                    nit = attn_item(p, item + nclus, rank);
+                    nid = load_ids(item + nclus, nit);
+                }
+                fetched = true;
+            };
+            for (int j = 0; j < it.npages; ++j) {
+                const int s = krg.idx;
+                if (!(ok = __all_sync(0xffffffffu, wait2_bounded(kempty(s), krg.ph ^ 1u, true, vempty(s), krg.ph ^ 1u,
+                                                                 abort_flag, kSiteAttnProducer))))
+                    break;
+                const int64_t pg = __shfl_sync(0xffffffffu, id, j);
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(kfull(s), kDataBytes + kScaleBytes);
+                    tma_load_5d(sbase + AttnSmem::kK + s * kTileBytes, &tmap_k, kfull(s), 0, 0, 0, it.kvh,
+                                static_cast<int>(pg), policy);
+                    tma_load_3d(sbase + AttnSmem::kKs + s * kScaleBytes, &tmap_ks, kfull(s), 0, it.kvh,
+                                static_cast<int>(pg), policy);
+                    mbar_arrive_expect_tx(vfull(s), kDataBytes + kScaleBytes);
+                    bulk_load(sbase + AttnSmem::kV + s * kDataBytes, p.v_data + pg * p.vd_ps + it.kvh * p.vd_hs,
+                              kDataBytes, vfull(s), policy);
+                    bulk_load(sbase + AttnSmem::kVs + s * kScaleBytes, p.v_scale + pg * p.vs_ps + it.kvh * p.vs_hs,
+                              kScaleBytes, vfull(s), policy);
+                }
+                __syncwarp();
+                ++g;
+                krg.next();
+                // the next row's context and ids once the first stages are
+                // issued (the warp waits for stages after that anyway)
+                if (j == kAttnKStages - 1) fetch_next();
+            }
+            fetch_next();
+            it = nit;
+            id = nid;
         }
         // no copy may be in flight when the CTA exits: the last use of each
         // stage this warp armed completes (bounded)
         if (lane == 0) {
-            const int n = issued < kAttnKStages ? issued : kAttnKStages;
-            for (int i = 0; i < n; ++i) {
-                const int j = issued - 1 - i;
-                if (!drain_bounded(kfull(j % kAttnKStages), (j / kAttnKStages) & 1)) break;
-                if (!drain_bounded(vfull(j % kAttnKStages), (j / kAttnKStages) & 1)) break;
+            const int64_t n = g < kAttnKStages ? g : kAttnKStages;
+            for (int64_t i = 0; i < n; ++i) {
+                const int64_t gg = g - 1 - i;
+                const uint32_t ph = static_cast<uint32_t>(gg / kAttnKStages) & 1u;
+                if (!drain_bounded(kfull(static_cast<int>(gg % kAttnKStages)), ph)) break;
+                if (!drain_bounded(vfull(static_cast<int>(gg % kAttnKStages)), ph)) break;
             }
         }
         __syncwarp();
@@ -418,52 +491,74 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         // V^T and P^T are written.  Each waits for its own products to
         // complete before the CTA frees TMEM.
         if (lane == 0) {
-            const bool is_qk = warp == 5;
             bool ok = true;
-            if (is_qk) {
-                ok = wait_bounded(qready, 0, abort_flag, kSiteAttnMma);
+            int64_t g = 0;
+            int64_t k = 0;                                 // rows done
+            uint32_t done_b = qk_done;
+            if (warp == 5) {
                 const uint32_t sfb = tmem_base + kAttnSfbCol;
-                const uint64_t qdesc = smem_desc(sbase + AttnSmem::kQ, 16, 1024, 2);
-                if (ok) {
+                PageRing<kAttnKStages> krg;
+                PageRing<kAttnSlots> srg;
+                for (int64_t item = item0; item < p.num_items && ok; item += nclus, ++k) {
+                    const AttnItem it = attn_item(p, item, rank);
+                    const int qb = static_cast<int>(k & 1);
+                    if (!(ok = wait_bounded(qready(qb), static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
+                                            kSiteAttnMma)))
+                        break;
                     tc_fence_after();
-                    tc_cp_32x128b_warpx4(sfb, smem_desc(sbase + AttnSmem::kUnit, 16, 128, 0));
-                }
-                for (int j = 0; j < npages && ok; ++j) {
-                    const int s = j % kAttnKStages;
-                    if (!(ok = wait_bounded(kfull(s), (j / kAttnKStages) & 1, abort_flag, kSiteAttnMma))) break;
-                    tc_fence_after();
-                    const uint32_t sfa = tmem_base + kAttnSfaCol + 4u * j;
-                    tc_cp_32x128b_warpx4(sfa, smem_desc(sbase + AttnSmem::kKs + s * kScaleBytes, 16, 128, 0));
-                    const uint64_t kdesc = smem_desc(sbase + AttnSmem::kK + s * kTileBytes, 16, 1024, 2);
-                    const uint32_t d = tmem_base + kAttnSCol + kAttnN * j;
+                    if (k == 0) tc_cp_32x128b_warpx4(sfb, smem_desc(sbase + AttnSmem::kUnit, 16, 128, 0));
+                    const uint64_t qdesc = smem_desc(sbase + AttnSmem::kQ + qb * 2048u, 16, 1024, 2);
+                    for (int j = 0; j < it.npages; ++j, ++g, krg.next(), srg.next()) {
+                        const int s = krg.idx;
+                        const uint32_t slot = static_cast<uint32_t>(srg.idx);
+                        if (!(ok = wait_bounded(kfull(s), krg.ph, abort_flag, kSiteAttnMma))) break;
+                        tc_fence_after();
+                        const uint32_t sfa = tmem_base + kAttnSfaCol + 4u * slot;
+                        tc_cp_32x128b_warpx4(sfa, smem_desc(sbase + AttnSmem::kKs + s * kScaleBytes, 16, 128, 0));
+                        const uint64_t kdesc = smem_desc(sbase + AttnSmem::kK + s * kTileBytes, 16, 1024, 2);
+                        const uint32_t d = tmem_base + kAttnSCol + kAttnN * slot;
 #pragma unroll
-                    for (uint32_t k = 0; k < 4; ++k)
-                        tc_mma_mx_ss(d, kdesc + 2 * k, qdesc + 2 * k, attn_idesc_qk(k), sfa, sfb, k > 0 ? 1u : 0u);
-                    tc_commit(kempty(s));
-                    tc_commit(sready(j));
+                        for (uint32_t kb = 0; kb < 4; ++kb)
+                            tc_mma_mx_ss(d, kdesc + 2 * kb, qdesc + 2 * kb, attn_idesc_qk(kb), sfa, sfb,
+                                         kb > 0 ? 1u : 0u);
+                        tc_commit(kempty(s));
+                        tc_commit(sready(slot));
+                    }
+                    tc_commit(qfree(qb));
                 }
             } else {
-                // page j waits here only after page j - 2 was ready, hence
-                // page j - 3 (the previous phase of its buffer's barrier) too
-                for (int j = warp == 15 ? 0 : 1; j < npages && ok; j += 2) {
-                    const int b = j % kAttnPvBufs;
-                    if (!(ok = wait_bounded(pvready(b), (j / kAttnPvBufs) & 1, abort_flag, kSiteAttnMma))) break;
-                    tc_fence_after();
-                    const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
-                    const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
-                    const uint32_t d = tmem_base + kAttnAccCol + kAttnN * j;
+                // page g waits here only after page g - 2 was ready, hence
+                // page g - 3 (the previous phase of its buffer's barrier) too
+                const int64_t mine = warp == 15 ? 0 : 1;
+                done_b = pv_fin(static_cast<int>(mine));
+                PageRing<kAttnPvBufs> brg;
+                PageRing<kAttnSlots> srg;
+                for (int64_t item = item0; item < p.num_items && ok; item += nclus, ++k) {
+                    const AttnItem it = attn_item(p, item, rank);
+                    int issued = 0;
+                    for (int j = 0; j < it.npages; ++j, ++g, brg.next(), srg.next()) {
+                        if ((g & 1) != mine) continue;
+                        ++issued;
+                        const int b = brg.idx;
+                        if (!(ok = wait_bounded(pvready(b), brg.ph, abort_flag, kSiteAttnMma))) break;
+                        tc_fence_after();
+                        const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
+                        const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
+                        const uint32_t d = tmem_base + kAttnAccCol + kAttnN * static_cast<uint32_t>(srg.idx);
 #pragma unroll
-                    for (uint32_t ks = 0; ks < 8; ++ks) {
-                        // K step of 16 tokens: two 8-token groups of each operand
-                        const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
-                        const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
-                        tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : 0u);
+                        for (uint32_t ks = 0; ks < 8; ++ks) {
+                            // K step of 16 tokens: two 8-token groups of each operand
+                            const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
+                            const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
+                            tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : 0u);
+                        }
+                        tc_commit(pvfree(b));
                     }
-                    tc_commit(pvfree(b));
+                    if (ok && issued > 0) tc_commit(pv_done);   // this warp's PV products of the row are done
                 }
             }
-            // every product issued above completes before TMEM is read or freed
-            const uint32_t done_b = is_qk ? qk_done : pv_done;
+            // every product issued above completes before TMEM is read or
+            // freed (a barrier of this warp's own, waited for here only)
             tc_commit(done_b);
             const uint64_t t1 = globaltimer_ns();
             while (!mbar_try_wait(done_b, 0) && globaltimer_ns() - t1 < kWaitLimitNs) {
@@ -473,20 +568,27 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     } else if (warp >= 6) {
         // ---------------------------------------------------------- V widening --
         // warps 6-9 and 11-14 (warps 10 and 15 are PV issuers)
-        for (int j = 0; j < npages; ++j) {
-            const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
-            const int vs = j % kAttnVStages;
-            if (!__all_sync(0xffffffffu, wait2_bounded(vfull(vs), (j / kAttnVStages) & 1, u > 0, pvfree(b),
-                                                       (u - 1) & 1, abort_flag, kSiteAttnEpi)))
-                break;
-            attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
-                       smem + AttnSmem::kVt + b * 32768, warp < 10 ? warp - 6 : warp - 7, lane,
-                       ctx - (pbase + j) * kPage);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(pvready(b));
-                mbar_arrive(vempty(vs));
+        int64_t g = 0;
+        bool ok = true;
+        PageRing<kAttnPvBufs> brg;
+        PageRing<kAttnVStages> krg;
+        for (int64_t item = item0; item < p.num_items && ok; item += nclus) {
+            const AttnItem it = attn_item(p, item, rank);
+            for (int j = 0; j < it.npages; ++j, ++g, brg.next(), krg.next()) {
+                const int b = brg.idx, vs = krg.idx;
+                // (a buffer's first use waits for no PV product)
+                if (!(ok = __all_sync(0xffffffffu, wait2_bounded(vfull(vs), krg.ph, g >= kAttnPvBufs, pvfree(b),
+                                                                 brg.ph ^ 1u, abort_flag, kSiteAttnEpi))))
+                    break;
+                attn_widen(smem + AttnSmem::kV + vs * kDataBytes, smem + AttnSmem::kVs + vs * kScaleBytes,
+                           smem + AttnSmem::kVt + b * 32768, warp < 10 ? warp - 6 : warp - 7, lane,
+                           it.ctx - (it.pbase + j) * kPage);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(pvready(b));
+                    mbar_arrive(vempty(vs));
+                }
             }
         }
     } else {
@@ -497,158 +599,199 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         const int G = p.groups;
         float *red = reinterpret_cast<float *>(smem + AttnSmem::kRed);
         float *pmax = reinterpret_cast<float *>(smem + AttnSmem::kPmax);
-        float *fac = reinterpret_cast<float *>(smem + AttnSmem::kFac);
-        float *fin = reinterpret_cast<float *>(smem + AttnSmem::kFin);
         float *psum = reinterpret_cast<float *>(smem + AttnSmem::kPsum);
-        {
-            // Q tile (16 rows x 128 B, SW128) and the unit scale block
+        float *fin = reinterpret_cast<float *>(smem + AttnSmem::kFin);
+        // Q of a row (16 rows x 128 B, SW128) into buffer qb, then qready
+        auto stage_q = [&](int64_t item, int qb) {
             const int h = m >> 3, c = m & 7;
             uint4 v = make_uint4(0, 0, 0, 0);
             if (h < G) v = *reinterpret_cast<const uint4 *>(p.q + ((item * G + h) << 7) + c * 16);
-            *reinterpret_cast<uint4 *>(smem + AttnSmem::kQ + (h >> 3) * 1024 + (h & 7) * 128 + ((c ^ (h & 7)) << 4)) = v;
-            reinterpret_cast<uint32_t *>(smem + AttnSmem::kUnit)[m] = 0x7F7F7F7Fu;
+            *reinterpret_cast<uint4 *>(smem + AttnSmem::kQ + qb * 2048 + (h >> 3) * 1024 + (h & 7) * 128 +
+                                       ((c ^ (h & 7)) << 4)) = v;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(qready);
-        }
+            if (lane == 0) mbar_arrive(qready(qb));
+        };
+        reinterpret_cast<uint32_t *>(smem + AttnSmem::kUnit)[m] = 0x7F7F7F7Fu;   // before the first qready
+        stage_q(item0, 0);
         // scores in log2 units: x = s * softmax_scale * log2(e)
         const float sl = p.softmax_scale * 1.4426950408889634f;
         const int hl = lane & 15;
         bool ok = true;
+        int64_t g = 0;
+        int64_t k = 0;                                   // rows done
+        PageRing<kAttnPvBufs> brg;
+        PageRing<kAttnSlots> srg;
         // (the named-barrier syncs below run on every path, so the four
         // warps always pass the same number of them)
-        for (int j = 0; j < npages; ++j) {
-            const int b = j % kAttnPvBufs, u = j / kAttnPvBufs;
-            const bool okw = __all_sync(
-                0xffffffffu, wait2_bounded(sready(j), 0, u > 0, pvfree(b), (u - 1) & 1, abort_flag, kSiteAttnEpi));
-            const bool valid = (pbase + j) * kPage + tok_m < ctx;
-            float x[16];
-            if (okw) {
-                tc_fence_after();
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * j, v);
-                float wm = 0.0f;
+        for (int64_t item = item0; item < p.num_items; item += nclus, ++k) {
+            const AttnItem it = attn_item(p, item, rank);
+            // the next row's Q, one row ahead, once QK is done with the buffer
+            if (item + nclus < p.num_items) {
+                const int64_t kn = k + 1;
+                if (kn < 2 || __all_sync(0xffffffffu, wait_bounded(qfree(static_cast<int>(kn & 1)),
+                                                                   static_cast<uint32_t>((kn >> 1) - 1) & 1u,
+                                                                   abort_flag, kSiteAttnEpi)))
+                    stage_q(item + nclus, static_cast<int>(kn & 1));
+            }
+            const int64_t g0 = g;
+            const int slot0 = srg.idx;
+            for (int j = 0; j < it.npages && ok; ++j, ++g, brg.next(), srg.next()) {
+                const int b = brg.idx;
+                const uint32_t slot = static_cast<uint32_t>(srg.idx);
+                const bool okw = __all_sync(0xffffffffu, wait2_bounded(sready(srg.idx), srg.ph, g >= kAttnPvBufs,
+                                                                       pvfree(b), brg.ph ^ 1u, abort_flag, kSiteAttnEpi));
+                const bool valid = (it.pbase + j) * kPage + tok_m < it.ctx;
+                float x[16];
+                if (okw) {
+                    tc_fence_after();
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * slot, v);
+                    float wm = 0.0f;
 #pragma unroll
-                for (int h = 0; h < kAttnN; ++h) {
-                    x[h] = valid ? __uint_as_float(v[h]) * sl : -INFINITY;
-                    const float r = warp_max(x[h]);
-                    wm = hl == h ? r : wm;
+                    for (int h = 0; h < kAttnN; ++h) {
+                        x[h] = valid ? __uint_as_float(v[h]) * sl : -INFINITY;
+                        const float r = warp_max(x[h]);
+                        wm = hl == h ? r : wm;
+                    }
+                    if (lane < kAttnN) red[((j & 1) * 16 + lane) * 4 + warp] = wm;
                 }
-                if (lane < kAttnN) red[((j & 1) * 16 + lane) * 4 + warp] = wm;
+                ok = epi_bar_and(okw);
+                if (!ok) break;
+                // the page's max of head hl over the four warps, then every head's
+                const float4 r4 = reinterpret_cast<const float4 *>(red)[(j & 1) * 16 + hl];
+                const float mh = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+                if (warp == 0 && lane < kAttnN) pmax[j * 16 + lane] = mh;
+                uint32_t w[8];
+                float ps[16];
+#pragma unroll
+                for (int h2 = 0; h2 < 8; ++h2) {
+                    const float m0 = __shfl_sync(0xffffffffu, mh, 2 * h2);
+                    const float m1 = __shfl_sync(0xffffffffu, mh, 2 * h2 + 1);
+                    const float p0 = valid && 2 * h2 < G ? ex2_approx(x[2 * h2] - m0) : 0.0f;
+                    const float p1 = valid && 2 * h2 + 1 < G ? ex2_approx(x[2 * h2 + 1] - m1) : 0.0f;
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    ps[2 * h2] = __low2float(pb);
+                    ps[2 * h2 + 1] = __high2float(pb);
+                    w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
+                }
+                uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(tok_m);
+                *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                // P^T visible to the tensor core
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(pvready(b));
+                // this warp's per-head sums of the bf16 weights (lanes 2 h, 2 h + 1
+                // hold head h)
+                const float wsum = warp_sum16(ps, lane);
+                if ((lane & 1) == 0) psum[(j * 16 + (lane >> 1)) * 4 + warp] = wsum;
             }
-            ok = epi_bar_and(okw);
-            if (!ok) break;
-            // the page's max of head hl over the four warps, then every head's
-            const float4 r4 = reinterpret_cast<const float4 *>(red)[(j & 1) * 16 + hl];
-            const float mh = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
-            if (warp == 0 && lane < kAttnN) pmax[j * 16 + lane] = mh;
-            uint32_t w[8];
-            float ps[16];
-#pragma unroll
-            for (int h2 = 0; h2 < 8; ++h2) {
-                const float m0 = __shfl_sync(0xffffffffu, mh, 2 * h2);
-                const float m1 = __shfl_sync(0xffffffffu, mh, 2 * h2 + 1);
-                const float p0 = valid && 2 * h2 < G ? ex2_approx(x[2 * h2] - m0) : 0.0f;
-                const float p1 = valid && 2 * h2 + 1 < G ? ex2_approx(x[2 * h2 + 1] - m1) : 0.0f;
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                ps[2 * h2] = __low2float(pb);
-                ps[2 * h2 + 1] = __high2float(pb);
-                w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
+            epi_bar_sync();
+            // per head (threads 0-15): M = max_j m_j, the page factors
+            // 2^(m_j - M) (in place of the maxima) and the CTA's weight sum
+            const int nj = ok ? it.npages : 0;
+            if (m < kAttnN) {
+                float M = -INFINITY, S = 0.0f;
+                for (int j = 0; j < nj; ++j) M = fmaxf(M, pmax[j * 16 + m]);
+                for (int j = 0; j < nj; ++j) {
+                    const float f = ex2_approx(pmax[j * 16 + m] - M);
+                    const float4 s4 = reinterpret_cast<const float4 *>(psum)[j * 16 + m];
+                    pmax[j * 16 + m] = f;
+                    S += f * ((s4.x + s4.y) + (s4.z + s4.w));
+                }
+                fin[m] = S;
+                fin[kAttnN + m] = M;
             }
-            uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(tok_m);
-            *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
-            // P^T visible to the tensor core
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pvready(b));
-            // this warp's per-head sums of the bf16 weights (lanes 2 h, 2 h + 1
-            // hold head h)
-            const float wsum = warp_sum16(ps, lane);
-            if ((lane & 1) == 0) psum[(j * 16 + (lane >> 1)) * 4 + warp] = wsum;
-        }
-        epi_bar_sync();
-        // per head (threads 0-15): M = max_j m_j, the page factors
-        // 2^(m_j - M) and the CTA's weight sum
-        const int nj = ok ? npages : 0;
-        if (m < kAttnN) {
-            float M = -INFINITY, S = 0.0f;
-            for (int j = 0; j < nj; ++j) M = fmaxf(M, pmax[j * 16 + m]);
-            for (int j = 0; j < nj; ++j) {
-                const float f = ex2_approx(pmax[j * 16 + m] - M);
-                const float4 s4 = reinterpret_cast<const float4 *>(psum)[j * 16 + m];
-                fac[j * 16 + m] = f;
-                S += f * ((s4.x + s4.y) + (s4.z + s4.w));
+            // this row's PV products: a PV warp without pages in the row
+            // does not commit, the softmax arrives in its place (every row's
+            // phase is waited for, so the parities stay in step)
+            if (m == 0) {
+                const int n = it.npages;
+                const int has_even = n >= 2 || (n == 1 && (g0 & 1) == 0);
+                const int has_odd = n >= 2 || (n == 1 && (g0 & 1) == 1);
+                for (int i = has_even + has_odd; i < 2; ++i) mbar_arrive(pv_done);
             }
-            fin[m] = S;
-            fin[kAttnN + m] = M;
-        }
-        if (ok && npages > 0)
-            ok = __all_sync(0xffffffffu, wait_bounded(pv_done, 0, abort_flag, kSiteAttnEpi));
-        epi_bar_sync();
-        // lane m of the accumulators holds head dim m of every head
-        float acc[kAttnN];
+            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(pv_done, static_cast<uint32_t>(k) & 1u, abort_flag,
+                                                              kSiteAttnEpi));
+            epi_bar_sync();
+            // lane m of the accumulators holds head dim m of every head
+            float acc[kAttnN];
 #pragma unroll
-        for (int h = 0; h < kAttnN; ++h) acc[h] = 0.0f;
-        if (ok && npages > 0) {
-            tc_fence_after();
-            for (int j0 = 0; j0 < npages; j0 += 4) {
-                uint32_t v[64];
-                tmem_ld_32x32b_x64(tmem_base + lane_addr + kAttnAccCol + kAttnN * j0, v);
+            for (int h = 0; h < kAttnN; ++h) acc[h] = 0.0f;
+            if (ok && it.npages > 0) {
+                tc_fence_after();
+                for (int j0 = 0; j0 < it.npages; j0 += 2) {
+                    uint32_t v[2][16];
+                    int s0 = slot0 + j0, s1 = s0 + 1;
+                    s0 -= s0 >= kAttnSlots ? kAttnSlots : 0;
+                    s0 -= s0 >= kAttnSlots ? kAttnSlots : 0;
+                    s1 -= s1 >= kAttnSlots ? kAttnSlots : 0;
+                    s1 -= s1 >= kAttnSlots ? kAttnSlots : 0;
+                    tmem_ld2_32x32b_x16(tmem_base + lane_addr + kAttnAccCol + kAttnN * static_cast<uint32_t>(s0),
+                                        tmem_base + lane_addr + kAttnAccCol + kAttnN * static_cast<uint32_t>(s1), v[0],
+                                        v[1]);
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    if (j0 + jj < npages) {
-                        const float4 *f4 = reinterpret_cast<const float4 *>(fac) + (j0 + jj) * 4;
+                    for (int jj = 0; jj < 2; ++jj) {
+                        if (j0 + jj < it.npages) {
+                            const float4 *f4 = reinterpret_cast<const float4 *>(pmax) + (j0 + jj) * 4;
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const float4 f = f4[q4];
-                            acc[4 * q4 + 0] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 0]), f.x, acc[4 * q4 + 0]);
-                            acc[4 * q4 + 1] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 1]), f.y, acc[4 * q4 + 1]);
-                            acc[4 * q4 + 2] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 2]), f.z, acc[4 * q4 + 2]);
-                            acc[4 * q4 + 3] = fmaf(__uint_as_float(v[16 * jj + 4 * q4 + 3]), f.w, acc[4 * q4 + 3]);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float4 f = f4[q4];
+                                acc[4 * q4 + 0] = fmaf(__uint_as_float(v[jj][4 * q4 + 0]), f.x, acc[4 * q4 + 0]);
+                                acc[4 * q4 + 1] = fmaf(__uint_as_float(v[jj][4 * q4 + 1]), f.y, acc[4 * q4 + 1]);
+                                acc[4 * q4 + 2] = fmaf(__uint_as_float(v[jj][4 * q4 + 2]), f.z, acc[4 * q4 + 2]);
+                                acc[4 * q4 + 3] = fmaf(__uint_as_float(v[jj][4 * q4 + 3]), f.w, acc[4 * q4 + 3]);
+                            }
                         }
                     }
                 }
             }
-        }
-        // Combine the two halves: rank r finalises heads 8r .. 8r+7.  Each
-        // CTA pushes the peer's heads of its accumulator ([dim][8 heads]) and
-        // its 16 sums and maxima into the peer's shared memory with st.async,
-        // whose bytes complete the peer's comb_ready; it then waits for its
-        // own comb_ready, rescales both halves to the row's max, adds,
-        // normalises and stores bf16 (a half with no weight contributes
-        // nothing).
-        {
-            const uint32_t peer = rank ^ 1u;
-            const uint32_t pc = cluster_map(sbase + AttnSmem::kComb, peer);
-            const uint32_t pbar = cluster_map(comb_ready, peer);
-            float a8[8];
+            // Combine the two halves: rank r finalises heads 8r .. 8r+7.
+            // Each CTA pushes the peer's heads of its accumulator ([dim][8
+            // heads]) and its 16 sums and maxima into the peer's buffer of
+            // this row's parity with st.async, whose bytes complete the
+            // peer's comb_ready; it then waits for its own, rescales both
+            // halves to the row's max, adds, normalises and stores bf16 (a
+            // half with no weight contributes nothing).
+            {
+                const int cb = static_cast<int>(k & 1);
+                const uint32_t peer = rank ^ 1u;
+                const uint32_t pc = cluster_map(sbase + AttnSmem::kComb + cb * kCombBytes, peer);
+                const uint32_t pbar = cluster_map(comb_ready(cb), peer);
+                float a8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a8[i] = peer ? acc[8 + i] : acc[i];
-            st_async_v4_u32(pc + 32u * m, __float_as_uint(a8[0]), __float_as_uint(a8[1]), __float_as_uint(a8[2]),
-                            __float_as_uint(a8[3]), pbar);
-            st_async_v4_u32(pc + 32u * m + 16u, __float_as_uint(a8[4]), __float_as_uint(a8[5]),
-                            __float_as_uint(a8[6]), __float_as_uint(a8[7]), pbar);
-            if (m < 2 * kAttnN) st_async_u32(pc + 4096u + 4u * m, __float_as_uint(fin[m]), pbar);
-            if (__all_sync(0xffffffffu, wait_bounded(comb_ready, 0, abort_flag, kSiteAttnEpi))) {
-                const float *cm = reinterpret_cast<const float *>(smem + AttnSmem::kComb);
-                const float4 c0 = reinterpret_cast<const float4 *>(cm)[2 * m];
-                const float4 c1 = reinterpret_cast<const float4 *>(cm)[2 * m + 1];
-                const float a1[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                __nv_bfloat16 *o = p.out + (item * G) * kDim;
+                for (int i = 0; i < 8; ++i) a8[i] = peer ? acc[8 + i] : acc[i];
+                st_async_v4_u32(pc + 32u * m, __float_as_uint(a8[0]), __float_as_uint(a8[1]),
+                                __float_as_uint(a8[2]), __float_as_uint(a8[3]), pbar);
+                st_async_v4_u32(pc + 32u * m + 16u, __float_as_uint(a8[4]), __float_as_uint(a8[5]),
+                                __float_as_uint(a8[6]), __float_as_uint(a8[7]), pbar);
+                if (m < 2 * kAttnN) st_async_u32(pc + 4096u + 4u * m, __float_as_uint(fin[m]), pbar);
+                if (__all_sync(0xffffffffu, wait_bounded(comb_ready(cb), static_cast<uint32_t>(k >> 1) & 1u,
+                                                         abort_flag, kSiteAttnEpi))) {
+                    const float *cm = reinterpret_cast<const float *>(smem + AttnSmem::kComb + cb * kCombBytes);
+                    const float4 c0 = reinterpret_cast<const float4 *>(cm)[2 * m];
+                    const float4 c1 = reinterpret_cast<const float4 *>(cm)[2 * m + 1];
+                    const float a1[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    __nv_bfloat16 *o = p.out + (item * G) * kDim;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int h = 8 * static_cast<int>(rank) + i;
-                    // this thread's own values of head h (static register indexes)
-                    const float a0 = rank ? acc[8 + i] : acc[i];
-                    const float s0 = fin[h], m0 = fin[kAttnN + h];
-                    const float s1 = cm[1024 + h], m1 = cm[1024 + kAttnN + h];
-                    const float mx = s1 > 0.0f && m1 > m0 ? m1 : m0;
-                    const float f0 = s0 > 0.0f ? ex2_approx(m0 - mx) : 0.0f;
-                    const float f1 = s1 > 0.0f ? ex2_approx(m1 - mx) : 0.0f;
-                    const float a = a0 * f0 + a1[i] * f1, sum = s0 * f0 + s1 * f1;
-                    if (h < G) o[h * kDim + m] = __float2bfloat16_rn(sum > 0.0f ? __fdividef(a, sum) : 0.0f);
+                    for (int i = 0; i < 8; ++i) {
+                        const int h = 8 * static_cast<int>(rank) + i;
+                        // this thread's own values of head h (static register indexes)
+                        const float a0 = rank ? acc[8 + i] : acc[i];
+                        const float s0 = fin[h], m0 = fin[kAttnN + h];
+                        const float s1 = cm[1024 + h], m1 = cm[1024 + kAttnN + h];
+                        const float mx = s1 > 0.0f && m1 > m0 ? m1 : m0;
+                        const float f0 = s0 > 0.0f ? ex2_approx(m0 - mx) : 0.0f;
+                        const float f1 = s1 > 0.0f ? ex2_approx(m1 - mx) : 0.0f;
+                        const float a = a0 * f0 + a1[i] * f1, sum = s0 * f0 + s1 * f1;
+                        if (h < G) o[h * kDim + m] = __float2bfloat16_rn(sum > 0.0f ? __fdividef(a, sum) : 0.0f);
+                    }
                 }
+                // every thread has read this buffer, fin and the factors: the
+                // buffer's barrier is re-armed for the row after next
+                epi_bar_sync();
+                if (m == 0) mbar_arrive_expect_tx(comb_ready(cb), kCombBytes);
             }
         }
     }

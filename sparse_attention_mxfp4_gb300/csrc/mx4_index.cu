@@ -46,6 +46,7 @@ struct DeviceState {
     int sm_count = 0;
     bool topk_attr_set[2] = {false, false};
     bool attn_attr_set = false;
+    int attn_clusters = 0;          // attention clusters resident at once on the device
     bool smem_attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 
@@ -601,7 +602,7 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     if (!q || !k_data || !k_scale || !v_data || !v_scale || !block_table || !context_lens || !out)
         return MX4_ERR_INVALID_ARG;
     if (num_pool_pages < 1) return MX4_ERR_INVALID_ARG;
-    // the grid is rows x KV heads x kAttnSplit CTAs, within grid.x's limit of 2^31 - 1
+    // rows x KV heads items, kept within the range the per-item indexing was checked for
     if (num_pool_pages > INT32_MAX || num_rows > INT32_MAX / (static_cast<int64_t>(kv_heads) * mx4::kAttnSplit))
         return MX4_ERR_UNSUPPORTED;
     // views: a page of one head holds 8192 code bytes and 512 scale bytes
@@ -622,6 +623,7 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
         return MX4_ERR_MISALIGNED;
 
     int dev = 0;
+    int max_clusters = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX4_ERR_CUDA;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -630,8 +632,18 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
             if (cudaFuncSetAttribute(mx4::mx4_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(mx4::AttnSmem::kAlloc)) != cudaSuccess)
                 return MX4_ERR_CUDA;
+            // how many 2-CTA clusters of this kernel fit on the device at once
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(mx4::kAttnSplit, 1, 1);
+            cfg.blockDim = dim3(mx4::kAttnThreads, 1, 1);
+            cfg.dynamicSmemBytes = mx4::AttnSmem::kAlloc;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, mx4::mx4_attn_kernel, &cfg) != cudaSuccess || n < 1)
+                return MX4_ERR_CUDA;
+            st.attn_clusters = n;
             st.attn_attr_set = true;
         }
+        max_clusters = st.attn_clusters;
     }
     alignas(64) CUtensorMap tmap_k;
     alignas(64) CUtensorMap tmap_ks;
@@ -660,10 +672,13 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     p.groups = groups;
     p.width = block_table_width;
     p.softmax_scale = softmax_scale;
-    // one cluster of kAttnSplit CTAs per (row, KV head)
+    p.num_items = num_rows * kv_heads;
+    // clusters of kAttnSplit CTAs, at most as many as are resident at once;
+    // cluster c takes the (row, KV head) items c, c + clusters, ...
+    const int64_t clusters = p.num_items < max_clusters ? p.num_items : max_clusters;
     cudaGetLastError();
     // (the cluster shape comes from the kernel's own attribute)
-    if (launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(num_rows * kv_heads * mx4::kAttnSplit),
+    if (launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(clusters * mx4::kAttnSplit),
                   mx4::kAttnThreads, mx4::AttnSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k,
                   tmap_ks, p) != cudaSuccess)
         return MX4_ERR_CUDA;

@@ -242,9 +242,17 @@ __device__ __forceinline__ bool stall_in_cta()
 {
     return g_mx4_stall_site >= 0 && static_cast<int>(blockIdx.x) == g_mx4_stall_cta;
 }
+// The waits that depend on a stalled one run out too, some of them having
+// started earlier; they get four times the limit, so that the stalled site is
+// the one the status word names.
+__device__ __forceinline__ uint64_t wait_limit_ns(uint32_t site)
+{
+    return stall_in_cta() && !stalled_here(site) ? 4 * kWaitLimitNs : kWaitLimitNs;
+}
 #else
 __device__ __forceinline__ constexpr bool stalled_here(uint32_t) { return false; }
 __device__ __forceinline__ constexpr bool stall_in_cta() { return false; }
+__device__ __forceinline__ constexpr uint64_t wait_limit_ns(uint32_t) { return kWaitLimitNs; }
 #endif
 
 // Bounded wait: true when the phase completed; false after the time limit or
@@ -254,12 +262,13 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
                                              uint32_t site)
 {
     const bool stall = stalled_here(site);
+    const uint64_t limit = wait_limit_ns(site);
     if (!stall && mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (!stall && mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit) {
             atomicOr(&g_mx4_device_status, 0x2u | (0x100u << site));
             *abort_flag = 1;
             return false;
