@@ -103,3 +103,46 @@ def test_attn_empty_rows_are_zero():
 def test_attn_full_size_config(name):
     c = W.make_attn_config(name)
     print("rel_l2", _check(c))
+
+
+def _abs_weighted_v_rows(c):
+    """E_p|v| as _abs_weighted_v, dequantizing only each row's listed pages
+    (for cases whose pool is too large to dequantize whole)."""
+    q = e4m3_values_numpy(c.q.numpy())
+    out = np.zeros(q.shape)
+    for r in range(c.rows):
+        for h in range(c.kv_heads):
+            n = int(c.context_lens[r, h])
+            if n <= 0:
+                continue
+            ids = torch.tensor([int(x) for x in c.block_table[r, h, : (n + 127) // 128]], dtype=torch.long)
+            k = _dequant_pool(c.k_pool[ids][:, h:h + 1])[:, 0].reshape(-1, 128)[:n]
+            v = _dequant_pool(c.v_pool[ids][:, h:h + 1])[:, 0].reshape(-1, 128)[:n]
+            s = c.softmax_scale * (q[r, h] @ k.T)
+            w = np.exp(s - s.max(axis=1, keepdims=True))
+            out[r, h] = (w / w.sum(axis=1, keepdims=True)) @ np.abs(v)
+    return out
+
+
+def test_attn_persistent_rows_of_every_length():
+    """More rows than clusters, so every cluster streams several rows back to
+    back with its stage, buffer and TMEM-slot rings carried across them; the
+    lengths cycle through 0, 1, 127, 128, 129, 255, 256, 1536, 3071 and 3072
+    tokens (rows with no page, with one page for one PV warp only, and with
+    12 pages a CTA, which wraps the 12-slot ring every row) between seeded
+    random ones."""
+    rows, width = 400, 24
+    special = [0, 1, 127, 128, 129, 255, 256, 1536, 3071, 3072]
+    g = torch.Generator().manual_seed(131)
+    rand = torch.randint(0, width * 128 + 1, (rows,), generator=g).tolist()
+    ctx = [special[r // 2 % len(special)] if r % 2 == 0 else rand[r] for r in range(rows)]
+    c = W.make_attn_case("persist", seed=132, rows=rows, kv_heads=1, groups=16, width=width,
+                         pool_pages=rows * width, ctx=ctx)
+    got = _gpu(c)
+    ref = oracle_attn(c)
+    lim = 2.0 ** -8 * (_abs_weighted_v_rows(c) + np.abs(ref)) + 2.0 ** -8 * np.abs(ref) + 1e-30
+    err = np.abs(got - ref)
+    assert not (err > lim).any(), f"{int((err > lim).sum())} of {err.size} outside; worst err {err.max():.3e}"
+    empty = np.array(ctx) == 0
+    assert (got[empty] == 0).all()
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 4e-3
