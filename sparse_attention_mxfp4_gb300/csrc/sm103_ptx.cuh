@@ -248,7 +248,9 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         : "memory");
 }
 
-// 64-column forms of the two loads above (half the destination registers).
+// Load 64 consecutive 32-bit TMEM columns of this warp's 32 lanes, each
+// thread also getting the maximum of its lane's 64 values (tcgen05.ld.red),
+// and wait.
 __device__ __forceinline__ float tmem_ld_max_32x32b_x64(uint32_t taddr, uint32_t (&v)[64])
 {
     float mx;
