@@ -14,10 +14,14 @@
 //               the selected pages, the context the attention step reads.
 //
 // One CTA per (row, group) work item, grid-stride; or, when there are fewer
-// items than two per SM, one cluster of kTopkSplit CTAs per item: each CTA
-// of the cluster computes the keys of a quarter of the pages and stores them
-// into the shared memory of the cluster's rank 0, which alone selects (a
-// row's score reads are then spread over four SMs).  The values become
+// items than two per SM, one cluster of kTopkSplit CTAs per item, each CTA
+// computing the keys of a quarter of the pages (a row's score reads are then
+// spread over four SMs).  With at most kTopkFastWant = 32 chosen pages of at
+// most 4 x 256 candidates the select has two stages: each CTA sorts its
+// (key, page) ranks one a thread in warp bitonic sorts and keeps the 32
+// largest through a merge tree; rank 0 merges the four lists and takes the
+// first `want`.  Otherwise the CTAs store their keys into rank 0's
+// shared memory and rank 0 alone selects, as one CTA does.  The values become
 // order-preserving 32-bit keys in shared memory; an exact MSB-first radix
 // select (4 passes of 8 bits, shared-memory histograms fed by warp-aggregated
 // atomics) finds the m-th largest key T and how many keys equal to T are
@@ -37,6 +41,7 @@ namespace mx4 {
 constexpr int kTopkThreads = 256;
 constexpr int kTopkSplit = 4;          // CTAs (one cluster) per item when items are few
 constexpr int kTopkMaxPages = 16384;   // ceil(max_seq_len / 128) supported (2M tokens)
+constexpr int kTopkFastWant = 32;      // cluster path: two-stage select up to this many chosen pages
 
 struct TopkParams {
     const float *scores;           // [rows, 64, P]
@@ -66,6 +71,46 @@ __device__ __forceinline__ uint32_t topk_key(float v)
     if (v == 0.0f) v = 0.0f;
     const uint32_t u = __float_as_uint(v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Ranks of the two-stage select: (key << 32) | (2^32 - 1 - page), so the
+// larger rank comes first in the selection order (key descending, ties to the
+// lower page); 0 marks an empty slot, below every page's rank.
+__device__ __forceinline__ uint64_t topk_rank(uint32_t key, int page)
+{
+    return (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(page));
+}
+
+// Bitonic sort of one value a lane, descending over the warp's lanes.
+__device__ __forceinline__ uint64_t topk_warp_sort_desc(uint64_t x)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const uint64_t y = __shfl_xor_sync(0xffffffffu, x, j);
+            // the lower lane of a pair keeps the larger value in runs that
+            // end descending ((lane & k) == 0; every lane in the last run)
+            const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0 || k == 32);
+            x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+        }
+    }
+    return x;
+}
+
+// The 32 largest of two descending warp lists a and b (lane i gives a[i] and
+// b[31 - i], a bitonic run), descending.
+__device__ __forceinline__ uint64_t topk_warp_merge_desc(uint64_t a, uint64_t b_rev)
+{
+    const int lane = threadIdx.x & 31;
+    uint64_t x = a > b_rev ? a : b_rev;
+#pragma unroll
+    for (int j = 16; j > 0; j >>= 1) {
+        const uint64_t y = __shfl_xor_sync(0xffffffffu, x, j);
+        x = (lane & j) == 0 ? (x > y ? x : y) : (x < y ? x : y);
+    }
+    return x;
 }
 
 // Block-wide exclusive scan of one int per thread (256 threads); also
@@ -106,6 +151,10 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
     __shared__ uint32_t sel_prefix;
     __shared__ int sel_remaining;
     __shared__ int sel_done;
+    // cluster path, two-stage select: the warps' sorted lists (two buffers,
+    // one per merge level), and in rank 0 every rank's 32 largest
+    __shared__ uint64_t run[2][kTopkThreads];
+    __shared__ uint64_t cand[kTopkSplit * 32];
 
     const int tid = threadIdx.x;
     const int hg = 64 / p.groups;
@@ -151,6 +200,10 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
             const int h0 = sl * hper < hg ? sl * hper : hg;
             const int h1 = h0 + hper < hg ? h0 + hper : hg;
             const uint32_t keys0 = cluster_map(static_cast<uint32_t>(__cvta_generic_to_shared(keys)), 0);
+            // few chosen pages of at most 4 x 256 candidates: the two-stage
+            // select below, else rank 0 selects over all the keys
+            const bool fast = want > 0 && want < nc && want <= kTopkFastWant && nc <= kTopkSplit * kTopkThreads;
+            int pj0 = 0, pj1 = 0;                        // this rank's candidate pages
             // Rank 0's shared memory may be written only once every CTA of the
             // cluster is known to have started: arrive here, wait just before
             // the remote stores, so the barrier overlaps the score reads.
@@ -180,11 +233,15 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                     atomicMax(&keys[4 * qd + 3], topk_key(m.w));
                 }
                 __syncthreads();
-                cluster_wait();
-                if (rank != 0)
-                    for (int qd = q0 + tid; qd < q1; qd += kTopkThreads)
-                        st_cluster_v4_u32(keys0 + 16u * qd, keys[4 * qd], keys[4 * qd + 1], keys[4 * qd + 2],
-                                          keys[4 * qd + 3]);
+                pj0 = 4 * q0;
+                pj1 = 4 * q1 < nc ? 4 * q1 : nc;
+                if (!fast) {
+                    cluster_wait();
+                    if (rank != 0)
+                        for (int qd = q0 + tid; qd < q1; qd += kTopkThreads)
+                            st_cluster_v4_u32(keys0 + 16u * qd, keys[4 * qd], keys[4 * qd + 1], keys[4 * qd + 2],
+                                              keys[4 * qd + 3]);
+                }
             } else {
                 const int share = (nc + kSplit - 1) / kSplit;
                 const int j0 = static_cast<int>(rank) * share < nc ? static_cast<int>(rank) * share : nc;
@@ -198,14 +255,83 @@ __global__ void __launch_bounds__(kTopkThreads, 4) mx4_topk_kernel(const __grid_
                     atomicMax(&keys[j], topk_key(m));
                 }
                 __syncthreads();
-                cluster_wait();
-                if (rank != 0)
-                    for (int j = j0 + tid; j < j1; j += kTopkThreads) st_cluster_u32(keys0 + 4u * j, keys[j]);
+                pj0 = j0;
+                pj1 = j1;
+                if (!fast) {
+                    cluster_wait();
+                    if (rank != 0)
+                        for (int j = j0 + tid; j < j1; j += kTopkThreads) st_cluster_u32(keys0 + 4u * j, keys[j]);
+                }
             }
-            // every rank's keys have landed in rank 0 (release / acquire);
-            // the other ranks are done with the item
+            if (fast) {
+                // Two-stage select, first stage: this rank's 32 largest
+                // candidate ranks, from one a thread over its pages [pj0, pj1):
+                // each warp sorts its 32, three merge levels keep the 32
+                // largest of all.  Every page of the row's top want (want <=
+                // 32) is among its CTA's 32 largest.
+                const int lane = tid & 31, warp = tid >> 5;
+                const int jt = pj0 + tid;
+                uint64_t x = topk_warp_sort_desc(jt < pj1 ? topk_rank(keys[jt], jt) : 0ull);
+                run[0][tid] = x;
+                __syncthreads();
+#pragma unroll
+                for (int lv = 0, n = kTopkThreads / 64; n >= 1; ++lv, n >>= 1) {
+                    if (warp < n) {
+                        x = topk_warp_merge_desc(run[lv & 1][64 * warp + lane], run[lv & 1][64 * warp + 63 - lane]);
+                        if (n > 1) run[(lv + 1) & 1][32 * warp + lane] = x;
+                    }
+                    if (n > 1) __syncthreads();
+                }
+                cluster_wait();
+                if (warp == 0)
+                    st_cluster_u64(cluster_map(static_cast<uint32_t>(__cvta_generic_to_shared(cand)), 0) +
+                                       8u * (32u * rank + lane),
+                                   x);
+            }
+            // every rank's keys (or chosen pages) have landed in rank 0
+            // (release / acquire); the other ranks are done with the item
             cluster_sync();
             if (rank != 0) continue;
+            if (fast) {
+                // second stage (rank 0): the 32 largest of the four ranks'
+                // lists; the first want of them are the chosen pages, each
+                // placed by how many chosen pages lie below it
+                const int lane = tid & 31, warp = tid >> 5;
+                static_assert(kTopkSplit == 4, "two merge levels");
+                if (warp < 2) run[0][32 * warp + lane] =
+                    topk_warp_merge_desc(cand[64 * warp + lane], cand[64 * warp + 63 - lane]);
+                __syncthreads();
+                int32_t *dst = p.sel + (row * p.groups + g) * static_cast<int64_t>(p.topk);
+                const int32_t *bt = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+                if (warp == 0) {
+                    const uint64_t x = topk_warp_merge_desc(run[0][lane], run[0][63 - lane]);
+                    const int pg = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(x));
+                    const bool chosen = lane < want;
+                    int below = 0;
+#pragma unroll
+                    for (int s2 = 0; s2 < 32; ++s2) {
+                        const int q = __shfl_sync(0xffffffffu, pg, s2);
+                        below += (s2 < want) & (q < pg);
+                    }
+                    if (chosen) dst[below] = bt[pg];
+                    // the row's last live page (the only partial one) is
+                    // taken when it is forced or chosen
+                    const bool last_taken = forced > 0 || __any_sync(0xffffffffu, chosen && pg == nl - 1);
+                    if (lane == 0) {
+                        p.count[row * p.groups + g] = want + forced;
+                        if (p.tokens) {
+                            const int64_t full = 128 * static_cast<int64_t>(want + forced);
+                            p.tokens[row * p.groups + g] =
+                                static_cast<int32_t>(last_taken ? full - (128 * static_cast<int64_t>(nl) - L) : full);
+                        }
+                    }
+                }
+                // then the forced tail in page order, and -1 up to topk
+                for (int f = tid; f < forced; f += kTopkThreads) dst[want + f] = bt[nc + f];
+                for (int f = want + forced + tid; f < p.topk; f += kTopkThreads) dst[f] = -1;
+                __syncthreads();   // shared state is reused by the next item
+                continue;
+            }
         } else {
             if (p.vec) {
                 const int64_t hstride = p.num_pages >> 2;            // float4 per head

@@ -76,10 +76,13 @@ def test_scorer_then_topk_decode_many_rows():
     _check_chain(w, 6, 1, 1)
 
 
-@pytest.mark.parametrize("P_tokens,offset", [(1100, 0), (4096, 1), (16384, 0)])
+@pytest.mark.parametrize("P_tokens,offset", [(1100, 0), (4096, 1), (16384, 0), (131072, 0), (131072, 1)])
 def test_ties_signed_zeros_and_scalar_path(P_tokens, offset):
     """Integer-valued scores (many ties) with +0 / -0 mixed; P not a multiple
-    of 4 or a misaligned scores pointer take the scalar path."""
+    of 4 or a misaligned scores pointer take the scalar path.  Few items run
+    as clusters: up to 32 chosen pages of at most 1024 candidates take the
+    two-stage select (ties split across the cluster's CTAs), more take the
+    radix select."""
     g = torch.Generator().manual_seed(82 + P_tokens)
     w = W.make_workload("ties", seed=83, q_lens=[3, 6], seq_lens=[P_tokens, P_tokens - 300],
                         prefix_lens=[P_tokens - 3, P_tokens - 306], pool_pages=2 * ((P_tokens + 127) // 128))
@@ -91,7 +94,7 @@ def test_ties_signed_zeros_and_scalar_path(P_tokens, offset):
     base = torch.empty(vals.numel() + offset, dtype=torch.float32, device="cuda")
     scores = base[offset:].view(vals.shape)
     scores.copy_(vals.cuda())
-    for k, local, groups in ((3, 1, 1), (7, 2, 2), (40, 1, 8)):
+    for k, local, groups in ((3, 1, 1), (7, 2, 2), (40, 1, 8), (33, 1, 1), (34, 1, 4), (1024, 1, 1)):
         sel, cnt, tok = _topk_gpu(w, scores, k, local, groups)
         torch.cuda.synchronize()
         ref_sel, ref_cnt, ref_tok = _topk_oracle(w, host, k, local, groups)
