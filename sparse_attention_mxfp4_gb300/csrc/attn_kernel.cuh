@@ -12,16 +12,18 @@
 // 2-CTA clusters, 512 threads a CTA; a cluster takes rows c, c + C, c + 2C,
 // ... (C clusters, at most as many as fit on the GPU at once), each CTA half
 // of each row's pages, so that one row's tail overlaps the next row's
-// copies.  The pages stream: each page's weights are taken against that
-// page's own per-head maximum m_j, P_j = bf16(2^(x - m_j)) with x the score
-// in log2 units, and its PV product goes to its own TMEM accumulator D_j, so
-// no page waits for the scores of a later one.  With sigma_j = sum_t P_j[t]
-// and M = max_j m_j, at the end
-//     out = sum_j 2^(m_j - M) D_j / sum_j 2^(m_j - M) sigma_j,
-// which is the softmax above up to the bf16 rounding of the weights; the
-// two CTAs then combine their halves the same way, each finalising 8 of the
-// 16 heads from the partial output, weight sums and maxima that the peer
-// pushed into its shared memory.  Per CTA:
+// copies.  The pages stream against per-head weight offsets o (x the score
+// in log2 units): P = bf16(2^(x - o)), summed per thread and multiplied
+// into V by the tensor core as each page's QK product lands.  An offset
+// moves up only when some score passes it by more than 2^8 (always on the
+// row's first page): then the weight sums and the PV accumulators are
+// rescaled by 2^(o_old - o_new) in place.  With sigma = sum P and D = sum P V,
+//     out = D / sigma,
+// which is the softmax above up to the bf16 rounding of the weights (each
+// weight is rounded once, whatever the offset); the two CTAs then combine
+// their halves the same way (rescaled to the larger offset), each finalising
+// 8 of the 16 heads from the partial output, weight sums and offsets that
+// the peer pushed into its shared memory.  Per CTA:
 //   warp 4   copies: per page, the K codes (4-D token-permuting TMA view
 //            plus a KV-head dimension, the scorer's smem form) and K scales,
 //            and the V codes and scales as two plain bulk copies (natural
@@ -34,16 +36,16 @@
 //   warps 15, 10  PV MMAs (one thread each, even and odd pages): per page as
 //            soon as its operands are written, kind::f16, A = V^T (M = 128
 //            head dims, K = 128 tokens, bf16, MN-major), B = P^T (N = 16
-//            heads, bf16, MN-major), D = the page's 16 accumulator columns.
+//            heads, bf16, MN-major), D = the warp's 16 accumulator columns.
 //            A warp issues one of these small MMAs every hundred-odd cycles,
 //            so the PV products of a page take two warps to keep up.
 //   warps 0-3 softmax: thread m reads TMEM lane m (token 4(m%32)+m/32 of each
-//            page) as each page's QK product completes, takes the page's
-//            per-head max (redux.sync in the warp, shared memory across the
-//            four warps), writes P^T (bf16, at the token's position: two
-//            16-byte stores) and the warp's per-head sums of the bf16
-//            weights; finally folds the D_j and sigma_j with the factors
-//            2^(m_j - M), and the cluster combine.
+//            page) as each page's QK product completes, tests its scores
+//            against the offsets (one barrier a page; the exact page max
+//            only when an offset moves), writes P^T (bf16, at the token's
+//            position: two 16-byte stores) and adds its weights to its
+//            per-head sums; at the row's end the sums over the CTA, the two
+//            accumulators and the cluster combine.
 //   warps 6-9, 11-14 widen each page's V into V^T (bf16, natural token
 //            order), two (token, 32-dim scale group) cells a thread.
 #pragma once
@@ -70,17 +72,22 @@ constexpr int kAttnN = 16;              // query heads per KV head (fewer are ze
 constexpr int kAttnKStages = 4;
 constexpr int kAttnVStages = 4;         // V pages load from the start, alongside the K pages
 constexpr int kAttnPvBufs = 3;          // V^T / P^T operand buffers: widening runs up to 3 pages ahead of PV
-// The CTA's g-th page (counted over all its rows) uses slot g % kAttnSlots.
-// A QK product into a slot comes only after the softmax has read the scores
-// of the page 7 before it (K and V copies go in step, V waits on the
-// widening, the widening on PV, PV on the softmax), and a row's PV products
-// only after the softmax has folded the row before, so 12 slots are never
-// overwritten early.
+// The CTA's g-th page (counted over all its rows) uses score slot
+// g % kAttnSlots.  A QK product into a slot comes only after the softmax has
+// read the scores of the page 7 before it (K and V copies go in step, V
+// waits on the widening, the widening on PV, PV on the softmax), so 12 slots
+// are never overwritten early.  The PV products of the even and of the odd
+// pages accumulate in one accumulator each; a row's first product of each
+// overwrites it, and comes only after the softmax has read the row before.
 constexpr uint32_t kAttnSCol = 0;                                     // scores of slot i: 16 columns at 16 i
-constexpr uint32_t kAttnAccCol = kAttnSlots * kAttnN;                 // 192: PV accumulator of slot i at + 16 i
-constexpr uint32_t kAttnSfaCol = kAttnAccCol + kAttnSlots * kAttnN;   // 384: K scales, 4 per slot
-constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnSlots;        // 432: unit Q scales
+constexpr uint32_t kAttnAccCol = kAttnSlots * kAttnN;                 // 192: even-page and odd-page accumulators
+constexpr uint32_t kAttnSfaCol = kAttnAccCol + 2 * kAttnN;            // 224: K scales, 4 per slot
+constexpr uint32_t kAttnSfbCol = kAttnSfaCol + 4 * kAttnSlots;        // 272: unit Q scales
 static_assert(kAttnSfbCol + 4 <= 512, "attention TMEM budget");
+// Weight offsets: a head's offset moves up only when a score passes it by
+// more than this (log2 units), so every weight stays below 2^8.
+constexpr float kAttnOffsetSlack = 8.0f;
+constexpr float kAttnNoOffset = -3.0e38f;   // a row's offsets before its first score (below every finite one)
 static_assert(kAttnKStages == kAttnVStages, "one copy warp runs the K and V stages in step");
 static_assert(kAttnCtaPages <= 32, "the copy warp holds a row's page ids one per lane");
 
@@ -112,9 +119,8 @@ struct AttnSmem {
     static constexpr uint32_t kQ = kPt + kAttnPvBufs * 4096;             // 2 x (16 x 128 B), by row parity
     static constexpr uint32_t kUnit = kQ + 2 * 2048;                     // 512 B of 0x7F
     static constexpr uint32_t kRed = kUnit + 512;                        // [2][16 heads][4 warps] warp maxima
-    static constexpr uint32_t kPmax = kRed + 2 * 16 * 4 * 4;             // [page][16] page maxima, then factors
-    static constexpr uint32_t kPsum = kPmax + kAttnCtaPages * 16 * 4;    // [page][16][4 warps] weight sums
-    static constexpr uint32_t kFin = kPsum + kAttnCtaPages * 16 * 4 * 4; // this CTA's 16 sums, then 16 maxima
+    static constexpr uint32_t kPsum = kRed + 2 * 16 * 4 * 4;             // [16 heads][4 warps] weight sums
+    static constexpr uint32_t kFin = kPsum + 16 * 4 * 4;                 // this CTA's 16 sums, then 16 offsets
     static constexpr uint32_t kComb = kFin + 2 * 16 * 4;                 // 2 x from the peer (by row parity)
     static constexpr uint32_t kBars = kComb + 2 * (128 * 8 * 4 + 2 * 16 * 4);
     // kfull[4] kempty[4] vfull[4] vempty[4] qready[2] qfree[2] sready[12] pvready[3] pvfree[3] pv_done qk_done
@@ -127,7 +133,7 @@ struct AttnSmem {
 };
 static_assert(AttnSmem::kAlloc <= 227 * 1024, "attention shared memory budget");
 static_assert(AttnSmem::kComb % 16 == 0 && AttnSmem::kRed % 16 == 0 && AttnSmem::kPsum % 16 == 0 &&
-                  AttnSmem::kPmax % 16 == 0 && AttnSmem::kQ % 1024 == 0 && AttnSmem::kBars % 8 == 0,
+                  AttnSmem::kQ % 1024 == 0 && AttnSmem::kBars % 8 == 0,
               "attention shared memory alignment");
 
 // Instruction descriptors.  QK (kind::mxf8f6f4): A = E2M1 (5, bits 7..9),
@@ -163,6 +169,22 @@ __device__ __forceinline__ bool epi_bar_and(bool pred)
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
         "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+// Named barrier 1 over the 4 softmax warps that also ORs a predicate across
+// them.
+__device__ __forceinline__ bool epi_bar_or(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 128, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"(static_cast<uint32_t>(pred))
@@ -532,25 +554,26 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 const int64_t mine = warp == 15 ? 0 : 1;
                 done_b = pv_fin(static_cast<int>(mine));
                 PageRing<kAttnPvBufs> brg;
-                PageRing<kAttnSlots> srg;
                 for (int64_t item = item0; item < p.num_items && ok; item += nclus, ++k) {
                     const AttnItem it = attn_item(p, item, rank);
                     int issued = 0;
-                    for (int j = 0; j < it.npages; ++j, ++g, brg.next(), srg.next()) {
+                    const uint32_t d = tmem_base + kAttnAccCol + kAttnN * static_cast<uint32_t>(mine);
+                    for (int j = 0; j < it.npages; ++j, ++g, brg.next()) {
                         if ((g & 1) != mine) continue;
+                        // the row's first product overwrites the accumulator
+                        const uint32_t acc_in = issued > 0 ? 1u : 0u;
                         ++issued;
                         const int b = brg.idx;
                         if (!(ok = wait_bounded(pvready(b), brg.ph, abort_flag, kSiteAttnMma))) break;
                         tc_fence_after();
                         const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
                         const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
-                        const uint32_t d = tmem_base + kAttnAccCol + kAttnN * static_cast<uint32_t>(srg.idx);
 #pragma unroll
                         for (uint32_t ks = 0; ks < 8; ++ks) {
                             // K step of 16 tokens: two 8-token groups of each operand
                             const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
                             const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
-                            tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : 0u);
+                            tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : acc_in);
                         }
                         tc_commit(pvfree(b));
                     }
@@ -598,7 +621,6 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         const int tok_m = token_of_col(m);               // token of lane m within each page
         const int G = p.groups;
         float *red = reinterpret_cast<float *>(smem + AttnSmem::kRed);
-        float *pmax = reinterpret_cast<float *>(smem + AttnSmem::kPmax);
         float *psum = reinterpret_cast<float *>(smem + AttnSmem::kPsum);
         float *fin = reinterpret_cast<float *>(smem + AttnSmem::kFin);
         // Q of a row (16 rows x 128 B, SW128) into buffer qb, then qready
@@ -635,7 +657,14 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                     stage_q(item + nclus, static_cast<int>(kn & 1));
             }
             const int64_t g0 = g;
-            const int slot0 = srg.idx;
+            // the row's per-head weight offsets (the same in every thread)
+            // and this thread's per-head sums of its tokens' bf16 weights
+            float mo[kAttnN], S[kAttnN];
+#pragma unroll
+            for (int h = 0; h < kAttnN; ++h) {
+                mo[h] = kAttnNoOffset;
+                S[h] = 0.0f;
+            }
             for (int j = 0; j < it.npages && ok; ++j, ++g, brg.next(), srg.next()) {
                 const int b = brg.idx;
                 const uint32_t slot = static_cast<uint32_t>(srg.idx);
@@ -643,36 +672,82 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                                                                        pvfree(b), brg.ph ^ 1u, abort_flag, kSiteAttnEpi));
                 const bool valid = (it.pbase + j) * kPage + tok_m < it.ctx;
                 float x[16];
+                bool need = false;
                 if (okw) {
                     tc_fence_after();
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * slot, v);
-                    float wm = 0.0f;
 #pragma unroll
                     for (int h = 0; h < kAttnN; ++h) {
                         x[h] = valid ? __uint_as_float(v[h]) * sl : -INFINITY;
-                        const float r = warp_max(x[h]);
-                        wm = hl == h ? r : wm;
+                        need |= h < G && x[h] - mo[h] > kAttnOffsetSlack;
+                    }
+                }
+                // One barrier a page: the four warps leave together after a
+                // failed wait, and raise the offsets together when a score
+                // passed its head's offset by more than the slack (always on
+                // a row's first page).
+                if (epi_bar_or(need || !okw)) {
+                    float wm = 0.0f;
+                    if (okw) {
+#pragma unroll
+                        for (int h = 0; h < kAttnN; ++h) {
+                            const float r = warp_max(x[h]);
+                            wm = hl == h ? r : wm;
+                        }
                     }
                     if (lane < kAttnN) red[((j & 1) * 16 + lane) * 4 + warp] = wm;
+                    ok = epi_bar_and(okw);
+                    if (!ok) break;
+                    // the page's max of head hl over the four warps; each
+                    // head's offset becomes the larger of it and the old one,
+                    // and what was summed against the old offset is rescaled
+                    const float4 r4 = reinterpret_cast<const float4 *>(red)[(j & 1) * 16 + hl];
+                    const float mh = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
+                    float f[kAttnN];
+#pragma unroll
+                    for (int h = 0; h < kAttnN; ++h) {
+                        const float mn = fmaxf(mo[h], __shfl_sync(0xffffffffu, mh, h));
+                        f[h] = ex2_approx(mo[h] - mn);
+                        mo[h] = mn;
+                        S[h] *= f[h];
+                    }
+                    if (j > 0) {
+                        // the PV accumulators, once every product issued so
+                        // far (those of pages g - 1 and g - 2, one from each
+                        // PV warp) has completed; the next product is issued
+                        // only after this page's P^T, below
+                        const int b1 = b > 0 ? b - 1 : kAttnPvBufs - 1;
+                        const uint32_t ph1 = b > 0 ? brg.ph : brg.ph ^ 1u;
+                        const int b2 = b > 1 ? b - 2 : b + 1;
+                        const uint32_t ph2 = b > 1 ? brg.ph : brg.ph ^ 1u;
+                        const bool okp = __all_sync(
+                            0xffffffffu, wait_bounded(pvfree(b1), ph1, abort_flag, kSiteAttnEpi) &&
+                                             (g < 2 || wait_bounded(pvfree(b2), ph2, abort_flag, kSiteAttnEpi)));
+                        ok = epi_bar_and(okp);
+                        if (!ok) break;
+                        tc_fence_after();
+                        uint32_t a[2][16];
+                        tmem_ld2_32x32b_x16(tmem_base + lane_addr + kAttnAccCol,
+                                            tmem_base + lane_addr + kAttnAccCol + kAttnN, a[0], a[1]);
+                        uint32_t o[32];
+#pragma unroll
+                        for (int h = 0; h < kAttnN; ++h) {
+                            o[h] = __float_as_uint(__uint_as_float(a[0][h]) * f[h]);
+                            o[kAttnN + h] = __float_as_uint(__uint_as_float(a[1][h]) * f[h]);
+                        }
+                        tmem_st_32x32b_x32(tmem_base + lane_addr + kAttnAccCol, o);
+                        tc_fence_before();
+                    }
                 }
-                ok = epi_bar_and(okw);
-                if (!ok) break;
-                // the page's max of head hl over the four warps, then every head's
-                const float4 r4 = reinterpret_cast<const float4 *>(red)[(j & 1) * 16 + hl];
-                const float mh = fmaxf(fmaxf(r4.x, r4.y), fmaxf(r4.z, r4.w));
-                if (warp == 0 && lane < kAttnN) pmax[j * 16 + lane] = mh;
                 uint32_t w[8];
-                float ps[16];
 #pragma unroll
                 for (int h2 = 0; h2 < 8; ++h2) {
-                    const float m0 = __shfl_sync(0xffffffffu, mh, 2 * h2);
-                    const float m1 = __shfl_sync(0xffffffffu, mh, 2 * h2 + 1);
-                    const float p0 = valid && 2 * h2 < G ? ex2_approx(x[2 * h2] - m0) : 0.0f;
-                    const float p1 = valid && 2 * h2 + 1 < G ? ex2_approx(x[2 * h2 + 1] - m1) : 0.0f;
+                    const float p0 = valid && 2 * h2 < G ? ex2_approx(x[2 * h2] - mo[2 * h2]) : 0.0f;
+                    const float p1 = valid && 2 * h2 + 1 < G ? ex2_approx(x[2 * h2 + 1] - mo[2 * h2 + 1]) : 0.0f;
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                    ps[2 * h2] = __low2float(pb);
-                    ps[2 * h2 + 1] = __high2float(pb);
+                    S[2 * h2] += __low2float(pb);
+                    S[2 * h2 + 1] += __high2float(pb);
                     w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
                 }
                 uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(tok_m);
@@ -682,26 +757,20 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(pvready(b));
-                // this warp's per-head sums of the bf16 weights (lanes 2 h, 2 h + 1
-                // hold head h)
-                const float wsum = warp_sum16(ps, lane);
-                if ((lane & 1) == 0) psum[(j * 16 + (lane >> 1)) * 4 + warp] = wsum;
+            }
+            // the CTA's weight sum and offset per head (threads 0-15)
+            {
+                const float wsum = warp_sum16(S, lane);      // lanes 2 h, 2 h + 1 hold head h
+                if ((lane & 1) == 0) psum[(lane >> 1) * 4 + warp] = wsum;
             }
             epi_bar_sync();
-            // per head (threads 0-15): M = max_j m_j, the page factors
-            // 2^(m_j - M) (in place of the maxima) and the CTA's weight sum
-            const int nj = ok ? it.npages : 0;
             if (m < kAttnN) {
-                float M = -INFINITY, S = 0.0f;
-                for (int j = 0; j < nj; ++j) M = fmaxf(M, pmax[j * 16 + m]);
-                for (int j = 0; j < nj; ++j) {
-                    const float f = ex2_approx(pmax[j * 16 + m] - M);
-                    const float4 s4 = reinterpret_cast<const float4 *>(psum)[j * 16 + m];
-                    pmax[j * 16 + m] = f;
-                    S += f * ((s4.x + s4.y) + (s4.z + s4.w));
-                }
-                fin[m] = S;
-                fin[kAttnN + m] = M;
+                float om = 0.0f;
+#pragma unroll
+                for (int h = 0; h < kAttnN; ++h) om = m == h ? mo[h] : om;
+                const float4 s4 = reinterpret_cast<const float4 *>(psum)[m];
+                fin[m] = ok ? (s4.x + s4.y) + (s4.z + s4.w) : 0.0f;
+                fin[kAttnN + m] = om;
             }
             // this row's PV products: a PV warp without pages in the row
             // does not commit, the softmax arrives in its place (every row's
@@ -715,37 +784,22 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(pv_done, static_cast<uint32_t>(k) & 1u, abort_flag,
                                                               kSiteAttnEpi));
             epi_bar_sync();
-            // lane m of the accumulators holds head dim m of every head
+            // lane m of the accumulators holds head dim m of every head: the
+            // even pages' and the odd pages' products (each only if the row
+            // had such a page)
             float acc[kAttnN];
 #pragma unroll
             for (int h = 0; h < kAttnN; ++h) acc[h] = 0.0f;
             if (ok && it.npages > 0) {
                 tc_fence_after();
-                for (int j0 = 0; j0 < it.npages; j0 += 2) {
-                    uint32_t v[2][16];
-                    int s0 = slot0 + j0, s1 = s0 + 1;
-                    s0 -= s0 >= kAttnSlots ? kAttnSlots : 0;
-                    s0 -= s0 >= kAttnSlots ? kAttnSlots : 0;
-                    s1 -= s1 >= kAttnSlots ? kAttnSlots : 0;
-                    s1 -= s1 >= kAttnSlots ? kAttnSlots : 0;
-                    tmem_ld2_32x32b_x16(tmem_base + lane_addr + kAttnAccCol + kAttnN * static_cast<uint32_t>(s0),
-                                        tmem_base + lane_addr + kAttnAccCol + kAttnN * static_cast<uint32_t>(s1), v[0],
-                                        v[1]);
+                uint32_t a[2][16];
+                tmem_ld2_32x32b_x16(tmem_base + lane_addr + kAttnAccCol, tmem_base + lane_addr + kAttnAccCol + kAttnN,
+                                    a[0], a[1]);
+                const bool use_even = it.npages >= 2 || (g0 & 1) == 0;
+                const bool use_odd = it.npages >= 2 || (g0 & 1) == 1;
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        if (j0 + jj < it.npages) {
-                            const float4 *f4 = reinterpret_cast<const float4 *>(pmax) + (j0 + jj) * 4;
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                const float4 f = f4[q4];
-                                acc[4 * q4 + 0] = fmaf(__uint_as_float(v[jj][4 * q4 + 0]), f.x, acc[4 * q4 + 0]);
-                                acc[4 * q4 + 1] = fmaf(__uint_as_float(v[jj][4 * q4 + 1]), f.y, acc[4 * q4 + 1]);
-                                acc[4 * q4 + 2] = fmaf(__uint_as_float(v[jj][4 * q4 + 2]), f.z, acc[4 * q4 + 2]);
-                                acc[4 * q4 + 3] = fmaf(__uint_as_float(v[jj][4 * q4 + 3]), f.w, acc[4 * q4 + 3]);
-                            }
-                        }
-                    }
-                }
+                for (int h = 0; h < kAttnN; ++h)
+                    acc[h] = (use_even ? __uint_as_float(a[0][h]) : 0.0f) + (use_odd ? __uint_as_float(a[1][h]) : 0.0f);
             }
             // Combine the two halves: rank r finalises heads 8r .. 8r+7.
             // Each CTA pushes the peer's heads of its accumulator ([dim][8

@@ -146,3 +146,33 @@ def test_attn_persistent_rows_of_every_length():
     empty = np.array(ctx) == 0
     assert (got[empty] == 0).all()
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 4e-3
+
+
+@pytest.mark.parametrize("pattern", ["rising", "falling", "spike", "zigzag"])
+def test_attn_offsets_move_within_a_row(pattern):
+    """K scale bytes set by each page's position within its CTA's half of the
+    row, so that the scores of later pages pass the earlier ones by far more
+    than 2^8 (log2 units): the per-head weight offsets then move up mid-row
+    (every page for "rising", every other page for "zigzag", once for
+    "spike", only on the first page for "falling"), and each move rescales
+    the weight sums and both PV accumulators in TMEM.  Garbage past the
+    context stays as drawn."""
+    rows, kvh, width = 6, 2, 16
+    ctx = [2048, 1921, 1000, 129, 2048, 1500]
+    c = W.make_attn_case(f"offsets-{pattern}", seed=140, rows=rows, kv_heads=kvh, groups=16, width=width,
+                         ctx=ctx, scale_lo=121, scale_hi=123)
+    kp = c.k_pool.clone()
+    for r in range(rows):
+        for h in range(kvh):
+            n = int(c.context_lens[r, h])
+            npg = (n + 127) // 128
+            half = (npg + 1) // 2
+            for i in range(npg):
+                pos = i if i < half else i - half
+                b = {"rising": 122 + 2 * pos, "falling": 136 - 2 * pos, "spike": 136 if pos == 3 else 122,
+                     "zigzag": 122 + 2 * pos if pos % 2 == 0 else 121}[pattern]
+                nt = min(128, n - 128 * i)
+                pg = int(c.block_table[r, h, i])
+                kp[pg, h, W.DATA_BYTES:W.DATA_BYTES + 4 * nt] = b
+    c = dataclasses.replace(c, k_pool=kp)
+    _check(c)
