@@ -781,8 +781,11 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 const int has_odd = n >= 2 || (n == 1 && (g0 & 1) == 1);
                 for (int i = has_even + has_odd; i < 2; ++i) mbar_arrive(pv_done);
             }
-            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(pv_done, static_cast<uint32_t>(k) & 1u, abort_flag,
-                                                              kSiteAttnEpi));
+            // (the result is made the group's: a warp whose wait ran out must
+            // not run fewer named barriers than the others in the next row)
+            const bool pv_ok = !ok || __all_sync(0xffffffffu, wait_bounded(pv_done, static_cast<uint32_t>(k) & 1u,
+                                                                           abort_flag, kSiteAttnEpi));
+            ok = epi_bar_and(ok && pv_ok);
             epi_bar_sync();
             // lane m of the accumulators holds head dim m of every head: the
             // even pages' and the odd pages' products (each only if the row
@@ -821,8 +824,9 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 st_async_v4_u32(pc + 32u * m + 16u, __float_as_uint(a8[4]), __float_as_uint(a8[5]),
                                 __float_as_uint(a8[6]), __float_as_uint(a8[7]), pbar);
                 if (m < 2 * kAttnN) st_async_u32(pc + 4096u + 4u * m, __float_as_uint(fin[m]), pbar);
-                if (__all_sync(0xffffffffu, wait_bounded(comb_ready(cb), static_cast<uint32_t>(k >> 1) & 1u,
-                                                         abort_flag, kSiteAttnEpi))) {
+                const bool comb_ok = __all_sync(0xffffffffu, wait_bounded(comb_ready(cb), static_cast<uint32_t>(k >> 1) & 1u,
+                                                                         abort_flag, kSiteAttnEpi));
+                if (comb_ok) {
                     const float *cm = reinterpret_cast<const float *>(smem + AttnSmem::kComb + cb * kCombBytes);
                     const float4 c0 = reinterpret_cast<const float4 *>(cm)[2 * m];
                     const float4 c1 = reinterpret_cast<const float4 *>(cm)[2 * m + 1];
@@ -842,10 +846,12 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                         if (h < G) o[h * kDim + m] = __float2bfloat16_rn(sum > 0.0f ? __fdividef(a, sum) : 0.0f);
                     }
                 }
-                // every thread has read this buffer, fin and the factors: the
-                // buffer's barrier is re-armed for the row after next
+                // every thread has read this buffer and fin: the buffer's
+                // barrier is re-armed for the row after next (only once its
+                // phase has completed; after a wait that ran out the CTA is
+                // aborting and every later wait gives up at once)
                 epi_bar_sync();
-                if (m == 0) mbar_arrive_expect_tx(comb_ready(cb), kCombBytes);
+                if (m == 0 && comb_ok) mbar_arrive_expect_tx(comb_ready(cb), kCombBytes);
             }
         }
     }
