@@ -220,13 +220,24 @@ __device__ __forceinline__ float warp_sum16(const float (&x)[16], int lane)
     return d + __shfl_xor_sync(0xffffffffu, d, 1);
 }
 
-// Maximum over the 32 lanes of a warp, in every lane (NaN inputs are
-// ignored, like fmaxf).
-__device__ __forceinline__ float warp_max(float v)
+// Maximum of 16 per-head values over the 32 lanes of a warp by halving, as
+// warp_sum16: lane l ends with head (l >> 1) & 15 (NaN inputs are ignored,
+// like fmaxf).
+__device__ __forceinline__ float warp_max16(const float (&x)[16], int lane)
 {
-    float r;
-    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-    return r;
+    float a[8], b[4], c[2];
+    const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        a[i] = fmaxf(u4 ? x[i + 8] : x[i], __shfl_xor_sync(0xffffffffu, u4 ? x[i] : x[i + 8], 16));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        b[i] = fmaxf(u3 ? a[i + 4] : a[i], __shfl_xor_sync(0xffffffffu, u3 ? a[i] : a[i + 4], 8));
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        c[i] = fmaxf(u2 ? b[i + 2] : b[i], __shfl_xor_sync(0xffffffffu, u2 ? b[i] : b[i + 2], 4));
+    const float d = fmaxf(u1 ? c[1] : c[0], __shfl_xor_sync(0xffffffffu, u1 ? c[0] : c[1], 2));
+    return fmaxf(d, __shfl_xor_sync(0xffffffffu, d, 1));
 }
 
 // Wait for bar0 and, when need1, bar1 as well: one probe of both first (one
@@ -688,15 +699,9 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 // passed its head's offset by more than the slack (always on
                 // a row's first page).
                 if (epi_bar_or(need || !okw)) {
-                    float wm = 0.0f;
-                    if (okw) {
-#pragma unroll
-                        for (int h = 0; h < kAttnN; ++h) {
-                            const float r = warp_max(x[h]);
-                            wm = hl == h ? r : wm;
-                        }
-                    }
-                    if (lane < kAttnN) red[((j & 1) * 16 + lane) * 4 + warp] = wm;
+                    // the warp's max of each head (lanes 2 h, 2 h + 1 hold head h)
+                    const float wm = okw ? warp_max16(x, lane) : 0.0f;
+                    if ((lane & 1) == 0) red[((j & 1) * 16 + (lane >> 1)) * 4 + warp] = wm;
                     ok = epi_bar_and(okw);
                     if (!ok) break;
                     // the page's max of head hl over the four warps; each

@@ -15,6 +15,7 @@
 #include "writer_kernel.cuh"
 #include "topk_kernel.cuh"
 #include "attn_kernel.cuh"
+#include "attn_rows_kernel.cuh"
 
 namespace {
 
@@ -46,7 +47,8 @@ struct DeviceState {
     int sm_count = 0;
     bool topk_attr_set[2] = {false, false};
     bool attn_attr_set = false;
-    int attn_clusters = 0;          // attention clusters resident at once on the device
+    int attn_clusters = 0;          // single-group attention clusters resident at once on the device
+    int attn_rows_clusters = 0;     // two-group attention clusters resident at once on the device
     bool smem_attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 
@@ -623,27 +625,35 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
         return MX4_ERR_MISALIGNED;
 
     int dev = 0;
-    int max_clusters = 0;
+    int max_clusters = 0, rows_clusters = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX4_ERR_CUDA;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         DeviceState &st = g_dev[dev];
         if (!st.attn_attr_set) {
             if (cudaFuncSetAttribute(mx4::mx4_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(mx4::AttnSmem::kAlloc)) != cudaSuccess)
+                                     static_cast<int>(mx4::AttnSmem::kAlloc)) != cudaSuccess ||
+                cudaFuncSetAttribute(mx4::mx4_attn_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(mx4::ArSmem::kAlloc)) != cudaSuccess)
                 return MX4_ERR_CUDA;
-            // how many 2-CTA clusters of this kernel fit on the device at once
+            // how many 2-CTA clusters of each kernel fit on the device at once
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(mx4::kAttnSplit, 1, 1);
             cfg.blockDim = dim3(mx4::kAttnThreads, 1, 1);
             cfg.dynamicSmemBytes = mx4::AttnSmem::kAlloc;
-            int n = 0;
+            int n = 0, nr = 0;
             if (cudaOccupancyMaxActiveClusters(&n, mx4::mx4_attn_kernel, &cfg) != cudaSuccess || n < 1)
                 return MX4_ERR_CUDA;
+            cfg.blockDim = dim3(mx4::kArThreads, 1, 1);
+            cfg.dynamicSmemBytes = mx4::ArSmem::kAlloc;
+            if (cudaOccupancyMaxActiveClusters(&nr, mx4::mx4_attn_rows_kernel, &cfg) != cudaSuccess || nr < 1)
+                return MX4_ERR_CUDA;
             st.attn_clusters = n;
+            st.attn_rows_clusters = nr;
             st.attn_attr_set = true;
         }
         max_clusters = st.attn_clusters;
+        rows_clusters = st.attn_rows_clusters;
     }
     alignas(64) CUtensorMap tmap_k;
     alignas(64) CUtensorMap tmap_ks;
@@ -674,14 +684,22 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     p.softmax_scale = softmax_scale;
     p.num_items = num_rows * kv_heads;
     // clusters of kAttnSplit CTAs, at most as many as are resident at once;
-    // cluster c takes the (row, KV head) items c, c + clusters, ...
-    const int64_t clusters = p.num_items < max_clusters ? p.num_items : max_clusters;
+    // cluster c takes the (row, KV head) items c, c + clusters, ...  When every
+    // cluster gets at most one item, the single-group kernel runs; with more
+    // items than clusters, the two-group kernel overlaps one item's softmax
+    // with the next one's.
     cudaGetLastError();
-    // (the cluster shape comes from the kernel's own attribute)
-    if (launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(clusters * mx4::kAttnSplit),
-                  mx4::kAttnThreads, mx4::AttnSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k,
-                  tmap_ks, p) != cudaSuccess)
-        return MX4_ERR_CUDA;
+    // (the cluster shape comes from the kernels' own attribute)
+    cudaError_t e;
+    if (p.num_items <= max_clusters) {
+        e = launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(p.num_items * mx4::kAttnSplit), mx4::kAttnThreads,
+                      mx4::AttnSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k, tmap_ks, p);
+    } else {
+        const int64_t clusters = p.num_items < rows_clusters ? p.num_items : rows_clusters;
+        e = launch_ex(mx4::mx4_attn_rows_kernel, static_cast<unsigned>(clusters * mx4::kAttnSplit), mx4::kArThreads,
+                      mx4::ArSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k, tmap_ks, p);
+    }
+    if (e != cudaSuccess) return MX4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;
 }
 

@@ -95,8 +95,8 @@ def test_scorer_wait_runs_out_and_reports(libs, kind, site):
     _scorer_ok(w, case)
 
 
-def _attn_case():
-    ac = W.make_attn_case("stall-a", seed=43, rows=3, kv_heads=1, groups=16, width=5)
+def _attn_case(rows):
+    ac = W.make_attn_case(f"stall-a{rows}", seed=43, rows=rows, kv_heads=1, groups=16, width=5)
     dev = dict(q=ac.q.cuda(), k=ac.k_pool.cuda(), v=ac.v_pool.cuda(), bt=ac.block_table.cuda(),
                ctx=ac.context_lens.cuda())
     return ac, dev
@@ -120,10 +120,13 @@ def _attn_ok(ac, d):
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 4e-3
 
 
+# 3 rows: one item a cluster (single-group kernel); 200 rows: more items than
+# clusters (the kernel that overlaps consecutive items)
+@pytest.mark.parametrize("rows", [3, 200])
 @pytest.mark.parametrize("site", ATTN_SITES)
-def test_attention_wait_runs_out_and_reports(libs, site):
+def test_attention_wait_runs_out_and_reports(libs, site, rows):
     product, test = libs
-    ac, d = _attn_case()
+    ac, d = _attn_case(rows)
     mx4._lib = test
     try:
         assert _status(test) == 0
