@@ -88,6 +88,9 @@ static_assert(kAttnSfbCol + 4 <= 512, "attention TMEM budget");
 // more than this (log2 units), so every weight stays below 2^8.
 constexpr float kAttnOffsetSlack = 8.0f;
 constexpr float kAttnNoOffset = -3.0e38f;   // a row's offsets before its first score (below every finite one)
+// the offset of a head past `groups`: its zero query row scores 0, which this
+// offset turns into a weight of 0 and never raises
+constexpr float kAttnMuted = 3.0e38f;
 static_assert(kAttnKStages == kAttnVStages, "one copy warp runs the K and V stages in step");
 static_assert(kAttnCtaPages <= 32, "the copy warp holds a row's page ids one per lane");
 
@@ -673,7 +676,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             float mo[kAttnN], S[kAttnN];
 #pragma unroll
             for (int h = 0; h < kAttnN; ++h) {
-                mo[h] = kAttnNoOffset;
+                mo[h] = h < G ? kAttnNoOffset : kAttnMuted;
                 S[h] = 0.0f;
             }
             for (int j = 0; j < it.npages && ok; ++j, ++g, brg.next(), srg.next()) {
@@ -682,25 +685,41 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 const bool okw = __all_sync(0xffffffffu, wait2_bounded(sready(srg.idx), srg.ph, g >= kAttnPvBufs,
                                                                        pvfree(b), brg.ph ^ 1u, abort_flag, kSiteAttnEpi));
                 const bool valid = (it.pbase + j) * kPage + tok_m < it.ctx;
-                float x[16];
+                // (a page past whose end the context stops has invalid tokens)
+                const bool full = (it.pbase + j + 1) * kPage <= it.ctx;
+                const uint32_t s_addr = tmem_base + lane_addr + kAttnSCol + kAttnN * slot;
+                // y = score in log2 units minus the head's offset (-inf for an
+                // invalid token): one fma a score
+                float y[16];
                 bool need = false;
                 if (okw) {
                     tc_fence_after();
                     uint32_t v[16];
-                    tmem_ld_32x32b_x16(tmem_base + lane_addr + kAttnSCol + kAttnN * slot, v);
+                    tmem_ld_32x32b_x16(s_addr, v);
 #pragma unroll
-                    for (int h = 0; h < kAttnN; ++h) {
-                        x[h] = valid ? __uint_as_float(v[h]) * sl : -INFINITY;
-                        need |= h < G && x[h] - mo[h] > kAttnOffsetSlack;
+                    for (int h = 0; h < kAttnN; ++h) y[h] = fmaf(__uint_as_float(v[h]), sl, -mo[h]);
+                    if (!full) {
+#pragma unroll
+                        for (int h = 0; h < kAttnN; ++h) y[h] = valid ? y[h] : -INFINITY;
                     }
+#pragma unroll
+                    for (int h = 0; h < kAttnN; ++h) need |= y[h] > kAttnOffsetSlack;
                 }
                 // One barrier a page: the four warps leave together after a
                 // failed wait, and raise the offsets together when a score
                 // passed its head's offset by more than the slack (always on
                 // a row's first page).
                 if (epi_bar_or(need || !okw)) {
+                    // the scores themselves again, into y (y lost them against
+                    // the old offsets)
+                    if (okw) {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(s_addr, v);
+#pragma unroll
+                        for (int h = 0; h < kAttnN; ++h) y[h] = valid ? __uint_as_float(v[h]) * sl : -INFINITY;
+                    }
                     // the warp's max of each head (lanes 2 h, 2 h + 1 hold head h)
-                    const float wm = okw ? warp_max16(x, lane) : 0.0f;
+                    const float wm = okw ? warp_max16(y, lane) : 0.0f;
                     if ((lane & 1) == 0) red[((j & 1) * 16 + (lane >> 1)) * 4 + warp] = wm;
                     ok = epi_bar_and(okw);
                     if (!ok) break;
@@ -744,13 +763,16 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                         tmem_st_32x32b_x32(tmem_base + lane_addr + kAttnAccCol, o);
                         tc_fence_before();
                     }
+                    // y against the new offsets (-inf stays -inf)
+#pragma unroll
+                    for (int h = 0; h < kAttnN; ++h) y[h] -= mo[h];
                 }
+                // the weights 2^y (0 for an invalid token and for a head past
+                // `groups`), as bf16, and their sums
                 uint32_t w[8];
 #pragma unroll
                 for (int h2 = 0; h2 < 8; ++h2) {
-                    const float p0 = valid && 2 * h2 < G ? ex2_approx(x[2 * h2] - mo[2 * h2]) : 0.0f;
-                    const float p1 = valid && 2 * h2 + 1 < G ? ex2_approx(x[2 * h2 + 1] - mo[2 * h2 + 1]) : 0.0f;
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2_approx(y[2 * h2]), ex2_approx(y[2 * h2 + 1]));
                     S[2 * h2] += __low2float(pb);
                     S[2 * h2 + 1] += __high2float(pb);
                     w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
