@@ -333,8 +333,12 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
 #pragma unroll
                         for (int h = 0; h < kAttnN; ++h) y[h] = valid ? y[h] : -INFINITY;
                     }
+                    float ym[8];
 #pragma unroll
-                    for (int h = 0; h < kAttnN; ++h) need |= y[h] > kAttnOffsetSlack;
+                    for (int h = 0; h < 8; ++h) ym[h] = fmaxf(y[2 * h], y[2 * h + 1]);
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) ym[h] = fmaxf(ym[2 * h], ym[2 * h + 1]);
+                    need = fmaxf(fmaxf(ym[0], ym[1]), fmaxf(ym[2], ym[3])) > kAttnOffsetSlack;
                 }
                 // One barrier a page: the four warps leave together after a
                 // failed wait, and raise the offsets together when a score
@@ -390,13 +394,14 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                     for (int h = 0; h < kAttnN; ++h) y[h] -= mo[h];
                 }
                 // the weights 2^y (0 for an invalid token and for a head past
-                // `groups`), as bf16, and their sums
+                // `groups`): their sums in fp32, the operand in bf16
                 uint32_t w[8];
 #pragma unroll
                 for (int h2 = 0; h2 < 8; ++h2) {
-                    const __nv_bfloat162 pb = __floats2bfloat162_rn(ex2_approx(y[2 * h2]), ex2_approx(y[2 * h2 + 1]));
-                    S[2 * h2] += __low2float(pb);
-                    S[2 * h2 + 1] += __high2float(pb);
+                    const float p0 = ex2_approx(y[2 * h2]), p1 = ex2_approx(y[2 * h2 + 1]);
+                    S[2 * h2] += p0;
+                    S[2 * h2 + 1] += p1;
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                     w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
                 }
                 uint8_t *pt = smem + ArSmem::kPt + (kArPtBufs * grp + pb) * 4096 + pt_offset(tok_m);
