@@ -391,9 +391,10 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
     if (threadIdx.x == 0) {
         // arrivals: TMA / commits count 1; the 4 softmax warps arrive on
         // qready and pvready, the 8 widening warps on vempty and pvready;
-        // pv_done takes two a row: a commit from each PV warp that had pages
-        // in the row, the softmax arriving for one that had none (so that
-        // neither runs a phase ahead of the softmax's wait)
+        // pvfree takes a commit from each PV warp (each issues half of every
+        // page's products); pv_done takes two a row: a commit from each PV
+        // warp when the row has pages, else two arrivals of the softmax (so
+        // that neither runs a phase ahead of the softmax's wait)
         for (int i = 0; i < kAttnKStages; ++i) {
             mbar_init(kfull(i), 1);
             mbar_init(kempty(i), 1);
@@ -409,7 +410,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
         for (int i = 0; i < kAttnSlots; ++i) mbar_init(sready(i), 1);
         for (int i = 0; i < kAttnPvBufs; ++i) {
             mbar_init(pvready(i), 4 + kAttnWidenWarps);
-            mbar_init(pvfree(i), 1);
+            mbar_init(pvfree(i), 2);
         }
         mbar_init(pv_done, 2);
         mbar_init(qk_done, 1);
@@ -563,35 +564,35 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                     tc_commit(qfree(qb));
                 }
             } else {
-                // page g waits here only after page g - 2 was ready, hence
-                // page g - 3 (the previous phase of its buffer's barrier) too
+                // Both PV warps take every page, warp 15 its first 64 tokens
+                // (K steps 0-3) into the first accumulator and warp 10 its
+                // last 64 into the second, so that a page's products take
+                // half the issue time; the accumulators are added at the
+                // row's end.
                 const int64_t mine = warp == 15 ? 0 : 1;
                 done_b = pv_fin(static_cast<int>(mine));
                 PageRing<kAttnPvBufs> brg;
                 for (int64_t item = item0; item < p.num_items && ok; item += nclus, ++k) {
                     const AttnItem it = attn_item(p, item, rank);
-                    int issued = 0;
                     const uint32_t d = tmem_base + kAttnAccCol + kAttnN * static_cast<uint32_t>(mine);
                     for (int j = 0; j < it.npages; ++j, ++g, brg.next()) {
-                        if ((g & 1) != mine) continue;
-                        // the row's first product overwrites the accumulator
-                        const uint32_t acc_in = issued > 0 ? 1u : 0u;
-                        ++issued;
                         const int b = brg.idx;
                         if (!(ok = wait_bounded(pvready(b), brg.ph, abort_flag, kSiteAttnMma))) break;
                         tc_fence_after();
                         const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
                         const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
 #pragma unroll
-                        for (uint32_t ks = 0; ks < 8; ++ks) {
+                        for (uint32_t i = 0; i < 4; ++i) {
                             // K step of 16 tokens: two 8-token groups of each operand
+                            const uint32_t ks = 4u * static_cast<uint32_t>(mine) + i;
                             const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
                             const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
-                            tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : acc_in);
+                            // (the row's first product overwrites the accumulator)
+                            tc_mma_f16_ss(d, a, bd, kAttnIdescPv, (i > 0 || j > 0) ? 1u : 0u);
                         }
                         tc_commit(pvfree(b));
                     }
-                    if (ok && issued > 0) tc_commit(pv_done);   // this warp's PV products of the row are done
+                    if (ok && it.npages > 0) tc_commit(pv_done);   // this warp's PV products of the row are done
                 }
             }
             // every product issued above completes before TMEM is read or
@@ -670,7 +671,6 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                                                                    abort_flag, kSiteAttnEpi)))
                     stage_q(item + nclus, static_cast<int>(kn & 1));
             }
-            const int64_t g0 = g;
             // the row's per-head weight offsets (the same in every thread)
             // and this thread's per-head sums of its tokens' bf16 weights
             float mo[kAttnN], S[kAttnN];
@@ -742,16 +742,13 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                     }
                     if (j > 0) {
                         // the PV accumulators, once every product issued so
-                        // far (those of pages g - 1 and g - 2, one from each
-                        // PV warp) has completed; the next product is issued
-                        // only after this page's P^T, below
+                        // far has completed: both PV warps' commits of page
+                        // g - 1 (each tracks all of its warp's earlier
+                        // products); the next product is issued only after
+                        // this page's P^T, below
                         const int b1 = b > 0 ? b - 1 : kAttnPvBufs - 1;
                         const uint32_t ph1 = b > 0 ? brg.ph : brg.ph ^ 1u;
-                        const int b2 = b > 1 ? b - 2 : b + 1;
-                        const uint32_t ph2 = b > 1 ? brg.ph : brg.ph ^ 1u;
-                        const bool okp = __all_sync(
-                            0xffffffffu, wait_bounded(pvfree(b1), ph1, abort_flag, kSiteAttnEpi) &&
-                                             (g < 2 || wait_bounded(pvfree(b2), ph2, abort_flag, kSiteAttnEpi)));
+                        const bool okp = __all_sync(0xffffffffu, wait_bounded(pvfree(b1), ph1, abort_flag, kSiteAttnEpi));
                         ok = epi_bar_and(okp);
                         if (!ok) break;
                         tc_fence_after();
@@ -804,14 +801,12 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 fin[m] = ok ? (s4.x + s4.y) + (s4.z + s4.w) : 0.0f;
                 fin[kAttnN + m] = om;
             }
-            // this row's PV products: a PV warp without pages in the row
-            // does not commit, the softmax arrives in its place (every row's
+            // this row's PV products: in a row without pages the PV warps do
+            // not commit, the softmax arrives in their place (every row's
             // phase is waited for, so the parities stay in step)
-            if (m == 0) {
-                const int n = it.npages;
-                const int has_even = n >= 2 || (n == 1 && (g0 & 1) == 0);
-                const int has_odd = n >= 2 || (n == 1 && (g0 & 1) == 1);
-                for (int i = has_even + has_odd; i < 2; ++i) mbar_arrive(pv_done);
+            if (m == 0 && it.npages == 0) {
+                mbar_arrive(pv_done);
+                mbar_arrive(pv_done);
             }
             // (the result is made the group's: a warp whose wait ran out must
             // not run fewer named barriers than the others in the next row)
@@ -820,8 +815,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
             ok = epi_bar_and(ok && pv_ok);
             epi_bar_sync();
             // lane m of the accumulators holds head dim m of every head: the
-            // even pages' and the odd pages' products (each only if the row
-            // had such a page)
+            // products of the pages' first and last 64 tokens
             float acc[kAttnN];
 #pragma unroll
             for (int h = 0; h < kAttnN; ++h) acc[h] = 0.0f;
@@ -830,11 +824,8 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                 uint32_t a[2][16];
                 tmem_ld2_32x32b_x16(tmem_base + lane_addr + kAttnAccCol, tmem_base + lane_addr + kAttnAccCol + kAttnN,
                                     a[0], a[1]);
-                const bool use_even = it.npages >= 2 || (g0 & 1) == 0;
-                const bool use_odd = it.npages >= 2 || (g0 & 1) == 1;
 #pragma unroll
-                for (int h = 0; h < kAttnN; ++h)
-                    acc[h] = (use_even ? __uint_as_float(a[0][h]) : 0.0f) + (use_odd ? __uint_as_float(a[1][h]) : 0.0f);
+                for (int h = 0; h < kAttnN; ++h) acc[h] = __uint_as_float(a[0][h]) + __uint_as_float(a[1][h]);
             }
             // Combine the two halves: rank r finalises heads 8r .. 8r+7.
             // Each CTA pushes the peer's heads of its accumulator ([dim][8
