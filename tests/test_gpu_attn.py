@@ -185,3 +185,26 @@ def test_attn_offsets_move_within_a_row(pattern, rows):
                 kp[pg, h, W.DATA_BYTES:W.DATA_BYTES + 4 * nt] = b
     c = dataclasses.replace(c, k_pool=kp)
     _check_listed(c)
+
+
+def _leftover_case(name, seed, rows, kvh, width=16):
+    """Seeded case whose row contexts mix 0, 1, 129, 300, 383, 1000 and full
+    rows with random lengths (the same for a row's KV heads)."""
+    g = torch.Generator().manual_seed(seed)
+    special = [0, 1, 129, 300, 383, width * 128, 1000]
+    ctx = [special[r % len(special)] if r % 3 == 0 else
+           int(torch.randint(0, width * 128 + 1, (1,), generator=g)) for r in range(rows)]
+    return W.make_attn_case(name, seed=seed, rows=rows, kv_heads=kvh, groups=16, width=width,
+                            pool_pages=rows * kvh * width, ctx=ctx)
+
+
+@pytest.mark.parametrize("rows,kvh", [(77, 1), (79, 1), (151, 1), (233, 1), (64, 4)])
+def test_attn_rows_past_whole_rounds(rows, kvh):
+    """More rows x KV heads than clusters (76 on GB300) with a last round
+    that is not whole: 77 (one cluster takes a second row), 79, 151 (all but
+    one cluster take two), 233, 64 x 4 = 256.  Contexts ragged: empty rows,
+    rows of one to three pages, full rows."""
+    c = _leftover_case(f"left{rows}x{kvh}", 150 + rows, rows, kvh)
+    got = _check_listed(c)
+    empty = c.context_lens.numpy() == 0
+    assert (got[empty] == 0).all()
