@@ -96,6 +96,11 @@ static_assert(kAttnCtaPages <= 32, "the copy warp holds a row's page ids one per
 
 enum AttnSite : uint32_t { kSiteAttnProducer = 6, kSiteAttnMma = 7, kSiteAttnEpi = 8 };
 
+// P^T operand layout steps (see pt_offset below)
+constexpr uint32_t kPtLbo = 144;
+constexpr uint32_t kPtSbo = 2304;
+constexpr uint32_t kPtBytes = 2 * kPtSbo;               // one P^T buffer
+
 struct AttnParams {
     const uint8_t *q;                 // e4m3 [rows, kv_heads, groups, 128]
     const uint8_t *v_data;
@@ -118,8 +123,8 @@ struct AttnSmem {
     static constexpr uint32_t kV = kKs + kAttnKStages * kScaleBytes;     // V codes, natural order
     static constexpr uint32_t kVs = kV + kAttnVStages * kDataBytes;      // V scales
     static constexpr uint32_t kVt = ((kVs + kAttnVStages * kScaleBytes) + 1023) & ~1023u;   // 3 x 32 KB
-    static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // 3 x 4 KB
-    static constexpr uint32_t kQ = kPt + kAttnPvBufs * 4096;             // 2 x (16 x 128 B), by row parity
+    static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // 3 x 4.5 KB
+    static constexpr uint32_t kQ = (kPt + kAttnPvBufs * kPtBytes + 1023) & ~1023u;   // 2 x (16 x 128 B), by row parity
     static constexpr uint32_t kUnit = kQ + 2 * 2048;                     // 512 B of 0x7F
     static constexpr uint32_t kRed = kUnit + 512;                        // [2][16 heads][4 warps] warp maxima
     static constexpr uint32_t kPsum = kRed + 2 * 16 * 4 * 4;             // [16 heads][4 warps] weight sums
@@ -154,12 +159,17 @@ constexpr uint32_t kAttnIdescPv =
 
 // Both PV operands are MN-major without swizzling: an 8 x 8 core matrix is
 // 8 tokens of 16 bytes (8 bf16 along M or N), 128 contiguous bytes; core
-// matrices follow each other every 128 B along M / N (the stride offset)
-// and every LBO bytes along K (the leading offset):
-//   P^T (N = 16 heads):  byte 256 (t / 8) + 128 (h / 8) + 16 (t % 8) + 2 (h % 8), LBO 256
-//   V^T (M = 128 dims):  byte 2048 (t / 8) + 128 (d / 8) + 16 (t % 8) + 2 (d % 8), LBO 2048
-// One MMA (K = 16) takes two groups of 8 tokens of each.
-__device__ __forceinline__ uint32_t pt_offset(int t) { return 256u * (t >> 3) + 16u * (t & 7); }
+// matrices follow each other every SBO bytes along M / N (the stride
+// offset) and every LBO bytes along K (the leading offset):
+//   P^T (N = 16 heads):  byte 144 (t / 8) + 2304 (h / 8) + 16 (t % 8) + 2 (h % 8), LBO 144, SBO 2304
+//   V^T (M = 128 dims):  byte 2048 (t / 8) + 128 (d / 8) + 16 (t % 8) + 2 (d % 8), LBO 2048, SBO 128
+// One MMA (K = 16) takes two groups of 8 tokens of each.  The 144-byte step
+// of P^T (a 16-byte gap after each core matrix) keeps the softmax threads'
+// 16-byte stores free of bank conflicts: the 8 lanes of a quarter warp hold
+// tokens 8 (4 q + j / 2) + 4 (j % 2) + w, whose stores then fall in 8
+// distinct 16-byte bank groups (with a 256-byte step they fell in 2).  The
+// steps are kPtLbo and kPtSbo.
+__device__ __forceinline__ uint32_t pt_offset(int t) { return kPtLbo * (t >> 3) + 16u * (t & 7); }
 
 __device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -580,13 +590,13 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                         if (!(ok = wait_bounded(pvready(b), brg.ph, abort_flag, kSiteAttnMma))) break;
                         tc_fence_after();
                         const uint32_t vt = sbase + AttnSmem::kVt + b * 32768u;
-                        const uint32_t pt = sbase + AttnSmem::kPt + b * 4096u;
+                        const uint32_t pt = sbase + AttnSmem::kPt + b * kPtBytes;
 #pragma unroll
                         for (uint32_t i = 0; i < 4; ++i) {
                             // K step of 16 tokens: two 8-token groups of each operand
                             const uint32_t ks = 4u * static_cast<uint32_t>(mine) + i;
                             const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
-                            const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
+                            const uint64_t bd = smem_desc(pt + ks * (2 * kPtLbo), kPtLbo, kPtSbo, 0);
                             // (the row's first product overwrites the accumulator)
                             tc_mma_f16_ss(d, a, bd, kAttnIdescPv, (i > 0 || j > 0) ? 1u : 0u);
                         }
@@ -779,9 +789,9 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kAttnThread
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                     w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
                 }
-                uint8_t *pt = smem + AttnSmem::kPt + b * 4096 + pt_offset(tok_m);
+                uint8_t *pt = smem + AttnSmem::kPt + b * kPtBytes + pt_offset(tok_m);
                 *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                *reinterpret_cast<uint4 *>(pt + kPtSbo) = make_uint4(w[4], w[5], w[6], w[7]);
                 // P^T visible to the tensor core
                 fence_proxy_async_smem();
                 __syncwarp();

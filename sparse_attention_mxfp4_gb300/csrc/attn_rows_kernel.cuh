@@ -54,8 +54,8 @@ struct ArSmem {
     static constexpr uint32_t kV = kKs + kArKStages * kScaleBytes;     // V codes, natural order
     static constexpr uint32_t kVs = kV + kArVStages * kDataBytes;      // V scales
     static constexpr uint32_t kVt = ((kVs + kArVStages * kScaleBytes) + 1023) & ~1023u;   // kAttnPvBufs x 32 KB
-    static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // [group][2] x 4 KB
-    static constexpr uint32_t kQ = kPt + 2 * kArPtBufs * 4096;         // 2 x (16 x 128 B), by row parity
+    static constexpr uint32_t kPt = kVt + kAttnPvBufs * 32768;           // [group][2] x 4.5 KB
+    static constexpr uint32_t kQ = (kPt + 2 * kArPtBufs * kPtBytes + 1023) & ~1023u;   // 2 x (16 x 128 B), by row parity
     static constexpr uint32_t kUnit = kQ + 2 * 2048;                     // 512 B of 0x7F
     static constexpr uint32_t kRed = kUnit + 512;                        // [group][2][16 heads][4 warps] warp maxima
     static constexpr uint32_t kPsum = kRed + 2 * 2 * 16 * 4 * 4;         // [row parity][group][16 heads][4 warps] sums
@@ -404,9 +404,9 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                     const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
                     w[h2] = *reinterpret_cast<const uint32_t *>(&pb);
                 }
-                uint8_t *pt = smem + ArSmem::kPt + (kArPtBufs * grp + pb) * 4096 + pt_offset(tok_m);
+                uint8_t *pt = smem + ArSmem::kPt + (kArPtBufs * grp + pb) * kPtBytes + pt_offset(tok_m);
                 *reinterpret_cast<uint4 *>(pt) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4 *>(pt + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                *reinterpret_cast<uint4 *>(pt + kPtSbo) = make_uint4(w[4], w[5], w[6], w[7]);
                 // P^T visible to the tensor core
                 fence_proxy_async_smem();
                 if (await_free) {
@@ -704,12 +704,12 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                             tc_fence_after();
                             const uint32_t vt = sbase + ArSmem::kVt + b * 32768u;
                             const uint32_t pt = sbase + ArSmem::kPt + (kArPtBufs * static_cast<uint32_t>(mine) +
-                                                                         static_cast<uint32_t>(pb)) * 4096u;
+                                                                         static_cast<uint32_t>(pb)) * kPtBytes;
 #pragma unroll
                             for (uint32_t ks = 0; ks < 8; ++ks) {
                                 // K step of 16 tokens: two 8-token groups of each operand
                                 const uint64_t a = smem_desc(vt + ks * 4096u, 2048, 128, 0);
-                                const uint64_t bd = smem_desc(pt + ks * 512u, 256, 128, 0);
+                                const uint64_t bd = smem_desc(pt + ks * (2 * kPtLbo), kPtLbo, kPtSbo, 0);
                                 tc_mma_f16_ss(d, a, bd, kAttnIdescPv, ks > 0 ? 1u : acc_in);
                             }
                             tc_commit(pvfree(b));
