@@ -338,14 +338,14 @@ struct AttnItem {
     int ctx, npages, pbase, kvh;
 };
 
-__device__ __forceinline__ AttnItem attn_item(const AttnParams &p, int64_t item, uint32_t rank)
+__device__ __forceinline__ AttnItem attn_item(const AttnParams &p, int64_t item, uint32_t rank, int split = kAttnSplit)
 {
     AttnItem it;
     int ctx = p.context_lens[item];
     if (ctx > p.width * kPage) ctx = p.width * kPage;
     if (ctx < 0) ctx = 0;
     const int all = (ctx + kPage - 1) / kPage;
-    const int half = (all + 1) / 2;
+    const int half = split == 1 ? all : (all + 1) / 2;
     it.ctx = ctx;
     it.pbase = rank == 0 ? 0 : half;
     it.npages = rank == 0 ? half : all - half;

@@ -21,7 +21,10 @@
 // the one-group kernel: faster when clusters stream several rows
 // (pa-decode-4kvh 37.7 -> 35.3 us), slower for one row a cluster (pa-decode
 // 11.8 -> 12.1 us), so the host picks it only when there are more rows than
-// clusters.
+// clusters.  It runs in two forms: rows split over a 2-CTA cluster as in
+// attn_kernel.cuh (kSplit = 2), or whole rows on single CTAs (kSplit = 1:
+// twice the units, no combine, half the row transitions a CTA; 256 rows of
+// 16 pages: 32.7 -> 30.1 us); the host takes the one with fewer pages a CTA.
 //
 // Every barrier is waited for in each of its phases, in order, by the one
 // role that waits on it, and none can complete a phase ahead of that role:
@@ -47,6 +50,7 @@ constexpr uint32_t kArSfaCol = kArAccCol + 4 * kAttnN;              // 256
 constexpr uint32_t kArSfbCol = kArSfaCol + 4 * kAttnSlots;          // 304
 static_assert(kArSfbCol + 4 <= 512, "attention TMEM budget (rows kernel)");
 static_assert(kArKStages == kArVStages, "the copy warp arms K and V stage s together");
+static_assert(kAttnMaxPages <= 32, "the copy warp holds a whole row's page ids one per lane (kSplit = 1)");
 
 struct ArSmem {
     static constexpr uint32_t kK = 0;                                    // K pages, 16 KB each
@@ -120,7 +124,11 @@ __device__ __forceinline__ bool epi_bar_or(uint32_t id, bool pred)
     return r != 0;
 }
 
-__global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads, 1)
+// kSplit: CTAs a row is split over (2: a cluster of 2 launched with the
+// cluster attribute, the halves combined through distributed shared memory;
+// 1: a CTA takes whole rows and writes their output itself).
+template <int kSplit>
+__global__ void __launch_bounds__(kArThreads, 1)
     mx4_attn_rows_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_ks,
                          const __grid_constant__ AttnParams p)
 {
@@ -129,9 +137,9 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
     const uint32_t sbase = smem_u32(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();               // this CTA's half of each row's pages
-    const int64_t item0 = blockIdx.x / kAttnSplit;         // this cluster's first row (row * kv_heads + kv head)
-    const int64_t nclus = gridDim.x / kAttnSplit;          // rows item0, item0 + nclus, ...
+    const uint32_t rank = kSplit == 2 ? cluster_ctarank() : 0u;   // this CTA's half of each row's pages
+    const int64_t item0 = blockIdx.x / kSplit;             // this cluster's first row (row * kv_heads + kv head)
+    const int64_t nclus = gridDim.x / kSplit;              // rows item0, item0 + nclus, ...
 
     auto bar = [&](int i) { return sbase + ArSmem::kBars + 8u * i; };
     auto kfull = [&](int i) { return bar(i); };
@@ -226,7 +234,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
     tc_fence_before();
     __syncthreads();
     // the peer's barriers are initialised before anyone pushes into them
-    cluster_sync();
+    if (kSplit == 2) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<uint32_t *>(smem + ArSmem::kTmemSlot);
 
@@ -279,7 +287,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
         // (the named-barrier syncs below run on every path, so the four
         // warps of a group always pass the same number of them)
         for (int64_t item = item0; item < p.num_items; item += nclus, ++k) {
-            const AttnItem it = attn_item(p, item, rank);
+            const AttnItem it = attn_item(p, item, rank, kSplit);
             // the next row's Q, one row ahead, once QK is done with the buffer
             if (grp == 0 && item + nclus < p.num_items) {
                 const int kn = k + 1;
@@ -461,7 +469,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
         int64_t g = 0;
         int64_t k = 0;
         for (int64_t item = item0; item < p.num_items; item += nclus, ++k) {
-            const AttnItem it = attn_item(p, item, rank);
+            const AttnItem it = attn_item(p, item, rank, kSplit);
             const int pr = static_cast<int>(k & 1);
             const uint32_t par = static_cast<uint32_t>(k >> 1) & 1u;
             const int64_t g0 = g;
@@ -516,7 +524,16 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
             // peer's comb_ready; it then waits for its own, rescales both
             // halves to the larger offset, adds, normalises and stores bf16
             // (a half with no weight contributes nothing).
-            {
+            if (kSplit == 1) {
+                // a whole row: this CTA's sums and accumulators are the row's
+                __nv_bfloat16 *o = p.out + (item * G) * kDim;
+#pragma unroll
+                for (int h = 0; h < kAttnN; ++h) {
+                    const float sum = fin[64 + h];
+                    if (ok && h < G) o[h * kDim + m] = __float2bfloat16_rn(sum > 0.0f ? __fdividef(acc[h], sum) : 0.0f);
+                }
+                epi_bar_sync(3u);        // fin is rewritten for the next row
+            } else {
                 const int cb = static_cast<int>(k & 1);
                 const uint32_t peer = rank ^ 1u;
                 const uint32_t pc = cluster_map(sbase + ArSmem::kComb + cb * kCombBytes, peer);
@@ -581,7 +598,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                 }
                 return id;
             };
-            AttnItem it = attn_item(p, item0, rank);
+            AttnItem it = attn_item(p, item0, rank, kSplit);
             int32_t id = load_ids(item0, it);
             PageRing<kArKStages> krg;
             for (int64_t item = item0; item < p.num_items && ok; item += nclus) {
@@ -590,7 +607,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                 bool fetched = false;
                 auto fetch_next = [&]() {
                     if (!fetched && item + nclus < p.num_items) {
-                        nit = attn_item(p, item + nclus, rank);
+                        nit = attn_item(p, item + nclus, rank, kSplit);
                         nid = load_ids(item + nclus, nit);
                     }
                     fetched = true;
@@ -653,7 +670,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                     PageRing<kArKStages> krg;
                     PageRing<kAttnSlots> srg;
                     for (int64_t item = item0; item < p.num_items && ok; item += nclus, ++k) {
-                        const AttnItem it = attn_item(p, item, rank);
+                        const AttnItem it = attn_item(p, item, rank, kSplit);
                         const int qb = static_cast<int>(k & 1);
                         if (!(ok = wait_bounded(qready(qb), static_cast<uint32_t>(k >> 1) & 1u, abort_flag,
                                                 kSiteAttnMma)))
@@ -687,7 +704,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
                     PageRing<kAttnPvBufs> brg;
                     PageRing<kArPtBufs> prg;
                     for (int64_t item = item0; item < p.num_items && ok; item += nclus, ++k) {
-                        const AttnItem it = attn_item(p, item, rank);
+                        const AttnItem it = attn_item(p, item, rank, kSplit);
                         int issued = 0;
                         const uint32_t d = tmem_base + kArAccCol + kAttnN * static_cast<uint32_t>(2 * (k & 1) + mine);
                         for (int j = 0; j < it.npages; ++j, ++g, brg.next()) {
@@ -735,7 +752,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
             PageRing<kAttnPvBufs> brg;
             PageRing<kArVStages> krg;
             for (int64_t item = item0; item < p.num_items && ok; item += nclus) {
-                const AttnItem it = attn_item(p, item, rank);
+                const AttnItem it = attn_item(p, item, rank, kSplit);
                 for (int j = 0; j < it.npages; ++j, ++g, brg.next(), krg.next()) {
                     const int b = brg.idx, vs = krg.idx;
                     // (a buffer's first use waits for no PV product)
@@ -763,7 +780,7 @@ __global__ void __cluster_dims__(kAttnSplit, 1, 1) __launch_bounds__(kArThreads,
         tmem_dealloc(tmem_base, 512);
     }
     // neither CTA leaves while the other may still write into its shared memory
-    cluster_sync();
+    if (kSplit == 2) cluster_sync();
 }
 
 }  // namespace mx4

@@ -48,7 +48,8 @@ struct DeviceState {
     bool topk_attr_set[2] = {false, false};
     bool attn_attr_set = false;
     int attn_clusters = 0;          // single-group attention clusters resident at once on the device
-    int attn_rows_clusters = 0;     // two-group attention clusters resident at once on the device
+    int attn_rows_clusters = 0;     // two-group attention kernel: 2-CTA clusters resident at once
+    int attn_rows_ctas = 0;         // two-group attention kernel: single CTAs resident at once
     bool smem_attr_set[8] = {false, false, false, false, false, false, false, false};
 };
 
@@ -625,7 +626,7 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
         return MX4_ERR_MISALIGNED;
 
     int dev = 0;
-    int max_clusters = 0, rows_clusters = 0;
+    int max_clusters = 0, rows_clusters = 0, rows_ctas = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MX4_ERR_CUDA;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -633,7 +634,9 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
         if (!st.attn_attr_set) {
             if (cudaFuncSetAttribute(mx4::mx4_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(mx4::AttnSmem::kAlloc)) != cudaSuccess ||
-                cudaFuncSetAttribute(mx4::mx4_attn_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                cudaFuncSetAttribute(mx4::mx4_attn_rows_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(mx4::ArSmem::kAlloc)) != cudaSuccess ||
+                cudaFuncSetAttribute(mx4::mx4_attn_rows_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(mx4::ArSmem::kAlloc)) != cudaSuccess)
                 return MX4_ERR_CUDA;
             // how many 2-CTA clusters of each kernel fit on the device at once
@@ -644,16 +647,32 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
             int n = 0, nr = 0;
             if (cudaOccupancyMaxActiveClusters(&n, mx4::mx4_attn_kernel, &cfg) != cudaSuccess || n < 1)
                 return MX4_ERR_CUDA;
+            // (the two-group kernel takes its cluster shape from the launch)
+            cudaLaunchAttribute cl;
+            cl.id = cudaLaunchAttributeClusterDimension;
+            cl.val.clusterDim.x = mx4::kAttnSplit;
+            cl.val.clusterDim.y = 1;
+            cl.val.clusterDim.z = 1;
             cfg.blockDim = dim3(mx4::kArThreads, 1, 1);
             cfg.dynamicSmemBytes = mx4::ArSmem::kAlloc;
-            if (cudaOccupancyMaxActiveClusters(&nr, mx4::mx4_attn_rows_kernel, &cfg) != cudaSuccess || nr < 1)
+            cfg.attrs = &cl;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&nr, mx4::mx4_attn_rows_kernel<2>, &cfg) != cudaSuccess || nr < 1)
+                return MX4_ERR_CUDA;
+            int per_sm = 0, sms = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mx4::mx4_attn_rows_kernel<1>, mx4::kArThreads,
+                                                              mx4::ArSmem::kAlloc) != cudaSuccess ||
+                per_sm < 1 || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                sms < 1)
                 return MX4_ERR_CUDA;
             st.attn_clusters = n;
             st.attn_rows_clusters = nr;
+            st.attn_rows_ctas = per_sm * sms;
             st.attn_attr_set = true;
         }
         max_clusters = st.attn_clusters;
         rows_clusters = st.attn_rows_clusters;
+        rows_ctas = st.attn_rows_ctas;
     }
     alignas(64) CUtensorMap tmap_k;
     alignas(64) CUtensorMap tmap_ks;
@@ -683,21 +702,29 @@ mx4_status mx4_sparse_pa_decode(const uint8_t *q, int64_t num_rows, int kv_heads
     p.width = block_table_width;
     p.softmax_scale = softmax_scale;
     p.num_items = num_rows * kv_heads;
-    // clusters of kAttnSplit CTAs, at most as many as are resident at once;
-    // cluster c takes the (row, KV head) items c, c + clusters, ...  When every
-    // cluster gets at most one item, the single-group kernel runs; with more
-    // items than clusters, the two-group kernel overlaps one item's softmax
-    // with the next one's.
+    // Persistent launches: cluster (or CTA) c takes the (row, KV head) items
+    // c, c + n, ... .  When every 2-CTA cluster gets at most one item, the
+    // single-group kernel runs.  With more items than that, the two-group
+    // kernel overlaps one item's end with the next one's pages, either on
+    // 2-CTA clusters (each CTA half of every item's pages) or on single CTAs
+    // (whole items, no combine): of the two, the one with fewer pages a CTA,
+    // counted as ceil(items / units) x the pages a unit takes of an item, and
+    // on a tie the one with single CTAs (half the item transitions).
     cudaGetLastError();
-    // (the cluster shape comes from the kernels' own attribute)
     cudaError_t e;
-    if (p.num_items <= max_clusters) {
-        e = launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(p.num_items * mx4::kAttnSplit), mx4::kAttnThreads,
+    const int64_t items = p.num_items;
+    if (items <= max_clusters) {
+        e = launch_ex(mx4::mx4_attn_kernel, static_cast<unsigned>(items * mx4::kAttnSplit), mx4::kAttnThreads,
                       mx4::AttnSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k, tmap_ks, p);
+    } else if (2 * ((items + rows_ctas - 1) / rows_ctas) <= (items + rows_clusters - 1) / rows_clusters) {
+        const int64_t ctas = items < rows_ctas ? items : rows_ctas;
+        e = launch_ex(mx4::mx4_attn_rows_kernel<1>, static_cast<unsigned>(ctas), mx4::kArThreads, mx4::ArSmem::kAlloc,
+                      static_cast<cudaStream_t>(stream), 1, true, tmap_k, tmap_ks, p);
     } else {
-        const int64_t clusters = p.num_items < rows_clusters ? p.num_items : rows_clusters;
-        e = launch_ex(mx4::mx4_attn_rows_kernel, static_cast<unsigned>(clusters * mx4::kAttnSplit), mx4::kArThreads,
-                      mx4::ArSmem::kAlloc, static_cast<cudaStream_t>(stream), 1, true, tmap_k, tmap_ks, p);
+        const int64_t clusters = items < rows_clusters ? items : rows_clusters;
+        e = launch_ex(mx4::mx4_attn_rows_kernel<2>, static_cast<unsigned>(clusters * mx4::kAttnSplit),
+                      mx4::kArThreads, mx4::ArSmem::kAlloc, static_cast<cudaStream_t>(stream),
+                      static_cast<unsigned>(mx4::kAttnSplit), true, tmap_k, tmap_ks, p);
     }
     if (e != cudaSuccess) return MX4_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MX4_OK : MX4_ERR_CUDA;

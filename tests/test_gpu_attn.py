@@ -154,7 +154,7 @@ def test_attn_persistent_rows_of_every_length():
     assert (got[empty] == 0).all()
 
 
-@pytest.mark.parametrize("rows", [6, 96])
+@pytest.mark.parametrize("rows", [6, 64, 96])
 @pytest.mark.parametrize("pattern", ["rising", "falling", "spike", "zigzag"])
 def test_attn_offsets_move_within_a_row(pattern, rows):
     """K scale bytes set by each page's position within its CTA's half of the
@@ -163,9 +163,10 @@ def test_attn_offsets_move_within_a_row(pattern, rows):
     (every page for "rising", every other page for "zigzag", once for
     "spike", only on the first page for "falling"), and each move rescales
     the weight sums and both PV accumulators in TMEM.  Garbage past the
-    context stays as drawn.  With 96 rows of 2 KV heads there are more items
-    than clusters, so the moves also run in the kernel that overlaps the
-    softmax of one item with the next one's."""
+    context stays as drawn.  On GB300 (76 two-CTA clusters, 152 SMs) the 12
+    items of 6 rows x 2 KV heads run in the one-group kernel, the 128 of 64
+    rows in the two-group kernel on single CTAs (whole rows) and the 192 of
+    96 rows in the two-group kernel on 2-CTA clusters."""
     kvh, width = 2, 16
     ctx = [[2048, 1921, 1000, 129, 2048, 1500][r % 6] for r in range(rows)]
     c = W.make_attn_case(f"offsets-{pattern}", seed=140, rows=rows, kv_heads=kvh, groups=16, width=width,
@@ -198,12 +199,13 @@ def _leftover_case(name, seed, rows, kvh, width=16):
                             pool_pages=rows * kvh * width, ctx=ctx)
 
 
-@pytest.mark.parametrize("rows,kvh", [(77, 1), (79, 1), (151, 1), (233, 1), (64, 4)])
+@pytest.mark.parametrize("rows,kvh", [(77, 1), (79, 1), (151, 1), (160, 1), (233, 1), (305, 1), (64, 4)])
 def test_attn_rows_past_whole_rounds(rows, kvh):
-    """More rows x KV heads than clusters (76 on GB300) with a last round
-    that is not whole: 77 (one cluster takes a second row), 79, 151 (all but
-    one cluster take two), 233, 64 x 4 = 256.  Contexts ragged: empty rows,
-    rows of one to three pages, full rows."""
+    """More rows x KV heads than 2-CTA clusters (76 on GB300), with a last
+    round that is not whole.  The host runs the two-group kernel on single
+    CTAs (152 on GB300: 77, 79, 151, 233 and 64 x 4 = 256 items) or on
+    clusters (160, 305), whichever gives fewer pages a CTA.  Contexts ragged:
+    empty rows, rows of one to three pages, full rows."""
     c = _leftover_case(f"left{rows}x{kvh}", 150 + rows, rows, kvh)
     got = _check_listed(c)
     empty = c.context_lens.numpy() == 0

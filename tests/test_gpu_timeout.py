@@ -120,9 +120,10 @@ def _attn_ok(ac, d):
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) < 4e-3
 
 
-# 3 rows: one item a cluster (single-group kernel); 200 rows: more items than
-# clusters (the kernel that overlaps consecutive items)
-@pytest.mark.parametrize("rows", [3, 200])
+# 3 rows: one item a cluster (single-group kernel); 120 and 200 rows: more
+# items than clusters (the two-group kernel, on single CTAs for 120 items and
+# on 2-CTA clusters for 200 on GB300)
+@pytest.mark.parametrize("rows", [3, 120, 200])
 @pytest.mark.parametrize("site", ATTN_SITES)
 def test_attention_wait_runs_out_and_reports(libs, site, rows):
     product, test = libs
